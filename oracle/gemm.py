@@ -165,6 +165,15 @@ def linear_backward(dY, W, X, fp8: str = "e5m2") -> dict:
             "dX": dX, "dX_bound": dX_b, "dW": dW, "dW_bound": dW_b}
 
 
-def within_bound(y, y_ref, bound, rel: float = 2e-3) -> np.ndarray:
-    """Floating-point gate: ``|y - y_ref| <= rel * sum_k |a_s * b_s|``."""
-    return np.abs(_as64(y) - _as64(y_ref)) <= rel * _as64(bound)
+# Half a unit in the last place of a bfloat16 value, relative (8 significant bits).
+BF16_HALF_ULP = 2.0 ** -8
+
+
+def within_bound(y, y_ref, bound, rel: float = 2e-3, out_round: float = 0.0) -> np.ndarray:
+    """Floating-point gate: ``|y - y_ref| <= rel * sum_k |a_s * b_s|``, plus
+    ``out_round * |y_ref|`` for the rounding of the output to a narrower type
+    (``BF16_HALF_ULP`` for bfloat16 outputs: the NKI backward returns
+    bfloat16, and rounding an FP32 result to bfloat16 alone may move it by half
+    a bfloat16 ulp, up to 2**-8 of its magnitude)."""
+    y_ref = _as64(y_ref)
+    return np.abs(_as64(y) - y_ref) <= rel * _as64(bound) + out_round * np.abs(y_ref)

@@ -184,6 +184,18 @@ def test_within_bound_rejects_planted_error():
     assert not G.within_bound(y_ref + 0.021, y_ref, bound).all()
 
 
+def test_bf16_output_rounding_allowance_is_half_an_ulp():
+    """Rounding to bfloat16 may move a value by up to 2**-8 of it: 16447.25
+    rounds to 16384 (spacing 128 there); the allowance admits exactly that and
+    no more."""
+    import torch
+    v = 16447.25
+    r = torch.tensor([v]).to(torch.bfloat16).float().item()
+    assert r == 16384.0
+    assert G.within_bound(np.array([r]), np.array([v]), np.array([0.0]), out_round=G.BF16_HALF_ULP).all()
+    assert not G.within_bound(np.array([r - 1]), np.array([v]), np.array([0.0]), out_round=G.BF16_HALF_ULP).all()
+
+
 def test_dequantize_matches_scaled_operand():
     rng = np.random.default_rng(14)
     x = rng.standard_normal((4, 64)).astype(np.float32)
