@@ -1,0 +1,277 @@
+"""Python binding of libbsmm.so, the block-scaled low-precision GEMM library.
+
+Argument marshalling only: every function here checks nothing the library
+does not check itself, allocates its outputs with torch (device memory is the
+caller's, as the C ABI requires), passes raw device pointers and the current
+torch stream to the C entry point of the same name, and raises
+:class:`BsmmError` on a non-zero status.  All computation happens in the
+library's CUDA kernels; there is no CPU path.  The library is loaded on first
+use and its absence is an error.
+
+Entry points (see ``include/bsmm.h`` for the full contract):
+
+* :func:`quantize`        absmax block quantizer (E4M3/E5M2/E2M1/INT8 codes,
+                          FP32/UE8M0/UE4M3 scales, optional transposed output)
+* :func:`gemm`            batched block-scaled GEMM, MXFP8 or NVFP4
+* :func:`gemm_grouped`    FP8 GEMM with 1x128 / 128x128 FP32 scales
+* :func:`int8_channel`    INT8 per-channel matmul with exact INT32 sums
+* :func:`linear_backward` MXFP8 dX / dW of a linear layer
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "BsmmError", "lib", "library_path", "quantize", "gemm", "gemm_grouped", "int8_channel",
+    "linear_backward", "gemm_workspace_size", "int8_channel_workspace_size",
+    "linear_backward_workspace_size", "check_device_status", "selftest_wait_timeout",
+    "set_wait_timeout_ns", "version",
+    "F32", "BF16", "E4M3", "E5M2", "E2M1", "INT8", "SCALE_F32", "SCALE_UE8M0", "SCALE_UE4M3",
+]
+
+# bsmm_status
+OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(8)
+STATUS_NAMES = ["OK", "INVALID_ARG", "SHAPE", "ALIGNMENT", "UNSUPPORTED", "CUDA", "TIMEOUT", "WORKSPACE"]
+# bsmm_dtype
+F32, BF16, E4M3, E5M2, E2M1, INT8 = range(6)
+# bsmm_scale_type
+SCALE_F32, SCALE_UE8M0, SCALE_UE4M3 = range(3)
+
+_CODE_NAMES = {"e4m3": E4M3, "e5m2": E5M2, "e2m1": E2M1, "int8": INT8}
+_SCALE_NAMES = {"f32": SCALE_F32, "ue8m0": SCALE_UE8M0, "ue4m3": SCALE_UE4M3}
+
+library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libbsmm.so")
+_LIB = None
+
+
+class BsmmError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        self.status = status
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"{where}: BSMM_ERR_{name}: {msg}")
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "bsmm_version": ([], _INT),
+    "bsmm_last_error": ([], ctypes.c_char_p),
+    "bsmm_set_wait_timeout_ns": ([ctypes.c_uint64], None),
+    "bsmm_check_device_status": ([_P, ctypes.POINTER(_INT)], _INT),
+    "bsmm_selftest_wait_timeout": ([ctypes.c_uint64, _P], _INT),
+    "bsmm_quantize": ([_P, _INT, _I64, _I64, _I64, _INT, _INT, _INT, _INT, _INT, _P, _I64, _P, _I64, _P], _INT),
+    "bsmm_gemm_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
+    "bsmm_gemm": ([_I64, _I64, _I64, _I64, _P, _INT, _P, _INT, _P, _I64, _P, _I64, _INT, _P, _INT, _P, _SZ, _P],
+                  _INT),
+    "bsmm_gemm_grouped": ([_I64, _I64, _I64, _P, _INT, _P, _INT, _P, _P, _INT, _INT, _P, _P], _INT),
+    "bsmm_int8_channel_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "bsmm_int8_channel": ([_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _INT),
+    "bsmm_linear_backward_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "bsmm_linear_backward": ([_P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _SZ, _P], _INT),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        h = ctypes.CDLL(library_path)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(h, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = h
+    return _LIB
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise BsmmError(status, where, lib().bsmm_last_error().decode())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _code(c) -> int:
+    return _CODE_NAMES[c] if isinstance(c, str) else int(c)
+
+
+def _scale(s) -> int:
+    return _SCALE_NAMES[s] if isinstance(s, str) else int(s)
+
+
+def version() -> int:
+    return lib().bsmm_version()
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    lib().bsmm_set_wait_timeout_ns(int(ns))
+
+
+def check_device_status(stream=None):
+    """Synchronizes the stream; returns (status, site) of the device status word."""
+    where = ctypes.c_int(0)
+    st = lib().bsmm_check_device_status(_stream(stream), ctypes.byref(where))
+    return st, where.value
+
+
+def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(lib().bsmm_selftest_wait_timeout(int(timeout_ns), _stream(stream)), "bsmm_selftest_wait_timeout")
+
+
+# --------------------------------------------------------------------------- #
+# quantize                                                                    #
+# --------------------------------------------------------------------------- #
+
+def quantize(x: torch.Tensor, block, code="e4m3", scale="f32", transpose=False, codes=None, scales=None,
+             stream=None):
+    """Block-quantize a 2-D float32/bfloat16 CUDA tensor.
+
+    Returns ``(codes, scales)``: codes uint8 (int8 for INT8; E2M1 packed two
+    per byte) of shape [rows, cols] (or [cols, rows] transposed), scales
+    float32 or uint8 of shape [rows/br, cols/bc] (or transposed)."""
+    _dev(x, "x")
+    if x.dim() != 2 or x.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("x must be a 2-D float32 or bfloat16 tensor")
+    br, bc = int(block[0]), int(block[1])
+    c, s = _code(code), _scale(scale)
+    rows, cols = x.shape
+    orows, ocols = (cols, rows) if transpose else (rows, cols)
+    srows, scols = ((cols // bc, rows // br) if transpose else (rows // br, cols // bc)) if br and bc else (0, 0)
+    if codes is None:
+        width = ocols // 2 if c == E2M1 else ocols
+        codes = torch.empty((orows, width), dtype=torch.int8 if c == INT8 else torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((srows, scols), dtype=torch.float32 if s == SCALE_F32 else torch.uint8,
+                             device=x.device)
+    _check(lib().bsmm_quantize(_ptr(x), BF16 if x.dtype == torch.bfloat16 else F32, rows, cols, cols, br, bc, c, s,
+                               1 if transpose else 0, _ptr(codes), ocols, _ptr(scales), scols, _stream(stream)),
+           "bsmm_quantize")
+    return codes, scales
+
+
+# --------------------------------------------------------------------------- #
+# GEMMs                                                                       #
+# --------------------------------------------------------------------------- #
+
+def gemm_workspace_size(B, M, N, K, a_type) -> int:
+    return lib().bsmm_gemm_workspace_size(B, M, N, K, _code(a_type))
+
+
+def gemm(a, b, a_scales, b_scales, a_type="e4m3", b_type="e4m3", scale="ue8m0", out_dtype=torch.float32, y=None,
+         workspace=None, K=None, stream=None):
+    """Batched block-scaled GEMM ``(B,M,K) x (B,N,K) -> (B,M,N)``.
+
+    ``a``/``b`` hold codes (uint8 or float8 tensors; E2M1 packed, so their last
+    dimension is K/2 and ``K`` is inferred as twice it), ``a_scales``
+    (B,M,K_a) / ``b_scales`` (B,N,K_b) hold scale bytes."""
+    for t, n in ((a, "a"), (b, "b"), (a_scales, "a_scales"), (b_scales, "b_scales")):
+        _dev(t, n)
+    at, bt = _code(a_type), _code(b_type)
+    if a.dim() == 2:
+        a, b, a_scales, b_scales = a[None], b[None], a_scales[None], b_scales[None]
+    Bn, M, ka = a.shape
+    N = b.shape[1]
+    if K is None:
+        K = ka * 2 if at == E2M1 else ka
+    if y is None:
+        y = torch.empty((Bn, M, N), dtype=out_dtype, device=a.device)
+    need = gemm_workspace_size(Bn, M, N, K, at)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=a.device)
+    _check(lib().bsmm_gemm(Bn, M, N, K, _ptr(a), at, _ptr(b), bt, _ptr(a_scales), a_scales.shape[-1],
+                           _ptr(b_scales), b_scales.shape[-1], _scale(scale), _ptr(y),
+                           BF16 if y.dtype == torch.bfloat16 else F32, _ptr(workspace), workspace.numel(),
+                           _stream(stream)), "bsmm_gemm")
+    return y
+
+
+def gemm_grouped(a, b, a_scales, b_scales, group_n=128, group_k=128, a_type="e4m3", b_type="e4m3", y=None,
+                 stream=None):
+    """``y[m,n] = sum_kb a_scales[m,kb] * b_scales[n//group_n,kb] * (a.b over block kb)``."""
+    for t, n in ((a, "a"), (b, "b"), (a_scales, "a_scales"), (b_scales, "b_scales")):
+        _dev(t, n)
+    M, K = a.shape
+    N = b.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _check(lib().bsmm_gemm_grouped(M, N, K, _ptr(a), _code(a_type), _ptr(b), _code(b_type), _ptr(a_scales),
+                                   _ptr(b_scales), group_n, group_k, _ptr(y), _stream(stream)),
+           "bsmm_gemm_grouped")
+    return y
+
+
+def int8_channel_workspace_size(B, D_in, D_out) -> int:
+    return lib().bsmm_int8_channel_workspace_size(B, D_in, D_out)
+
+
+def int8_channel(x, w, return_acc=False, out=None, workspace=None, stream=None) -> dict:
+    """INT8 per-channel matmul; returns the dict of the page (w_q, w_scales,
+    x_q, x_scales, y) plus ``acc`` (int32 sums) when ``return_acc``."""
+    _dev(x, "x")
+    _dev(w, "w")
+    Bn, D_in = x.shape
+    D_out = w.shape[1]
+    dev = x.device
+    o = out or {
+        "x_q": torch.empty((Bn, D_in), dtype=torch.int8, device=dev),
+        "x_scales": torch.empty(Bn, dtype=torch.float32, device=dev),
+        "w_q": torch.empty((D_in, D_out), dtype=torch.int8, device=dev),
+        "w_scales": torch.empty(D_out, dtype=torch.float32, device=dev),
+        "y": torch.empty((Bn, D_out), dtype=torch.float32, device=dev),
+    }
+    if return_acc and "acc" not in o:
+        o["acc"] = torch.empty((Bn, D_out), dtype=torch.int32, device=dev)
+    need = int8_channel_workspace_size(Bn, D_in, D_out)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(lib().bsmm_int8_channel(_ptr(x), _ptr(w), Bn, D_in, D_out, _ptr(o["x_q"]), _ptr(o["x_scales"]),
+                                   _ptr(o["w_q"]), _ptr(o["w_scales"]), _ptr(o["y"]), _ptr(o.get("acc")),
+                                   _ptr(workspace), workspace.numel(), _stream(stream)), "bsmm_int8_channel")
+    return o
+
+
+def linear_backward_workspace_size(M, N, K) -> int:
+    return lib().bsmm_linear_backward_workspace_size(M, N, K)
+
+
+def linear_backward(dY, W, X, fp8="e5m2", dX=None, dW=None, workspace=None, stream=None):
+    """MXFP8 backward of ``Y = X @ W^T``: returns ``(dX, dW)`` in bfloat16."""
+    for t, n in ((dY, "dY"), (W, "W"), (X, "X")):
+        _dev(t, n)
+    M, N = dY.shape
+    K = W.shape[1]
+    dev = dY.device
+    if dX is None:
+        dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if dW is None:
+        dW = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    need = linear_backward_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(lib().bsmm_linear_backward(_ptr(dY), _ptr(W), _ptr(X), M, N, K, _code(fp8), _ptr(dX), _ptr(dW),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)), "bsmm_linear_backward")
+    return dX, dW

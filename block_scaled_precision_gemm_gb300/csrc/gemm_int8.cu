@@ -1,0 +1,293 @@
+// INT8 per-channel symmetric matmul (TensorTonic "Int8 Matmul with Per-Channel
+// Scales"): s_x[b] = max_i |x[b,i]|/127, s_w[j] = max_i |w[i,j]|/127 (all-zero
+// line -> 1), codes clip(round(v/s), +-127), a = sum_i x_q*w_q exact in int32,
+// y = float(a) * s_x[b] * s_w[j].
+//
+// tcgen05 has no integer MMA kind on sm_103a, so the matmul runs on the
+// warp-level integer MMA (mma.sync m16n8k32 s8.s8.s32), which accumulates
+// exactly in int32.  Kernels:
+//   i8_quant_rows   one CTA per row of x: absmax, scale, codes into x_q and a
+//                   zero-padded copy [B, Kp] the matmul reads.
+//   i8_colmax       column maxima of w, split over row chunks, combined with
+//                   an integer atomicMax on the (non-negative) float bits.
+//   i8_quant_cols   codes of w in the page's layout [D_in, D_out] and
+//                   transposed [D_out, Kp] through a shared-memory tile.
+//   i8_gemm         128x128 CTA tile, 8 warps of 64x32, 128-byte K steps,
+//                   4-stage cp.async pipeline, XOR-swizzled shared memory.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsmm {
+namespace {
+
+constexpr int kKpAlign = 128;  // padded K (bytes per operand row)
+
+__device__ __forceinline__ float i8_scale(float absmax) {
+  return absmax == 0.f ? 1.f : __fdiv_rn(absmax, 127.f);
+}
+__device__ __forceinline__ int8_t i8_code(float v, float s) {
+  const float q = fminf(fmaxf(__fdiv_rn(v, s), -127.f), 127.f);
+  return static_cast<int8_t>(__float2int_rn(q));
+}
+
+__global__ void __launch_bounds__(256) i8_quant_rows(const float* __restrict__ x, int64_t D, int64_t Kp,
+                                                     int8_t* __restrict__ xq, float* __restrict__ xs,
+                                                     int8_t* __restrict__ xq_pad) {
+  __shared__ float wmax[8];
+  const int64_t r = blockIdx.x;
+  const float* row = x + r * D;
+  float m = 0.f;
+  for (int64_t c = threadIdx.x; c < D; c += 256) m = fmaxf(m, fabsf(__ldg(row + c)));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = wmax[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
+  const float s = i8_scale(m);
+  if (threadIdx.x == 0) xs[r] = s;
+  for (int64_t c = threadIdx.x; c < Kp; c += 256) {
+    const int8_t q = c < D ? i8_code(__ldg(row + c), s) : int8_t(0);
+    if (c < D) xq[r * D + c] = q;
+    xq_pad[r * Kp + c] = q;
+  }
+}
+
+// grid (ceil(D_out/32), row chunks); lane = column, 8 warps stride rows.
+__global__ void __launch_bounds__(256) i8_colmax(const float* __restrict__ w, int64_t D_in, int64_t D_out,
+                                                 int rows_per_cta, unsigned* __restrict__ colmax) {
+  __shared__ float wm[8][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_cta;
+  const int64_t r1 = (D_in < r0 + rows_per_cta) ? D_in : r0 + rows_per_cta;
+  float m = 0.f;
+  if (c < D_out)
+    for (int64_t r = r0 + warp; r < r1; r += 8) m = fmaxf(m, fabsf(__ldg(w + r * D_out + c)));
+  wm[warp][lane] = m;
+  __syncthreads();
+  if (warp == 0 && c < D_out) {
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, wm[i][lane]);
+    atomicMax(colmax + c, __float_as_uint(m));  // non-negative floats order like their bits
+  }
+}
+
+// 64 x 64 tiles of w (rows i over Kp, columns j): codes into w_q[i][j] and
+// wqT[j][i]; rows i >= D_in give zero codes in wqT (the K padding).
+__global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w, int64_t D_in, int64_t D_out,
+                                                     int64_t Kp, const unsigned* __restrict__ colmax,
+                                                     int8_t* __restrict__ wq, float* __restrict__ ws,
+                                                     int8_t* __restrict__ wqT) {
+  __shared__ int8_t tile[64][64 + 4];
+  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * 64, j0 = static_cast<int64_t>(blockIdx.x) * 64;
+  const int t = threadIdx.x;
+  const int jj = t & 63, ig = t >> 6;  // column in tile, row group (16 rows each)
+  const int64_t j = j0 + jj;
+  const float s = j < D_out ? i8_scale(__uint_as_float(colmax[j])) : 1.f;
+  if (blockIdx.y == 0 && ig == 0 && j < D_out) ws[j] = s;
+  for (int k = 0; k < 16; ++k) {
+    const int ii = ig * 16 + k;
+    const int64_t i = i0 + ii;
+    int8_t q = 0;
+    if (i < D_in && j < D_out) {
+      q = i8_code(__ldg(w + i * D_out + j), s);
+      wq[i * D_out + j] = q;
+    }
+    tile[ii][jj] = q;
+  }
+  __syncthreads();
+  // transposed write: thread -> (row j of wqT, 16 consecutive i)
+  const int jt = t >> 2, part = t & 3;
+  const int64_t jrow = j0 + jt;
+  if (jrow < D_out) {
+    const int64_t ibase = i0 + part * 16;
+    if (ibase < Kp) {
+      uint32_t word[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        word[g] = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          word[g] |= static_cast<uint32_t>(static_cast<uint8_t>(tile[part * 16 + 4 * g + b][jt])) << (8 * b);
+      }
+      *reinterpret_cast<uint4*>(wqT + jrow * Kp + ibase) = make_uint4(word[0], word[1], word[2], word[3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- the matmul
+constexpr int GM = 128, GN = 128, GK = 128, GSTAGES = 4;
+constexpr int G_STAGE_BYTES = (GM + GN) * GK;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_s8(int (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// 16-byte chunk `c` of row `r` in a [rows][128 B] tile, XOR-swizzled.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
+  return base + r * GK + ((c ^ (r & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(256) i8_gemm(const int8_t* __restrict__ A, const int8_t* __restrict__ Bt, int M,
+                                               int N, int Kp, const float* __restrict__ sx,
+                                               const float* __restrict__ sw, float* __restrict__ y,
+                                               int32_t* __restrict__ acc_out) {
+  extern __shared__ __align__(128) uint8_t gsm[];
+  const uint32_t sbase = smem_u32(gsm);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
+  const int ktiles = Kp / GK;
+
+  auto load_stage = [&](int st, int kt) {
+    const uint32_t sa = sbase + st * G_STAGE_BYTES, sb = sa + GM * GK;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // 1024 chunks of A, 1024 of B; 4 + 4 per thread
+      const int idx = t + 256 * i;
+      const int r = idx >> 3, c = idx & 7;
+      const int gm = m0 + r, gn = n0 + r;
+      const int8_t* pa = A + static_cast<int64_t>(gm < M ? gm : 0) * Kp + kt * GK + c * 16;
+      const int8_t* pb = Bt + static_cast<int64_t>(gn < N ? gn : 0) * Kp + kt * GK + c * 16;
+      cp_async16(swz(sa, r, c), pa, gm < M ? 16 : 0);
+      cp_async16(swz(sb, r, c), pb, gn < N ? 16 : 0);
+    }
+  };
+
+  int acc[4][4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[a][b][c] = 0;
+
+#pragma unroll
+  for (int st = 0; st < GSTAGES - 1; ++st) {
+    if (st < ktiles) load_stage(st, st);
+    cp_async_commit();
+  }
+  const int wm = warp >> 2, wn = warp & 3;  // warp tile rows wm*64, cols wn*32
+  for (int kt = 0; kt < ktiles; ++kt) {
+    cp_async_wait<GSTAGES - 2>();
+    __syncthreads();
+    {
+      const int nk = kt + GSTAGES - 1;
+      if (nk < ktiles) load_stage(nk % GSTAGES, nk);
+      cp_async_commit();
+    }
+    const uint32_t sa = sbase + (kt % GSTAGES) * G_STAGE_BYTES, sb = sa + GM * GK;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {  // 32-byte K steps
+      uint32_t af[4][4], bf[4][2];
+#pragma unroll
+      for (int mi = 0; mi < 4; ++mi) {
+        const int r = wm * 64 + mi * 16 + (lane & 15);
+        const int c = 2 * kk + (lane >> 4);
+        ldmatrix_x4(swz(sa, r, c), af[mi][0], af[mi][1], af[mi][2], af[mi][3]);
+      }
+#pragma unroll
+      for (int nj = 0; nj < 2; ++nj) {
+        const int r = wn * 32 + nj * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int c = 2 * kk + ((lane >> 3) & 1);
+        ldmatrix_x4(swz(sb, r, c), bf[2 * nj][0], bf[2 * nj][1], bf[2 * nj + 1][0], bf[2 * nj + 1][1]);
+      }
+#pragma unroll
+      for (int mi = 0; mi < 4; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) mma_s8(acc[mi][ni], af[mi], bf[ni][0], bf[ni][1]);
+    }
+  }
+  cp_async_wait<0>();
+
+  const int gr = lane >> 2, tc = lane & 3;
+#pragma unroll
+  for (int mi = 0; mi < 4; ++mi) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = m0 + wm * 64 + mi * 16 + gr + 8 * h;
+      if (row >= M) continue;
+      const float srow = sx[row];
+#pragma unroll
+      for (int ni = 0; ni < 4; ++ni) {
+        const int col = n0 + wn * 32 + ni * 8 + 2 * tc;
+        const int a0 = acc[mi][ni][2 * h], a1 = acc[mi][ni][2 * h + 1];
+        const int64_t o = static_cast<int64_t>(row) * N + col;
+        if (col + 1 < N) {
+          const float y0 = (static_cast<float>(a0) * srow) * sw[col];
+          const float y1 = (static_cast<float>(a1) * srow) * sw[col + 1];
+          if ((N & 1) == 0) {
+            *reinterpret_cast<float2*>(y + o) = make_float2(y0, y1);
+            if (acc_out) *reinterpret_cast<int2*>(acc_out + o) = make_int2(a0, a1);
+          } else {
+            y[o] = y0;
+            y[o + 1] = y1;
+            if (acc_out) {
+              acc_out[o] = a0;
+              acc_out[o + 1] = a1;
+            }
+          }
+        } else if (col < N) {
+          y[o] = (static_cast<float>(a0) * srow) * sw[col];
+          if (acc_out) acc_out[o] = a0;
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+size_t int8_workspace_bytes(int64_t B, int64_t D_in, int64_t D_out) {
+  const int64_t Kp = ceil_div(D_in, kKpAlign) * kKpAlign;
+  return align_up(static_cast<size_t>(D_out) * 4, 256) + align_up(static_cast<size_t>(B) * Kp, 256) +
+         align_up(static_cast<size_t>(D_out) * Kp, 256);
+}
+
+cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  const int64_t Kp = ceil_div(r.D_in, kKpAlign) * kKpAlign;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(r.workspace);
+  unsigned* colmax = reinterpret_cast<unsigned*>(ws);
+  int8_t* xq_pad = reinterpret_cast<int8_t*>(ws + align_up(static_cast<size_t>(r.D_out) * 4, 256));
+  int8_t* wqT = xq_pad + align_up(static_cast<size_t>(r.B) * Kp, 256);
+
+  cudaError_t e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(r.D_out) * 4, s);
+  if (e != cudaSuccess) return e;
+  i8_quant_rows<<<static_cast<unsigned>(r.B), 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xq_pad);
+  {
+    const int rows_per_cta = 256;
+    dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 32)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
+    i8_colmax<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
+  }
+  {
+    dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 64)), static_cast<unsigned>(Kp / 64));
+    i8_quant_cols<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales, wqT);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int smem = GSTAGES * G_STAGE_BYTES;
+  e = cudaFuncSetAttribute(i8_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, GN)), static_cast<unsigned>(ceil_div(r.B, GM)));
+  i8_gemm<<<grid, 256, smem, s>>>(xq_pad, wqT, static_cast<int>(r.B), static_cast<int>(r.D_out),
+                                  static_cast<int>(Kp), r.x_scales, r.w_scales, r.y, r.acc);
+  return cudaGetLastError();
+}
+
+}  // namespace bsmm

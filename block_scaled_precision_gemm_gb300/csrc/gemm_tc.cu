@@ -1,0 +1,621 @@
+// Block-scaled GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// One persistent, warp-specialised kernel template serves three paths:
+//
+//   kF32Scale  y[m,n] = sum_kb sa[m,kb] * sb[n/128,kb] * (a . b over K block kb)
+//              (atrex-bench #002 block_scaled_mm, Reference Implementation).
+//              FP8 x FP8 -> FP32 partial per 128-K block in tensor memory
+//              (kind::f8f6f4); the epilogue warps read each partial with
+//              tcgen05.ld and promote it into FP32 registers with sa*sb.
+//              Partials are double-buffered so the MMA runs a block ahead.
+//   kMXF8      y = sum_k a*2^(ea-127) * b*2^(eb-127), UE8M0 scale per 32 K
+//              (jax.nn.scaled_matmul, Notes: MXFP8 on Blackwell).  Hardware
+//              block scaling (kind::mxf8f6f4.block_scale.block32), scales
+//              staged into tensor memory with tcgen05.cp.
+//   kNVF4      packed E2M1 operands, UE4M3 scale per 16 K (Notes: NVFP4),
+//              kind::mxf4nvf4.block_scale.block16.
+//
+// CTA: 384 threads.  warp 0 issues TMA loads (A, B and scale-factor atoms)
+// into a STAGES-deep shared-memory ring; warp 1 issues the MMAs from one
+// thread; warp 2 owns the tensor-memory allocation; warps 4..11 are the
+// epilogue (two warpgroups, each owning half of the tile's columns; warp w
+// reads TMEM lanes 32*(w%4)..+31 = rows of the tile).  Output tiles leave
+// through a swizzled staging buffer and TMA stores.  Tiles are visited in
+// groups of kGroupM M-tiles so the operands a wave touches stay in L2.
+//
+// Every wait is bounded (mbar_wait); on expiry the kernel records the site,
+// drains its own copies and MMAs, frees its tensor memory and returns.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsmm {
+namespace {
+
+enum Mode { kF32Scale = 0, kMXF8 = 1, kNVF4 = 2 };
+
+constexpr int BM = 128;          // rows per tile (TMEM lanes)
+constexpr int BK_BYTES = 128;    // K bytes per stage: 128 FP8 or 256 FP4 elements
+constexpr int kThreads = 384;
+constexpr int kEpiWarps = 8;
+constexpr int kTmemCols = 512;
+constexpr int kGroupM = 16;
+constexpr int kStagingPerWarp = 2 * 4096;  // two 32-row x 128-byte buffers
+
+enum Site { kSiteProducer = 1, kSiteMmaTmem = 2, kSiteMmaFull = 3, kSiteEpilogue = 4, kSiteDrain = 5,
+            kSiteDone = 6, kSiteSelftest = 7 };
+
+constexpr int align1024(int v) { return (v + 1023) / 1024 * 1024; }
+
+template <int MODE, int BN, int STAGES>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK_BYTES;
+  static constexpr int B_BYTES = BN * BK_BYTES;
+  // scale-factor atoms (128 rows x 4 bytes = 512 B) per K-tile per 128 rows
+  static constexpr int ATOMS = MODE == kMXF8 ? 1 : (MODE == kNVF4 ? 4 : 0);
+  static constexpr int SFA_BYTES = ATOMS * 512;
+  static constexpr int SFB_BYTES = ATOMS * 512 * (BN / 128);
+  static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + SF_BYTES;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_STG = align1024(OFF_SF + STAGES * SF_BYTES);
+  static constexpr int OFF_BAR = OFF_STG + kEpiWarps * kStagingPerWarp;
+  static constexpr int N_BARS = 2 * STAGES + 4 + 1;
+  static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;  // + alignment slack
+  // tensor-memory columns
+  static constexpr int SF_COL0 = 2 * BN;
+  static constexpr int SFA_COLS = ATOMS * 4;
+  static constexpr int SFB_COLS = ATOMS * 4 * (BN / 128);
+  static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
+  static_assert(SF_COL0 + STAGES * SF_COLS <= kTmemCols, "tensor memory budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(BN % 128 == 0 && BN <= 256, "BN");
+};
+
+struct Params {
+  int M, N, K;  // K in elements
+  int m_tiles, n_tiles, k_tiles;
+  int num_tiles;  // over all batches
+  // block-scaled paths: scale-factor atoms [batch][row tile][K atom] x 512 B
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int sfa_rt, sfb_rt, ks4;
+  // FP32-scale path
+  const float* a_scales;
+  const float* b_scales;
+  int kb;  // K / 128
+  // output
+  void* y;
+  int y_bf16;
+  int tma_store;
+  uint32_t idesc;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void decode_tile(const Params& p, int t, int& b, int& mb, int& nb) {
+  const int per_batch = p.m_tiles * p.n_tiles;
+  b = t / per_batch;
+  const int r = t - b * per_batch;
+  const int span = kGroupM * p.n_tiles;
+  const int g = r / span;
+  const int within = r - g * span;
+  const int rows = min(kGroupM, p.m_tiles - g * kGroupM);
+  mb = g * kGroupM + within % rows;
+  nb = within / rows;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int MODE, int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const __grid_constant__ CUtensorMap tmY, const Params p) {
+  using C = Cfg<MODE, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sB = smem + C::OFF_B;
+  uint8_t* sSF = smem + C::OFF_SF;
+  uint8_t* stg = smem + C::OFF_STG;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int never_abort_storage = 0;  // drains ignore the CTA abort flag
+  volatile int* never_abort = &never_abort_storage;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kEpiWarps);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int b, mb, nb;
+        decode_tile(p, t, b, mb, nb);
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
+          tma_load_3d(sA + stage * C::A_BYTES, &tmA, &full[stage], kt * BK_BYTES, mb * BM, b);
+          tma_load_3d(sB + stage * C::B_BYTES, &tmB, &full[stage], kt * BK_BYTES, nb * BN, b);
+          if constexpr (MODE != kF32Scale) {
+            uint8_t* sf = sSF + stage * C::SF_BYTES;
+            const uint8_t* ga =
+                p.sfa + (static_cast<size_t>(b * p.sfa_rt + mb) * p.ks4 + static_cast<size_t>(kt) * C::ATOMS) * 512;
+            bulk_load(sf, ga, C::SFA_BYTES, &full[stage]);
+#pragma unroll
+            for (int i = 0; i < BN / 128; ++i) {
+              const uint8_t* gb = p.sfb + (static_cast<size_t>(b * p.sfb_rt + nb * (BN / 128) + i) * p.ks4 +
+                                           static_cast<size_t>(kt) * C::ATOMS) * 512;
+              bulk_load(sf + C::SFA_BYTES + i * C::ATOMS * 512, gb, C::ATOMS * 512, &full[stage]);
+            }
+          }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // No copy may still target this CTA's shared memory when it exits.
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          mbar_wait(&full[s], (last_par >> s) & 1u, p.timeout_ns, never_abort, p.status, kSiteDrain);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, tb = 0;
+      uint32_t phase = 0, tph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        if constexpr (MODE != kF32Scale) {
+          if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) break;
+          tc_fence_after();
+        }
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if constexpr (MODE == kF32Scale) {
+            if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
+          const uint32_t d = tmem + static_cast<uint32_t>(tb * BN);
+          if constexpr (MODE == kF32Scale) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f8f6f4(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2), p.idesc,
+                         k > 0 ? 1u : 0u);
+            tc_commit(&empty[stage]);
+            tc_commit(&tfull[tb]);
+            if (++tb == 2) {
+              tb = 0;
+              tph ^= 1u;
+            }
+          } else {
+            const uint32_t sf_t = tmem + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
+            const uint32_t sfa_t = sf_t, sfb_t = sf_t + C::SFA_COLS;
+            const uint32_t sf_s = smem_u32(sSF + stage * C::SF_BYTES);
+            // SFA atom i (K sub-block i) -> columns sfa_t + 4i.
+#pragma unroll
+            for (int i = 0; i < C::ATOMS; ++i) tc_cp_sf(sfa_t + 4 * i, smem_desc(sf_s + 512 * i, 0, 128, 0));
+            // SFB atom (row tile r, K sub-block i) -> columns sfb_t + 4*(i*(BN/128) + r).
+#pragma unroll
+            for (int r = 0; r < BN / 128; ++r)
+#pragma unroll
+              for (int i = 0; i < C::ATOMS; ++i)
+                tc_cp_sf(sfb_t + 4 * (i * (BN / 128) + r),
+                         smem_desc(sf_s + C::SFA_BYTES + 512 * (r * C::ATOMS + i), 0, 128, 0));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = smem_desc(a_base + 32 * k, 16, 1024, 2);
+              const uint64_t bd = smem_desc(b_base + 32 * k, 16, 1024, 2);
+              const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
+              if constexpr (MODE == kMXF8) {
+                // one byte of the 4-byte scale word per 32-K step
+                const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+                mma_mxf8(d, ad, bd, idesc, sfa_t, sfb_t, acc);
+              } else {
+                mma_nvf4(d, ad, bd, p.idesc, sfa_t + 4 * k, sfb_t + 4 * k * (BN / 128), acc);
+              }
+            }
+            tc_commit(&empty[stage]);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if constexpr (MODE != kF32Scale) {
+          if (!ok) break;
+          tc_commit(&tfull[tb]);
+          if (++tb == 2) {
+            tb = 0;
+            tph ^= 1u;
+          }
+        }
+      }
+      // Every MMA and copy this thread issued must finish before TMEM is freed.
+      tc_commit(done);
+      mbar_wait(done, 0, p.timeout_ns, never_abort, p.status, kSiteDone);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    constexpr int COLS = BN / 2;  // columns per thread
+    const int ew = warp - 4;
+    const int q = warp & 3;   // TMEM lane quarter
+    const int g = ew >> 2;    // column half of the tile
+    uint8_t* my_stg = stg + ew * kStagingPerWarp;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int tb = 0, sbuf = 0;
+    uint32_t tph = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      int b, mb, nb;
+      decode_tile(p, t, b, mb, nb);
+      const int row = mb * BM + q * 32 + lane;
+      const int col0 = nb * BN + g * COLS;
+      float acc[COLS];
+      bool ok = true;
+      if constexpr (MODE == kF32Scale) {
+#pragma unroll
+        for (int i = 0; i < COLS; ++i) acc[i] = 0.f;
+        const bool row_ok = row < p.M;
+        const float* sa_row = p.a_scales + static_cast<size_t>(row_ok ? row : 0) * p.kb;
+        const float* sb_row = p.b_scales + static_cast<size_t>(col0 / 128) * p.kb;
+        float sa_next = row_ok ? __ldg(sa_row) : 0.f;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          const float s = sa_next * __ldg(sb_row + kt);
+          if (kt + 1 < p.k_tiles) sa_next = row_ok ? __ldg(sa_row + kt + 1) : 0.f;
+          if (!mbar_wait(&tfull[tb], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(tb * BN + g * COLS);
+#pragma unroll
+          for (int c = 0; c < COLS / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + 32 * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(__uint_as_float(r[j]), s, acc[32 * c + j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[tb]);
+          if (++tb == 2) {
+            tb = 0;
+            tph ^= 1u;
+          }
+        }
+      } else {
+        if (!mbar_wait(&tfull[tb], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
+          ok = false;
+        } else {
+          tc_fence_after();
+          const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(tb * BN + g * COLS);
+#pragma unroll
+          for (int c = 0; c < COLS / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + 32 * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 * c + j] = __uint_as_float(r[j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[tb]);
+          if (++tb == 2) {
+            tb = 0;
+            tph ^= 1u;
+          }
+        }
+      }
+      if (!ok) break;
+      // ---- store the thread's row segment [col0, col0 + COLS)
+      if (p.tma_store) {
+        const int y0 = mb * BM + q * 32;
+        if (!p.y_bf16) {
+#pragma unroll
+          for (int c = 0; c < COLS / 32; ++c) {
+            uint8_t* buf = my_stg + sbuf * 4096;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float* v = &acc[32 * c + 4 * j];
+              const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
+              *reinterpret_cast<uint4*>(buf + off) = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                                                                __float_as_uint(v[2]), __float_as_uint(v[3]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmY, buf, col0 + 32 * c, y0, b);
+              bulk_commit();
+            }
+            sbuf ^= 1;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < COLS / 64; ++c) {
+            uint8_t* buf = my_stg + sbuf * 4096;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float* v = &acc[64 * c + 8 * j];
+              const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
+              *reinterpret_cast<uint4*>(buf + off) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                                pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmY, buf, col0 + 64 * c, y0, b);
+              bulk_commit();
+            }
+            sbuf ^= 1;
+          }
+        }
+      } else if (row < p.M) {
+        const size_t base = (static_cast<size_t>(b) * p.M + row) * static_cast<size_t>(p.N);
+        if (!p.y_bf16) {
+          float* y = reinterpret_cast<float*>(p.y) + base;
+#pragma unroll
+          for (int j = 0; j < COLS; ++j)
+            if (col0 + j < p.N) y[col0 + j] = acc[j];
+        } else {
+          __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y) + base;
+#pragma unroll
+          for (int j = 0; j < COLS; ++j)
+            if (col0 + j < p.N) y[col0 + j] = __float2bfloat16_rn(acc[j]);
+        }
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Scale bytes [batch][rows][KS] (row-major, one per K block) -> atoms of the
+// tensor-core scale-factor layout: atom (b, row tile rt, K atom j) is 512
+// bytes; byte (r%32)*16 + ((r%128)/32)*4 + (kb%4) holds the scale of row
+// rt*128 + r for K block 4j + kb%4.  Missing rows / blocks get `pad`.
+__global__ void __launch_bounds__(256) sf_relayout(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst,
+                                                   int nb, int R, int KS, int RT, int KS4, uint32_t pad) {
+  const int64_t total = static_cast<int64_t>(nb) * RT * KS4 * 128;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int w = static_cast<int>(idx & 127);
+    const int64_t atom = idx >> 7;
+    const int j = static_cast<int>(atom % KS4);
+    const int64_t t2 = atom / KS4;
+    const int rt = static_cast<int>(t2 % RT);
+    const int64_t b = t2 / RT;
+    const int r = rt * 128 + (w >> 2) + 32 * (w & 3);
+    uint32_t word = pad * 0x01010101u;
+    if (r < R) {
+      const uint8_t* row = src + (b * R + r) * static_cast<int64_t>(KS);
+      word = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int kb = 4 * j + i;
+        const uint32_t v = kb < KS ? row[kb] : pad;
+        word |= v << (8 * i);
+      }
+    }
+    dst[idx] = word;
+  }
+}
+
+__global__ void selftest_wait_kernel(uint64_t timeout_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, timeout_ns, &abort_flag, status, kSiteSelftest);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+int rt_rows(int64_t R) { return static_cast<int>(ceil_div(R, 256) * 2); }  // row tiles, even for BN = 256
+
+template <int MODE, int BN, int STAGES>
+cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const Params& p,
+                          const DeviceCtx* ctx, cudaStream_t s) {
+  using C = Cfg<MODE, BN, STAGES>;
+  auto kern = tc_gemm<MODE, BN, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int grid = std::max(1, std::min(p.num_tiles, ctx->num_sms));
+  kern<<<grid, kThreads, C::SMEM, s>>>(ta, tb, ty, p);
+  return cudaGetLastError();
+}
+
+uint32_t f8_fmt(int dtype) { return dtype == BSMM_E5M2 ? 1u : 0u; }
+
+bool make_output_map(CUtensorMap* ty, void* y, bool bf16, int64_t B, int64_t M, int64_t N) {
+  const int esz = bf16 ? 2 : 4;
+  if ((N * esz) % 16 != 0 || (reinterpret_cast<uintptr_t>(y) % 16) != 0) return false;
+  return make_tmap_3d(ty, y, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, esz, N, M, B,
+                      bf16 ? 64 : 32, 32, true);
+}
+
+}  // namespace
+
+size_t sf_atoms_bytes(int64_t B, int64_t R, int64_t K, bool nvf4) {
+  const int64_t k_tiles = ceil_div(K, nvf4 ? 256 : 128);
+  const int64_t ks4 = k_tiles * (nvf4 ? 4 : 1);
+  return static_cast<size_t>(B) * rt_rows(R) * ks4 * 512;
+}
+
+cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* why) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  constexpr int BN = 128;
+  const bool nv = r.nvf4;
+  const int64_t k_tiles = ceil_div(r.K, nv ? 256 : 128);
+  const int ks4 = static_cast<int>(k_tiles * (nv ? 4 : 1));
+  const int KS = static_cast<int>(r.K / (nv ? 16 : 32));
+  uint8_t* ws = reinterpret_cast<uint8_t*>(r.workspace);
+  const size_t a_bytes = align_up(sf_atoms_bytes(r.B, r.M, r.K, nv), 256);
+  uint8_t* sfa = ws;
+  uint8_t* sfb = ws + a_bytes;
+  const uint32_t pad = nv ? 0u : 127u;
+  {
+    const int RT = rt_rows(r.M);
+    const int64_t words = r.B * RT * static_cast<int64_t>(ks4) * 128;
+    const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
+    sf_relayout<<<blocks, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
+                                       static_cast<int>(r.M), KS, RT, ks4, pad);
+  }
+  {
+    const int RT = rt_rows(r.N);
+    const int64_t words = r.B * RT * static_cast<int64_t>(ks4) * 128;
+    const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
+    sf_relayout<<<blocks, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
+                                       static_cast<int>(r.N), KS, RT, ks4, pad);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const int64_t kbytes = nv ? r.K / 2 : r.K;
+  CUtensorMap ta, tb, ty;
+  if (!make_tmap_3d(&ta, r.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, r.M, r.B, BK_BYTES, BM, true) ||
+      !make_tmap_3d(&tb, r.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, r.N, r.B, BK_BYTES, BN, true)) {
+    *why = "cuTensorMapEncodeTiled failed for an operand";
+    return cudaErrorInvalidValue;
+  }
+  Params p{};
+  p.M = static_cast<int>(r.M);
+  p.N = static_cast<int>(r.N);
+  p.K = static_cast<int>(r.K);
+  p.m_tiles = static_cast<int>(ceil_div(r.M, BM));
+  p.n_tiles = static_cast<int>(ceil_div(r.N, BN));
+  p.k_tiles = static_cast<int>(k_tiles);
+  p.num_tiles = static_cast<int>(r.B) * p.m_tiles * p.n_tiles;
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.sfa_rt = rt_rows(r.M);
+  p.sfb_rt = rt_rows(r.N);
+  p.ks4 = ks4;
+  p.y = r.y;
+  p.y_bf16 = r.y_bf16 ? 1 : 0;
+  p.tma_store = make_output_map(&ty, r.y, r.y_bf16, r.B, r.M, r.N) ? 1 : 0;
+  if (!p.tma_store) std::memset(&ty, 0, sizeof(ty));
+  p.status = ctx->status;
+  p.timeout_ns = wait_timeout_ns();
+  if (nv) {
+    // kind::mxf4nvf4: E2M1 = 1 for A and B, UE4M3 scales (bit 23 = 0), M = 128.
+    p.idesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+    return launch_kernel<kNVF4, BN, 4>(ta, tb, ty, p, ctx, s);
+  }
+  // kind::mxf8f6f4: E4M3 = 0 / E5M2 = 1, UE8M0 scales (bit 23 = 1), M = 128.
+  p.idesc = (f8_fmt(r.a_fmt) << 7) | (f8_fmt(r.b_fmt) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+            (static_cast<uint32_t>(BM >> 4) << 24);
+  return launch_kernel<kMXF8, BN, 4>(ta, tb, ty, p, ctx, s);
+}
+
+cudaError_t launch_grouped_gemm(const GroupedGemmRequest& r, cudaStream_t s, std::string* why) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  constexpr int BN = 128;
+  CUtensorMap ta, tb, ty;
+  if (!make_tmap_3d(&ta, r.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, r.K, r.M, 1, BK_BYTES, BM, true) ||
+      !make_tmap_3d(&tb, r.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, r.K, r.N, 1, BK_BYTES, BN, true)) {
+    *why = "cuTensorMapEncodeTiled failed for an operand";
+    return cudaErrorInvalidValue;
+  }
+  Params p{};
+  p.M = static_cast<int>(r.M);
+  p.N = static_cast<int>(r.N);
+  p.K = static_cast<int>(r.K);
+  p.m_tiles = static_cast<int>(ceil_div(r.M, BM));
+  p.n_tiles = static_cast<int>(ceil_div(r.N, BN));
+  p.k_tiles = static_cast<int>(r.K / 128);
+  p.num_tiles = p.m_tiles * p.n_tiles;
+  p.a_scales = r.a_scales;
+  p.b_scales = r.b_scales;
+  p.kb = static_cast<int>(r.K / 128);
+  p.y = r.y;
+  p.y_bf16 = 0;
+  p.tma_store = make_output_map(&ty, r.y, false, 1, r.M, r.N) ? 1 : 0;
+  if (!p.tma_store) std::memset(&ty, 0, sizeof(ty));
+  p.status = ctx->status;
+  p.timeout_ns = wait_timeout_ns();
+  // kind::f8f6f4: D = F32 (bits 4-5 = 1), A/B E4M3 = 0 / E5M2 = 1, K-major, N >> 3, M >> 4.
+  p.idesc = (1u << 4) | (f8_fmt(r.a_fmt) << 7) | (f8_fmt(r.b_fmt) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+            (static_cast<uint32_t>(BM >> 4) << 24);
+  return launch_kernel<kF32Scale, BN, 4>(ta, tb, ty, p, ctx, s);
+}
+
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t s) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  selftest_wait_kernel<<<1, 32, 0, s>>>(timeout_ns, ctx->status);
+  return cudaGetLastError();
+}
+
+}  // namespace bsmm

@@ -1,0 +1,100 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "../../include/bsmm.h"
+
+namespace bsmm {
+
+// ---- error reporting (thread-local last error) ---------------------------
+void set_error(const std::string& msg);
+bsmm_status fail(bsmm_status st, const std::string& msg);
+bsmm_status cuda_fail(cudaError_t e, const char* what);
+
+// ---- per-device context ---------------------------------------------------
+struct DeviceCtx {
+  int device = -1;
+  int num_sms = 0;
+  int* status = nullptr;  // device address of the status word
+};
+// Context of the current device (sets up on first use).  Returns nullptr and
+// sets the last error on failure.
+const DeviceCtx* device_ctx();
+uint64_t wait_timeout_ns();
+
+// ---- TMA descriptors --------------------------------------------------------
+// 3-D tiled tensor map over a row-major [d2][d1][d0] array of `elem_bytes`
+// elements, box {b0, b1, 1}, 128-byte swizzle.  Returns false on failure.
+bool make_tmap_3d(CUtensorMap* tm, const void* base, CUtensorMapDataType dtype, int elem_bytes, uint64_t d0,
+                  uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, bool swizzle128);
+
+// ---- kernel launchers (return cudaSuccess or the launch error) -----------
+struct QuantRequest {
+  const void* x;
+  bool x_bf16;
+  int64_t rows, cols, ld_x;
+  int br, bc;
+  int code;   // bsmm_dtype of the codes
+  int scale;  // bsmm_scale_type
+  bool transpose;
+  void* codes;
+  int64_t ld_codes;
+  void* scales;
+  int64_t ld_scales;
+};
+cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s);
+
+// Scale relayout into the tensor-core scale-factor atoms (see gemm_tc.cu).
+size_t sf_atoms_bytes(int64_t B, int64_t R, int64_t K, bool nvf4);
+
+struct MxGemmRequest {
+  int64_t B, M, N, K;
+  const void* a;
+  const void* b;
+  int a_fmt, b_fmt;  // bsmm_dtype
+  const uint8_t* a_scales;
+  const uint8_t* b_scales;
+  bool nvf4;
+  void* y;
+  bool y_bf16;
+  void* workspace;
+};
+cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* why);
+
+struct GroupedGemmRequest {
+  int64_t M, N, K;
+  const void* a;
+  const void* b;
+  int a_fmt, b_fmt;
+  const float* a_scales;
+  const float* b_scales;
+  float* y;
+};
+cudaError_t launch_grouped_gemm(const GroupedGemmRequest& r, cudaStream_t s, std::string* why);
+
+struct Int8Request {
+  const float* x;
+  const float* w;
+  int64_t B, D_in, D_out;
+  int8_t* x_q;
+  float* x_scales;
+  int8_t* w_q;
+  float* w_scales;
+  float* y;
+  int32_t* acc;
+  void* workspace;
+};
+size_t int8_workspace_bytes(int64_t B, int64_t D_in, int64_t D_out);
+cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s);
+
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t s);
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace bsmm

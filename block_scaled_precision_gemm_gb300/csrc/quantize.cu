@@ -1,0 +1,536 @@
+// Absmax block quantizer kernels.
+//
+// Rule (atrex-bench #002 block_scaled_mm, Input Generation; TensorTonic "Int8
+// Matmul with Per-Channel Scales", problem statement): per block, absmax =
+// largest |x|; scale from absmax (see make_scale); code = round(x / scale)
+// with saturation.  All arithmetic is binary32 with IEEE division.
+//
+// Kernels:
+//   quant_rows   1 x {16,32,64,128} blocks along the contiguous axis; each
+//                block is a group of 2..32 lanes holding 16-byte vectors,
+//                absmax by xor-shuffle; HBM-streaming, unrolled loads.
+//   quant_cols   {16,32,64,128} x 1 blocks down the columns; a 128 x 64 tile
+//                staged in shared memory, codes written as is or transposed.
+//   quant_tile   128 x 128 blocks (one scale per tile).
+//   quant_wrow   one block per row (1 x cols).
+//   quant_wcol   one block per column (rows x 1).
+//   quant_any    one thread per block: every other block shape.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsmm {
+namespace {
+
+struct QP {
+  const void* x;
+  int64_t rows, cols, ld_x;
+  int br, bc;
+  int code, scale;
+  int transpose;
+  void* codes;
+  int64_t ld_codes;
+  void* scales;
+  int64_t ld_scales;
+};
+
+__device__ __forceinline__ float qmax_of(int code) {
+  return code == BSMM_E4M3 ? 448.f : code == BSMM_E5M2 ? 57344.f : code == BSMM_E2M1 ? 6.f : 127.f;
+}
+
+// Value of an unsigned E4M3 byte, exactly.
+__device__ __forceinline__ float ue4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 0xFu, m = b & 7u;
+  if (e == 0) return static_cast<float>(m) * 0.001953125f;  // m * 2^-9
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));     // 1.m * 2^(e-7)
+}
+
+struct Scale {
+  float s;          // the divisor
+  uint32_t stored;  // what is written: binary32 bits or the scale byte
+};
+
+__device__ __forceinline__ Scale make_scale(float absmax, int code, int scale) {
+  const float r = __fdiv_rn(absmax, qmax_of(code));
+  Scale out;
+  if (scale == BSMM_SCALE_F32) {
+    // INT8 (TensorTonic): absmax/127, an all-zero block gets 1.
+    // FP8/FP4 (atrex-bench): max(absmax/qmax, 1e-10).
+    const float s = (code == BSMM_INT8) ? (absmax == 0.f ? 1.f : r) : fmaxf(r, 1e-10f);
+    out.s = s;
+    out.stored = __float_as_uint(s);
+  } else if (scale == BSMM_SCALE_UE8M0) {
+    // Smallest power of two not below r: 2^ceil(log2 r), exponent in [-127,127].
+    int e;
+    if (absmax == 0.f) {
+      e = 0;
+    } else if (r == 0.f) {
+      e = -127;
+    } else {
+      const uint32_t bits = __float_as_uint(r);
+      const int E = static_cast<int>((bits >> 23) & 0xFFu);
+      const uint32_t man = bits & 0x7FFFFFu;
+      if (E == 0)
+        e = -149 + (32 - __clz(static_cast<int>(man - 1u)));  // subnormal r = man * 2^-149
+      else
+        e = E - 127 + (man != 0u ? 1 : 0);
+      e = max(-127, min(127, e));
+    }
+    out.stored = static_cast<uint32_t>(e + 127);
+    out.s = e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+  } else {
+    // UE4M3: nearest E4M3 value of r; zero block -> 1.0; a scale that rounds
+    // to zero -> the smallest subnormal.
+    uint32_t b;
+    if (absmax == 0.f) {
+      b = 0x38u;
+    } else {
+      b = cvt_e4m3x2(r, 0.f) & 0xFFu;
+      if (b == 0u) b = 1u;
+    }
+    out.stored = b;
+    out.s = ue4m3_value(b);
+  }
+  return out;
+}
+
+__device__ __forceinline__ float clampq(float q, float qmax) { return fminf(fmaxf(q, -qmax), qmax); }
+
+__device__ __forceinline__ uint32_t int8_code(float q) {
+  return static_cast<uint32_t>(__float2int_rn(clampq(q, 127.f))) & 0xFFu;
+}
+
+// Codes of four consecutive elements: 4 bytes (E4M3/E5M2/INT8, element 0 in
+// the low byte) or 2 bytes (E2M1, element 0 in the low nibble).
+__device__ __forceinline__ uint32_t encode4(float x0, float x1, float x2, float x3, float s, int code) {
+  const float qm = qmax_of(code);
+  const float q0 = clampq(__fdiv_rn(x0, s), qm), q1 = clampq(__fdiv_rn(x1, s), qm);
+  const float q2 = clampq(__fdiv_rn(x2, s), qm), q3 = clampq(__fdiv_rn(x3, s), qm);
+  switch (code) {
+    case BSMM_E4M3: return cvt_e4m3x2(q0, q1) | (cvt_e4m3x2(q2, q3) << 16);
+    case BSMM_E5M2: return cvt_e5m2x2(q0, q1) | (cvt_e5m2x2(q2, q3) << 16);
+    case BSMM_E2M1: return cvt_e2m1x2(q0, q1) | (cvt_e2m1x2(q2, q3) << 8);
+    default: return int8_code(q0) | (int8_code(q1) << 8) | (int8_code(q2) << 16) | (int8_code(q3) << 24);
+  }
+}
+
+// One code (8-bit formats) or one nibble (E2M1).
+__device__ __forceinline__ uint32_t encode1(float x, float s, int code) {
+  const float q = clampq(__fdiv_rn(x, s), qmax_of(code));
+  switch (code) {
+    case BSMM_E4M3: return cvt_e4m3x2(q, 0.f) & 0xFFu;
+    case BSMM_E5M2: return cvt_e5m2x2(q, 0.f) & 0xFFu;
+    case BSMM_E2M1: return cvt_e2m1x2(q, 0.f) & 0xFu;
+    default: return int8_code(q);
+  }
+}
+
+__device__ __forceinline__ void store_scale(void* scales, int64_t idx, int scale, uint32_t stored) {
+  if (scale == BSMM_SCALE_F32)
+    reinterpret_cast<uint32_t*>(scales)[idx] = stored;
+  else
+    reinterpret_cast<uint8_t*>(scales)[idx] = static_cast<uint8_t>(stored);
+}
+
+template <typename In>
+__device__ __forceinline__ float load1(const void* x, int64_t idx) {
+  if constexpr (sizeof(In) == 4) {
+    return __ldg(reinterpret_cast<const float*>(x) + idx);
+  } else {
+    const uint16_t b = __ldg(reinterpret_cast<const unsigned short*>(x) + idx);
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+}
+
+// 16-byte vector of 4 (binary32) or 8 (bfloat16) elements, streamed.
+template <typename In>
+__device__ __forceinline__ void load_vec(const void* p, float (&v)[16 / sizeof(In)]) {
+  const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
+  if constexpr (sizeof(In) == 4) {
+    v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+  } else {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 1 x bc blocks along rows
+// ---------------------------------------------------------------------------
+constexpr int kRowsUnroll = 4;
+
+template <typename In>
+__global__ void __launch_bounds__(256) quant_rows(QP p) {
+  constexpr int VEC = 16 / sizeof(In);
+  const int G = p.bc / VEC;  // lanes sharing one block: 2..32, a power of two
+  const int64_t vpr = p.cols / VEC;
+  const int64_t total = p.rows * vpr;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t chunk = nw * 32;
+  const bool fp4 = p.code == BSMM_E2M1;
+  for (int64_t base = warp * 32; base < total; base += chunk * kRowsUnroll) {
+    float v[kRowsUnroll][VEC];
+#pragma unroll
+    for (int u = 0; u < kRowsUnroll; ++u) {
+      const int64_t vi = base + u * chunk + lane;
+      if (vi < total) {
+        const int64_t r = vi / vpr, c = vi - r * vpr;
+        load_vec<In>(reinterpret_cast<const In*>(p.x) + r * p.ld_x + c * VEC, v[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) v[u][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsUnroll; ++u) {
+      const int64_t vi = base + u * chunk + lane;
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) m = fmaxf(m, fabsf(v[u][i]));
+      for (int o = G >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (vi >= total) continue;
+      const Scale sc = make_scale(m, p.code, p.scale);
+      const int64_t r = vi / vpr, c = vi - r * vpr;
+      if ((lane & (G - 1)) == 0) store_scale(p.scales, r * p.ld_scales + (c * VEC) / p.bc, p.scale, sc.stored);
+      const uint32_t w0 = encode4(v[u][0], v[u][1], v[u][2], v[u][3], sc.s, p.code);
+      const int64_t e = r * p.ld_codes + c * VEC;  // element offset
+      uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
+      if constexpr (VEC == 4) {
+        if (fp4)
+          *reinterpret_cast<uint16_t*>(out + e / 2) = static_cast<uint16_t>(w0);
+        else
+          *reinterpret_cast<uint32_t*>(out + e) = w0;
+      } else {
+        const uint32_t w1 = encode4(v[u][4], v[u][5], v[u][6], v[u][7], sc.s, p.code);
+        if (fp4)
+          *reinterpret_cast<uint32_t*>(out + e / 2) = w0 | (w1 << 16);
+        else
+          *reinterpret_cast<uint2*>(out + e) = make_uint2(w0, w1);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// br x 1 blocks down the columns, 128-row x 64-column tiles
+// ---------------------------------------------------------------------------
+constexpr int kColTileR = 128, kColTileC = 64;
+
+template <typename In>
+__global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok) {
+  __shared__ float tile[kColTileR][kColTileC + 1];
+  __shared__ float pmax[4][kColTileC];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColTileR;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kColTileC;
+  const int nr = static_cast<int>(p.rows - r0 < kColTileR ? p.rows - r0 : kColTileR);
+  const int nc = static_cast<int>(p.cols - c0 < kColTileC ? p.cols - c0 : kColTileC);
+  const int t = threadIdx.x;
+  const In* x = reinterpret_cast<const In*>(p.x);
+  // Stage the tile (coalesced along columns).
+  if (vec_ok) {
+    constexpr int VEC = 16 / sizeof(In);
+    constexpr int VPR = kColTileC / VEC;  // vectors per tile row
+    for (int i = t; i < kColTileR * VPR; i += 256) {
+      const int rr = i / VPR, cv = i % VPR;
+      float v[VEC];
+      if (rr < nr && cv * VEC < nc) {
+        load_vec<In>(x + (r0 + rr) * p.ld_x + c0 + cv * VEC, v);
+      } else {
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) v[k] = 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < VEC; ++k) tile[rr][cv * VEC + k] = v[k];
+    }
+  } else {
+    for (int i = t; i < kColTileR * kColTileC; i += 256) {
+      const int rr = i / kColTileC, cc = i % kColTileC;
+      tile[rr][cc] = (rr < nr && cc < nc) ? load1<In>(x, (r0 + rr) * p.ld_x + c0 + cc) : 0.f;
+    }
+  }
+  __syncthreads();
+  // Thread (col, part) owns rows 32*part .. 32*part+31 of one column.
+  const int col = t % kColTileC, part = t / kColTileC;
+  const int rbase = part * 32;
+  const int br = p.br;
+  float m0 = 0.f, m1 = 0.f;  // maxima of the two 16-row halves
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m0 = fmaxf(m0, fabsf(tile[rbase + i][col]));
+#pragma unroll
+  for (int i = 16; i < 32; ++i) m1 = fmaxf(m1, fabsf(tile[rbase + i][col]));
+  pmax[part][col] = fmaxf(m0, m1);
+  __syncthreads();
+  const bool active = rbase < nr && col < nc;
+  // Scales of the (one or two) blocks this thread's 32 rows belong to.
+  float amax_a, amax_b;
+  if (br == 16) {
+    amax_a = m0;
+    amax_b = m1;
+  } else if (br == 32) {
+    amax_a = amax_b = fmaxf(m0, m1);
+  } else if (br == 64) {
+    const int pp = part & ~1;
+    amax_a = amax_b = fmaxf(pmax[pp][col], pmax[pp + 1][col]);
+  } else {
+    amax_a = amax_b = fmaxf(fmaxf(pmax[0][col], pmax[1][col]), fmaxf(pmax[2][col], pmax[3][col]));
+  }
+  const Scale sa = make_scale(amax_a, p.code, p.scale);
+  const Scale sb = (br == 16) ? make_scale(amax_b, p.code, p.scale) : sa;
+  if (active) {
+    const int64_t gc = c0 + col;
+    const int64_t blk0 = (r0 + rbase) / br;
+    const bool writes_a = (rbase % br) == 0;
+    if (p.transpose) {
+      if (writes_a) store_scale(p.scales, gc * p.ld_scales + blk0, p.scale, sa.stored);
+      if (br == 16) store_scale(p.scales, gc * p.ld_scales + blk0 + 1, p.scale, sb.stored);
+    } else {
+      if (writes_a) store_scale(p.scales, blk0 * p.ld_scales + gc, p.scale, sa.stored);
+      if (br == 16) store_scale(p.scales, (blk0 + 1) * p.ld_scales + gc, p.scale, sb.stored);
+    }
+  }
+  uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
+  if (p.transpose) {
+    if (!active) return;
+    // 32 consecutive output elements of row `gc` of the transposed array.
+    uint32_t w[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const float s = (g < 4) ? sa.s : sb.s;
+      w[g] = encode4(tile[rbase + 4 * g][col], tile[rbase + 4 * g + 1][col], tile[rbase + 4 * g + 2][col],
+                     tile[rbase + 4 * g + 3][col], s, p.code);
+    }
+    const int64_t e = (c0 + col) * p.ld_codes + r0 + rbase;
+    const bool full32 = rbase + 32 <= nr;  // else only the first 16 rows exist
+    if (p.code == BSMM_E2M1) {
+      if (full32)
+        *reinterpret_cast<uint4*>(out + e / 2) =
+            make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16), w[6] | (w[7] << 16));
+      else
+        *reinterpret_cast<uint2*>(out + e / 2) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+    } else {
+      *reinterpret_cast<uint4*>(out + e) = make_uint4(w[0], w[1], w[2], w[3]);
+      if (full32) *reinterpret_cast<uint4*>(out + e + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  } else {
+    // Row-major codes: lanes hold consecutive columns.
+    for (int i = 0; i < 32; ++i) {
+      const float s = (i < 16) ? sa.s : sb.s;
+      const uint32_t cval = encode1(tile[rbase + i][col], s, p.code);
+      const int64_t e = (r0 + rbase + i) * p.ld_codes + c0 + col;
+      const bool ok = active && rbase + i < nr;
+      if (p.code == BSMM_E2M1) {
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, cval, 1);
+        if (ok && (col & 1) == 0) out[e / 2] = static_cast<uint8_t>(cval | (hi << 4));
+      } else if (ok) {
+        out[e] = static_cast<uint8_t>(cval);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 128 x 128 blocks
+// ---------------------------------------------------------------------------
+template <typename In>
+__global__ void __launch_bounds__(256) quant_tile(QP p) {
+  __shared__ float wmax[8];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
+  const int t = threadIdx.x;
+  const int row = t >> 1, half = t & 1;  // 64 elements per thread
+  const In* x = reinterpret_cast<const In*>(p.x) + (r0 + row) * p.ld_x + c0 + half * 64;
+  float v[64];
+  constexpr int VEC = 16 / sizeof(In);
+#pragma unroll
+  for (int i = 0; i < 64 / VEC; ++i) {
+    float tmp[VEC];
+    load_vec<In>(x + i * VEC, tmp);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) v[i * VEC + k] = tmp[k];
+  }
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(v[i]));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((t & 31) == 0) wmax[t >> 5] = m;
+  __syncthreads();
+  m = wmax[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
+  const Scale sc = make_scale(m, p.code, p.scale);
+  if (t == 0) store_scale(p.scales, blockIdx.y * p.ld_scales + blockIdx.x, p.scale, sc.stored);
+  uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
+  const int64_t e = (r0 + row) * p.ld_codes + c0 + half * 64;
+  uint32_t w[16];
+#pragma unroll
+  for (int g = 0; g < 16; ++g) w[g] = encode4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3], sc.s, p.code);
+  if (p.code == BSMM_E2M1) {
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+      *reinterpret_cast<uint4*>(out + e / 2 + 16 * g) =
+          make_uint4(w[8 * g] | (w[8 * g + 1] << 16), w[8 * g + 2] | (w[8 * g + 3] << 16),
+                     w[8 * g + 4] | (w[8 * g + 5] << 16), w[8 * g + 6] | (w[8 * g + 7] << 16));
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      *reinterpret_cast<uint4*>(out + e + 16 * g) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Whole-row and whole-column blocks, and the generic fallback
+// ---------------------------------------------------------------------------
+template <typename In>
+__global__ void __launch_bounds__(256) quant_wrow(QP p) {
+  __shared__ float wmax[8];
+  const int64_t r = blockIdx.x;
+  const int t = threadIdx.x;
+  const In* x = reinterpret_cast<const In*>(p.x);
+  float m = 0.f;
+  for (int64_t c = t; c < p.cols; c += 256) m = fmaxf(m, fabsf(load1<In>(x, r * p.ld_x + c)));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((t & 31) == 0) wmax[t >> 5] = m;
+  __syncthreads();
+  m = wmax[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
+  const Scale sc = make_scale(m, p.code, p.scale);
+  if (t == 0) store_scale(p.scales, r * p.ld_scales, p.scale, sc.stored);
+  uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
+  if (p.code == BSMM_E2M1) {
+    for (int64_t c = 2 * t; c < p.cols; c += 512) {
+      const uint32_t lo = encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code);
+      const uint32_t hi = (c + 1 < p.cols) ? encode1(load1<In>(x, r * p.ld_x + c + 1), sc.s, p.code) : 0u;
+      out[(r * p.ld_codes + c) / 2] = static_cast<uint8_t>(lo | (hi << 4));
+    }
+  } else {
+    for (int64_t c = t; c < p.cols; c += 256)
+      out[r * p.ld_codes + c] = static_cast<uint8_t>(encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code));
+  }
+}
+
+// One CTA per 32 columns, 8 warps striding down the rows.
+template <typename In>
+__global__ void __launch_bounds__(256) quant_wcol(QP p) {
+  __shared__ float wmax[8][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  const bool cok = c < p.cols;
+  const In* x = reinterpret_cast<const In*>(p.x);
+  float m = 0.f;
+  if (cok)
+    for (int64_t r = warp; r < p.rows; r += 8) m = fmaxf(m, fabsf(load1<In>(x, r * p.ld_x + c)));
+  wmax[warp][lane] = m;
+  __syncthreads();
+  m = wmax[0][lane];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i][lane]);
+  const Scale sc = make_scale(m, p.code, p.scale);
+  if (warp == 0 && cok) store_scale(p.scales, c, p.scale, sc.stored);
+  uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
+  const bool fp4 = p.code == BSMM_E2M1;
+  if (p.transpose) {
+    // Column c becomes row c of the output; elements along the rows.
+    if (!cok) return;
+    if (fp4) {
+      for (int64_t r = 2 * warp; r < p.rows; r += 16) {
+        const uint32_t lo = encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code);
+        const uint32_t hi = (r + 1 < p.rows) ? encode1(load1<In>(x, (r + 1) * p.ld_x + c), sc.s, p.code) : 0u;
+        out[(c * p.ld_codes + r) / 2] = static_cast<uint8_t>(lo | (hi << 4));
+      }
+    } else {
+      for (int64_t r = warp; r < p.rows; r += 8)
+        out[c * p.ld_codes + r] = static_cast<uint8_t>(encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code));
+    }
+  } else {
+    for (int64_t r = warp; r < p.rows; r += 8) {
+      const uint32_t v = cok ? encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code) : 0u;
+      if (fp4) {
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, v, 1);
+        if (cok && (lane & 1) == 0) out[(r * p.ld_codes + c) / 2] = static_cast<uint8_t>(v | (hi << 4));
+      } else if (cok) {
+        out[r * p.ld_codes + c] = static_cast<uint8_t>(v);
+      }
+    }
+  }
+}
+
+// One thread per block; any block shape that divides the array (E2M1 needs
+// an even block extent along the output's contiguous axis).
+template <typename In>
+__global__ void __launch_bounds__(256) quant_any(QP p) {
+  const int64_t nbr = p.rows / p.br, nbc = p.cols / p.bc;
+  const int64_t bid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (bid >= nbr * nbc) return;
+  const int64_t bi = bid / nbc, bj = bid % nbc;
+  const In* x = reinterpret_cast<const In*>(p.x);
+  float m = 0.f;
+  for (int i = 0; i < p.br; ++i)
+    for (int j = 0; j < p.bc; ++j) m = fmaxf(m, fabsf(load1<In>(x, (bi * p.br + i) * p.ld_x + bj * p.bc + j)));
+  const Scale sc = make_scale(m, p.code, p.scale);
+  store_scale(p.scales, p.transpose ? bj * p.ld_scales + bi : bi * p.ld_scales + bj, p.scale, sc.stored);
+  uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
+  for (int i = 0; i < p.br; ++i) {
+    for (int j = 0; j < p.bc; ++j) {
+      const int64_t r = bi * p.br + i, c = bj * p.bc + j;
+      const uint32_t v = encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code);
+      const int64_t e = p.transpose ? c * p.ld_codes + r : r * p.ld_codes + c;
+      if (p.code == BSMM_E2M1) {
+        uint8_t& byte = out[e / 2];
+        byte = (e & 1) ? static_cast<uint8_t>((byte & 0x0Fu) | (v << 4)) : static_cast<uint8_t>((byte & 0xF0u) | v);
+      } else {
+        out[e] = static_cast<uint8_t>(v);
+      }
+    }
+  }
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+template <typename In>
+cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
+  const int esz = sizeof(In);
+  const bool x_vec = aligned(p.x, 16) && (p.ld_x * esz) % 16 == 0 && p.cols % (16 / esz) == 0;
+  const bool codes16 = aligned(p.codes, 16) && p.ld_codes % 32 == 0;
+  const bool pow2_small = (p.bc == 16 || p.bc == 32 || p.bc == 64 || p.bc == 128);
+  const bool pow2_small_r = (p.br == 16 || p.br == 32 || p.br == 64 || p.br == 128);
+  if (p.br == 1 && pow2_small && !p.transpose && x_vec && codes16) {
+    const int64_t vecs = p.rows * (p.cols / (16 / esz));
+    int64_t blocks = ceil_div(vecs, 256 * kRowsUnroll);
+    blocks = std::min<int64_t>(blocks, static_cast<int64_t>(ctx->num_sms) * 8);
+    quant_rows<In><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(p);
+  } else if (p.bc == 1 && pow2_small_r && (!p.transpose || (codes16 && p.ld_codes % 32 == 0))) {
+    dim3 grid(static_cast<unsigned>(ceil_div(p.cols, kColTileC)), static_cast<unsigned>(ceil_div(p.rows, kColTileR)));
+    quant_cols<In><<<grid, 256, 0, s>>>(p, x_vec ? 1 : 0);
+  } else if (p.br == 128 && p.bc == 128 && !p.transpose && x_vec && codes16) {
+    dim3 grid(static_cast<unsigned>(p.cols / 128), static_cast<unsigned>(p.rows / 128));
+    quant_tile<In><<<grid, 256, 0, s>>>(p);
+  } else if (p.br == 1 && p.bc == p.cols && !p.transpose) {
+    quant_wrow<In><<<static_cast<unsigned>(p.rows), 256, 0, s>>>(p);
+  } else if (p.bc == 1 && p.br == p.rows) {
+    quant_wcol<In><<<static_cast<unsigned>(ceil_div(p.cols, 32)), 256, 0, s>>>(p);
+  } else {
+    const int64_t nblk = (p.rows / p.br) * (p.cols / p.bc);
+    quant_any<In><<<static_cast<unsigned>(ceil_div(nblk, 256)), 256, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  QP p{q.x, q.rows, q.cols, q.ld_x, q.br, q.bc, q.code, q.scale, q.transpose ? 1 : 0,
+       q.codes, q.ld_codes, q.scales, q.ld_scales};
+  return q.x_bf16 ? dispatch<__nv_bfloat16>(p, ctx, s) : dispatch<float>(p, ctx, s);
+}
+
+}  // namespace bsmm

@@ -1,0 +1,259 @@
+/*
+ * bsmm.h -- block-scaled low-precision matrix multiply for GB300 (sm_103a).
+ *
+ * C ABI of libbsmm.so.  Plain pointers and sizes only; no C++ or framework
+ * types cross this boundary and no exception leaves it.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *    never allocates, frees or keeps device memory of its own, apart from a
+ *    4-byte device status word per loaded module.  Scratch memory a call needs
+ *    is passed in as `workspace`; its size comes from the matching
+ *    *_workspace_size() query (0 means no workspace is needed).
+ *  - Every call is asynchronous with respect to the host: it validates its
+ *    arguments, enqueues kernels on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and returns.  Results are ready when the stream
+ *    reaches that point.  Calls are safe to issue from several host threads.
+ *  - Every call returns a bsmm_status.  On failure nothing has been enqueued
+ *    (argument errors) or the CUDA error is reported (BSMM_ERR_CUDA);
+ *    bsmm_last_error() then returns a message for the calling thread.
+ *  - Matrices are row-major.  Strides are in elements.  A GEMM operand's
+ *    contraction axis K is its innermost (contiguous) axis.  E2M1 codes are
+ *    packed two per byte along the contiguous axis, even element in the low
+ *    nibble, so a row of K E2M1 codes is K/2 bytes.
+ *  - Device pointers given to the GEMMs must be 16-byte aligned.
+ *  - A zero-sized problem (M == 0, or B == 0) is BSMM_OK and launches nothing.
+ *  - Kernels never spin without bound: every wait inside a kernel gives up
+ *    after a limit (bsmm_set_wait_timeout_ns), records the failure in the
+ *    device status word and returns.  bsmm_check_device_status() reports it.
+ *
+ * Sources (the four pages this library implements):
+ *  [JAX]  jax.nn.scaled_matmul documentation ("Mathematically" definition,
+ *         Parameters, Notes on the cuDNN/Blackwell formats, Examples).
+ *  [TT]   TensorTonic, "Int8 Matmul with Per-Channel Scales" (problem
+ *         statement, Requirements, Constraints, Examples).
+ *  [AB]   atrex-bench operator #002 "block_scaled_mm" (Reference
+ *         Implementation, Shapes table, Input Generation).
+ *  [NKI]  AWS Neuron NKI "Matmul MXFP8 Backward Kernel API Reference"
+ *         (introduction, Parameters, Returns).
+ */
+#ifndef BSMM_H_
+#define BSMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so this header needs no CUDA
+ * headers. */
+typedef struct CUstream_st* bsmm_stream_t;
+
+typedef enum bsmm_status {
+  BSMM_OK = 0,
+  BSMM_ERR_INVALID_ARG = 1,  /* null pointer, bad enum, negative size        */
+  BSMM_ERR_SHAPE = 2,        /* sizes inconsistent with each other           */
+  BSMM_ERR_ALIGNMENT = 3,    /* pointer or row pitch not 16-byte aligned     */
+  BSMM_ERR_UNSUPPORTED = 4,  /* valid request this build has no kernel for   */
+  BSMM_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed            */
+  BSMM_ERR_TIMEOUT = 6,      /* a bounded in-kernel wait gave up             */
+  BSMM_ERR_WORKSPACE = 7     /* workspace missing or smaller than required   */
+} bsmm_status;
+
+typedef enum bsmm_dtype {
+  BSMM_F32 = 0,   /* binary32                                               */
+  BSMM_BF16 = 1,  /* bfloat16                                               */
+  BSMM_E4M3 = 2,  /* float8_e4m3fn: bias 7, no Inf, max 448                 */
+  BSMM_E5M2 = 3,  /* float8_e5m2:   bias 15, IEEE-like, max 57344           */
+  BSMM_E2M1 = 4,  /* float4_e2m1fn: max 6, packed two per byte              */
+  BSMM_INT8 = 5   /* signed 8-bit integer codes in [-127, 127]              */
+} bsmm_dtype;
+
+typedef enum bsmm_scale_type {
+  BSMM_SCALE_F32 = 0,    /* one binary32 per block                           */
+  BSMM_SCALE_UE8M0 = 1,  /* one byte per block: 2^(byte-127); 0xFF is NaN   */
+  BSMM_SCALE_UE4M3 = 2   /* one byte per block: unsigned E4M3 value          */
+} bsmm_scale_type;
+
+/* ------------------------------------------------------------------------ */
+/* Library state                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Version as MAJOR*10000 + MINOR*100 + PATCH. */
+int bsmm_version(void);
+
+/* Message describing the most recent failure on the calling host thread
+ * ("" if none).  The pointer stays valid until the thread's next call. */
+const char* bsmm_last_error(void);
+
+/* Limit, in nanoseconds, of every bounded wait inside the library's kernels
+ * (default 1e9 = one second).  Applies to launches enqueued afterwards. */
+void bsmm_set_wait_timeout_ns(uint64_t ns);
+
+/* Synchronizes `stream`, then reads and clears the device status word of
+ * the current device.  Returns BSMM_ERR_TIMEOUT if any kernel gave up a wait
+ * since the last check (the kernel's outputs are then undefined, the CUDA
+ * context stays usable), BSMM_ERR_CUDA if the stream reported an error, else
+ * BSMM_OK.  `*where` (if not NULL) receives the recorded wait-site code. */
+bsmm_status bsmm_check_device_status(bsmm_stream_t stream, int* where);
+
+/* Diagnostic with no counterpart on the pages: launches one CTA that waits
+ * on an mbarrier nothing ever arrives on, with a limit of `timeout_ns`.  The
+ * wait gives up, the kernel records BSMM_ERR_TIMEOUT in the status word and
+ * returns.  Used to test the timeout path without faulting a GPU. */
+bsmm_status bsmm_selftest_wait_timeout(uint64_t timeout_ns, bsmm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Quantizer                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Absmax block quantizer.
+ *
+ * Defined by [AB] Input Generation (binary32 scale = max(absmax/448, 1e-10),
+ * codes = E4M3(clamp(x/scale, +-448))) and [TT] problem statement (INT8:
+ * scale = absmax/127, all-zero block -> 1, codes = clip(round(x/scale),
+ * +-127)).  UE8M0 and UE4M3 scales have no rule on the pages; this library
+ * uses: UE8M0 scale = 2^ceil(log2(absmax/qmax)) (exponent clamped to
+ * [-127,127]; zero block -> 1), UE4M3 scale = E4M3(absmax/qmax) rounded to
+ * nearest (zero block -> 1, a scale rounding to 0 -> 2^-9).  qmax is the
+ * code format's largest value: E4M3 448, E5M2 57344, E2M1 6, INT8 127.
+ * All arithmetic is binary32 with IEEE division (x/scale, never x*(1/scale));
+ * rounding is to nearest, ties to even; floating codes saturate.
+ *
+ *   x        [rows, cols] input, element (r, c) at x[r*ld_x + c]; F32 or BF16.
+ *   block_rows x block_cols
+ *            block shape.  Supported: 1 x {16,32,64,128}, 1 x cols (one scale
+ *            per row), {16,32,64,128} x 1, rows x 1 (one scale per column),
+ *            128 x 128.  rows % block_rows == 0 and cols % block_cols == 0.
+ *   code_type  E4M3, E5M2, E2M1 or INT8.   scale_type  F32, UE8M0 or UE4M3
+ *            (INT8 codes need F32 scales).
+ *   transpose_out
+ *            0: codes [rows, cols] at codes[r*ld_codes + c] (E2M1: byte
+ *               (r*ld_codes + c)/2 holds element c and c+1 of row r; ld_codes
+ *               counts elements and must be even), scales
+ *               [rows/block_rows, cols/block_cols] row-major, pitch
+ *               ld_scales elements.
+ *            1: (only for column blocks) codes stored transposed,
+ *               [cols, rows] at codes[c*ld_codes + r], scales transposed
+ *               [cols/block_cols, rows/block_rows] with pitch ld_scales.
+ *   codes    output, 1 byte per code (E2M1: half a byte).
+ *   scales   output, 4 bytes (F32) or 1 byte per scale.
+ *
+ * Errors: BSMM_ERR_INVALID_ARG (null pointer, bad enum), BSMM_ERR_SHAPE
+ * (indivisible shape, pitch too small), BSMM_ERR_UNSUPPORTED (other block
+ * shapes, transposed row blocks, INT8 with a non-F32 scale). */
+bsmm_status bsmm_quantize(const void* x, bsmm_dtype x_type, int64_t rows, int64_t cols,
+                          int64_t ld_x, int block_rows, int block_cols, bsmm_dtype code_type,
+                          bsmm_scale_type scale_type, int transpose_out, void* codes,
+                          int64_t ld_codes, void* scales, int64_t ld_scales,
+                          bsmm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Batched block-scaled GEMM                                                */
+/* ------------------------------------------------------------------------ */
+
+/* y[b,m,n] = sum_k (a[b,m,k] * a_scales[b,m,k/bs_a]) * (w[b,n,k] * b_scales[b,n,k/bs_b])
+ * with bs_a = K/K_a and bs_b = K/K_b inferred from the scale counts, FP32
+ * accumulation ([JAX] "Mathematically" definition and Parameters).
+ *
+ * Supported formats ([JAX] Notes, cuDNN on Blackwell):
+ *   MXFP8: a_type, b_type in {E4M3, E5M2} (may differ), scale_type UE8M0,
+ *          bs_a = bs_b = 32.
+ *   NVFP4: a_type = b_type = E2M1, scale_type UE4M3, bs_a = bs_b = 16.
+ * Other combinations return BSMM_ERR_UNSUPPORTED.
+ *
+ *   a        [B, M, K] codes, contiguous (E2M1: K/2 bytes per row).
+ *   b        [B, N, K] codes, contiguous.
+ *   a_scales [B, M, K_a] scale bytes, contiguous.  b_scales [B, N, K_b].
+ *   y        [B, M, N] output, F32 or BF16 (round to nearest even),
+ *            contiguous.
+ *   workspace  device scratch of at least bsmm_gemm_workspace_size() bytes
+ *            (holds the scales in the tensor-core scale-factor layout).
+ *   K must be a multiple of 32; pointers 16-byte aligned.
+ */
+size_t bsmm_gemm_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K, bsmm_dtype a_type);
+
+bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K,
+                      const void* a, bsmm_dtype a_type, const void* b, bsmm_dtype b_type,
+                      const void* a_scales, int64_t K_a, const void* b_scales, int64_t K_b,
+                      bsmm_scale_type scale_type, void* y, bsmm_dtype y_type,
+                      void* workspace, size_t workspace_bytes, bsmm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* GEMM with 1 x group_k activation and group_n x group_k weight FP32 scales */
+/* ------------------------------------------------------------------------ */
+
+/* y[m,n] = sum_kb a_scales[m,kb] * b_scales[n/group_n,kb] *
+ *          sum_{k in block kb} a[m,k] * b[n,k]
+ * with FP32 promotion of every K block's partial sum ([AB] Reference
+ * Implementation; inputs as produced by [AB] Input Generation).
+ *
+ *   a        [M, K] E4M3 (or E5M2) codes, contiguous.
+ *   b        [N, K] E4M3 (or E5M2) codes, contiguous.
+ *   a_scales [M, K/group_k] binary32.   b_scales [N/group_n, K/group_k].
+ *   y        [M, N] binary32 output, contiguous.
+ *   group_n = group_k = 128 (the pages' only configuration); other values
+ *   return BSMM_ERR_UNSUPPORTED.  N % group_n == 0 and K % group_k == 0
+ *   (BSMM_ERR_SHAPE otherwise).  M is arbitrary.
+ */
+bsmm_status bsmm_gemm_grouped(int64_t M, int64_t N, int64_t K, const void* a, bsmm_dtype a_type,
+                              const void* b, bsmm_dtype b_type, const float* a_scales,
+                              const float* b_scales, int group_n, int group_k, float* y,
+                              bsmm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* INT8 per-channel symmetric matmul                                        */
+/* ------------------------------------------------------------------------ */
+
+/* [TT] problem statement and Requirements: s_x[b] = max_i |x[b,i]| / 127,
+ * s_w[j] = max_i |w[i,j]| / 127 (all-zero row/column -> 1), codes
+ * clip(round(v/s), -127, 127), a[b,j] = sum_i x_q[b,i]*w_q[i,j] accumulated
+ * exactly in int32, y[b,j] = float32(a[b,j]) * s_x[b] * s_w[j].
+ *
+ *   x [B, D_in] binary32, w [D_in, D_out] binary32 (both contiguous).
+ *   Outputs (contiguous): x_q int8 [B, D_in], x_scales [B], w_q int8
+ *   [D_in, D_out] (the page's layout), w_scales [D_out], y [B, D_out].
+ *   acc      optional int32 [B, D_out] output of the exact integer sums
+ *            (NULL to skip).
+ *   workspace  at least bsmm_int8_channel_workspace_size() bytes (holds the
+ *            transposed weight codes the matmul reads).
+ *   D_in must be a multiple of 16.
+ */
+size_t bsmm_int8_channel_workspace_size(int64_t B, int64_t D_in, int64_t D_out);
+
+bsmm_status bsmm_int8_channel(const float* x, const float* w, int64_t B, int64_t D_in,
+                              int64_t D_out, int8_t* x_q, float* x_scales, int8_t* w_q,
+                              float* w_scales, float* y, int32_t* acc, void* workspace,
+                              size_t workspace_bytes, bsmm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* MXFP8 linear-layer backward                                              */
+/* ------------------------------------------------------------------------ */
+
+/* [NKI] introduction: forward Y = X W^T with X [M,K], W [N,K], Y [M,N];
+ * backward dX = dY W ([M,K], contraction over N) and dW = dY^T X ([N,K],
+ * contraction over M).  Every operand is MXFP8-quantized (UE8M0 scale per 32
+ * elements, rule as in bsmm_quantize) along its own contraction axis: dY
+ * and W along N for dX; dY and X along M for dW.  fp8_type is E5M2 (the
+ * page's default) or E4M3.  Outputs are bfloat16 (round to nearest even).
+ *
+ *   dY [M, N], W [N, K], X [M, K] bfloat16, contiguous.
+ *   dX [M, K], dW [N, K] bfloat16, contiguous.
+ *   workspace  at least bsmm_linear_backward_workspace_size() bytes (the
+ *            four quantized operands and their scales).
+ *   M, N and K must be multiples of 32.
+ */
+size_t bsmm_linear_backward_workspace_size(int64_t M, int64_t N, int64_t K);
+
+bsmm_status bsmm_linear_backward(const void* dY, const void* W, const void* X, int64_t M,
+                                 int64_t N, int64_t K, bsmm_dtype fp8_type, void* dX, void* dW,
+                                 void* workspace, size_t workspace_bytes, bsmm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSMM_H_ */

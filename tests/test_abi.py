@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads and exports every entry point the header
+declares; argument validation and the workspace queries run without a GPU
+(they return before any CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "bsmm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_scaled_precision_gemm_gb300 as bsmm
+    return bsmm.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsmm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("bsmm_quantize", "bsmm_gemm", "bsmm_gemm_grouped", "bsmm_int8_channel", "bsmm_linear_backward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_error_string(lib):
+    assert lib.bsmm_version() >= 100
+    assert isinstance(lib.bsmm_last_error(), bytes)
+
+
+def test_validation_without_gpu(lib):
+    import block_scaled_precision_gemm_gb300 as b
+    P = ctypes.c_void_p
+    fake = P(4096)
+    # K not a multiple of the scale count
+    st = lib.bsmm_gemm(1, 128, 128, 100, fake, b.E4M3, fake, b.E4M3, fake, 3, fake, 4, b.SCALE_UE8M0, fake, b.F32,
+                       fake, 1 << 20, None)
+    assert st == b.ERR_SHAPE
+    # block size 16 with UE8M0 scales: valid definition, no kernel (jax cuDNN example shapes)
+    st = lib.bsmm_gemm(3, 128, 128, 64, fake, b.E4M3, fake, b.E4M3, fake, 4, fake, 4, b.SCALE_UE8M0, fake, b.F32,
+                       fake, 1 << 20, None)
+    assert st == b.ERR_UNSUPPORTED
+    assert b"UE8M0" in lib.bsmm_last_error()
+    # grouped: n not a multiple of group_n; group other than 128
+    assert lib.bsmm_gemm_grouped(64, 200, 256, fake, b.E4M3, fake, b.E4M3, fake, fake, 128, 128, fake,
+                                 None) == b.ERR_SHAPE
+    assert lib.bsmm_gemm_grouped(64, 256, 256, fake, b.E4M3, fake, b.E4M3, fake, fake, 64, 64, fake,
+                                 None) == b.ERR_UNSUPPORTED
+    # quantize: INT8 needs F32 scales; bad enums; indivisible blocks
+    assert lib.bsmm_quantize(fake, b.F32, 4, 32, 32, 1, 32, b.INT8, b.SCALE_UE8M0, 0, fake, 32, fake, 1,
+                             None) == b.ERR_UNSUPPORTED
+    assert lib.bsmm_quantize(fake, 9, 4, 32, 32, 1, 32, b.E4M3, b.SCALE_F32, 0, fake, 32, fake, 1,
+                             None) == b.ERR_INVALID_ARG
+    assert lib.bsmm_quantize(fake, b.F32, 4, 33, 33, 1, 32, b.E4M3, b.SCALE_F32, 0, fake, 33, fake, 1,
+                             None) == b.ERR_SHAPE
+    # zero-sized problems are OK and launch nothing
+    assert lib.bsmm_gemm_grouped(0, 256, 256, None, b.E4M3, None, b.E4M3, None, None, 128, 128, None, None) == b.OK
+    assert lib.bsmm_gemm(1, 0, 128, 64, None, b.E4M3, None, b.E4M3, None, 2, None, 2, b.SCALE_UE8M0, None, b.F32,
+                         None, 0, None) == b.OK
+    # missing workspace is reported before any launch
+    st = lib.bsmm_gemm(1, 128, 128, 64, fake, b.E4M3, fake, b.E4M3, fake, 2, fake, 2, b.SCALE_UE8M0, fake, b.F32,
+                       None, 0, None)
+    assert st == b.ERR_WORKSPACE
+    # backward needs multiples of 32
+    assert lib.bsmm_linear_backward(fake, fake, fake, 33, 64, 64, b.E5M2, fake, fake, fake, 1 << 30,
+                                    None) == b.ERR_SHAPE
+
+
+def test_workspace_queries(lib):
+    import block_scaled_precision_gemm_gb300 as b
+    # scale atoms: 512 B per (row tile of 128, rounded to pairs) per K atom
+    assert lib.bsmm_gemm_workspace_size(1, 128, 128, 128, b.E4M3) == 2 * (2 * 512)
+    assert lib.bsmm_gemm_workspace_size(8, 4096, 4096, 8192, b.E4M3) == 2 * 8 * 32 * 64 * 512
+    assert lib.bsmm_gemm_workspace_size(1, 16384, 16384, 16384, b.E2M1) == 2 * 128 * 256 * 512
+    assert lib.bsmm_int8_channel_workspace_size(1, 3, 2) > 0
+    assert lib.bsmm_linear_backward_workspace_size(64, 64, 64) > 4 * 64 * 64

@@ -1,0 +1,222 @@
+"""GPU GEMMs vs the oracle on small shapes that span several tiles and ragged
+tails.  Inputs (codes and scales) come from the oracle's codec applied to
+seeded draws, so the GEMMs are checked independently of the GPU quantizer.
+Gate: |y - y_ref| <= 2e-3 * sum_k |a_s * b_s| per entry; bf16 outputs may
+additionally move by their own rounding, half a bf16 ulp (2^-8 |y_ref|)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import gemm as G
+from oracle import quantize as Q
+
+pytestmark = pytest.mark.gpu
+REL = 2e-3
+
+
+def _bsmm():
+    import block_scaled_precision_gemm_gb300 as bsmm
+    return bsmm
+
+
+def assert_within(y, y_ref, bound, what, out_round=0.0):
+    y = np.asarray(y, np.float64)
+    ok = G.within_bound(y, y_ref, bound, REL, out_round)
+    if not ok.all():
+        idx = np.argwhere(~ok)[:5]
+        raise AssertionError(f"{what}: {(~ok).sum()}/{ok.size} entries outside the bound; first {idx.tolist()}: "
+                             f"y={y[tuple(idx[0])]} ref={y_ref[tuple(idx[0])]} bound={bound[tuple(idx[0])]}")
+
+
+# ---------------------------------------------------------------------------
+# block_scaled_mm: 1x128 activation and 128x128 weight FP32 scales
+# ---------------------------------------------------------------------------
+
+def grouped_inputs(m, n, k, seed, code="e4m3"):
+    g = torch.Generator().manual_seed(seed)
+    a_raw = torch.randn(m, k, generator=g).numpy()
+    b_raw = torch.randn(n, k, generator=g).numpy()
+    ca, sa = Q.quantize(a_raw, (1, 128), code, "f32")
+    cb, sb = Q.quantize(b_raw, (128, 128), code, "f32")
+    return ca, sa, cb, sb
+
+
+def run_grouped(ca, sa, cb, sb, code="e4m3", bcode=None):
+    bsmm = _bsmm()
+    bcode = bcode or code
+    y = bsmm.gemm_grouped(torch.from_numpy(ca).cuda(), torch.from_numpy(cb).cuda(), torch.from_numpy(sa).cuda(),
+                          torch.from_numpy(sb).cuda(), 128, 128, a_type=code, b_type=bcode)
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    da, db = F.decode(ca, code), F.decode(cb, bcode)
+    y_ref = G.grouped_matmul(da, db, sa, sb, 128, 128)
+    a_s, b_s = G.grouped_operands(da, db, sa, sb, 128, 128)
+    return y.cpu().numpy(), y_ref, np.abs(a_s) @ np.abs(b_s).T
+
+
+@pytest.mark.parametrize("m,n,k", [(64, 256, 256), (1, 128, 128), (237, 256, 384), (349, 384, 256),
+                                   (300, 640, 1024), (129, 128, 2048)])
+def test_grouped_parity(m, n, k):
+    y, y_ref, bound = run_grouped(*grouped_inputs(m, n, k, seed=m + n + k))
+    assert_within(y, y_ref, bound, f"grouped m={m} n={n} k={k}")
+
+
+def test_grouped_e5m2_operands():
+    ca, sa, _, _ = grouped_inputs(100, 256, 256, 5, "e5m2")
+    _, _, cb, sb = grouped_inputs(100, 256, 256, 6, "e4m3")
+    y, y_ref, bound = run_grouped(ca, sa, cb, sb, "e5m2", "e4m3")
+    assert_within(y, y_ref, bound, "grouped e5m2 x e4m3")
+
+
+def test_grouped_one_hot_scales():
+    """Only one (row, K block) scale and one (n group, K block) scale are
+    nonzero: pins the scale indexing of the promotion epilogue."""
+    m, n, k = 256, 384, 512
+    ca, sa, cb, sb = grouped_inputs(m, n, k, 9)
+    sa = np.zeros_like(sa)
+    sb = np.zeros_like(sb)
+    for r in range(m):
+        sa[r, r % 4] = 1.0 + r / 1000
+    sb[1, 2] = 0.5
+    sb[2, 3] = 2.0
+    y, y_ref, bound = run_grouped(ca, sa, cb, sb)
+    assert_within(y, y_ref, bound, "one-hot scales")
+    assert np.count_nonzero(y_ref) > 0 and (y[:, :128] == 0).all()
+
+
+def test_grouped_end_to_end_with_gpu_quantizer():
+    bsmm = _bsmm()
+    g = torch.Generator().manual_seed(3)
+    a_raw = torch.randn(237, 1024, generator=g)
+    b_raw = torch.randn(512, 1024, generator=g)
+    aq, sa = bsmm.quantize(a_raw.cuda(), (1, 128), "e4m3", "f32")
+    bq, sb = bsmm.quantize(b_raw.cuda(), (128, 128), "e4m3", "f32")
+    y = bsmm.gemm_grouped(aq, bq, sa, sb).cpu().numpy()
+    ca, osa = Q.quantize(a_raw.numpy(), (1, 128), "e4m3", "f32")
+    cb, osb = Q.quantize(b_raw.numpy(), (128, 128), "e4m3", "f32")
+    np.testing.assert_array_equal(aq.cpu().numpy(), ca)
+    np.testing.assert_array_equal(bq.cpu().numpy(), cb)
+    da, db = F.decode(ca, "e4m3"), F.decode(cb, "e4m3")
+    a_s, b_s = G.grouped_operands(da, db, osa, osb, 128, 128)
+    assert_within(y, G.grouped_matmul(da, db, osa, osb, 128, 128), np.abs(a_s) @ np.abs(b_s).T, "end to end")
+
+
+# ---------------------------------------------------------------------------
+# batched MXFP8 / NVFP4 (jax.nn.scaled_matmul with the Blackwell formats)
+# ---------------------------------------------------------------------------
+
+def mx_inputs(Bn, M, N, K, at, bt, seed, pattern="random"):
+    g = torch.Generator().manual_seed(seed)
+    ca = F.encode(torch.randn(Bn, M, K, generator=g).numpy(), at)
+    cb = F.encode(torch.randn(Bn, N, K, generator=g).numpy(), bt)
+    ea = torch.randint(-6, 7, (Bn, M, K // 32), generator=g).numpy()
+    eb = torch.randint(-6, 7, (Bn, N, K // 32), generator=g).numpy()
+    if pattern == "one_hot_a":     # row m keeps only K block (m % KS); others ~2^-127
+        ks = K // 32
+        ea = np.full_like(ea, -127)
+        for r in range(M):
+            ea[:, r, r % ks] = (r % 5) - 2
+    elif pattern == "one_hot_b":
+        ks = K // 32
+        eb = np.full_like(eb, -127)
+        for r in range(N):
+            eb[:, r, (3 * r + 1) % ks] = (r % 3) - 1
+    return ca, cb, (ea + 127).astype(np.uint8), (eb + 127).astype(np.uint8)
+
+
+def run_mx(Bn, M, N, K, at, bt, out, seed, pattern="random"):
+    bsmm = _bsmm()
+    ca, cb, sa, sb = mx_inputs(Bn, M, N, K, at, bt, seed, pattern)
+    t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()  # noqa: E731
+    y = bsmm.gemm(t(ca), t(cb), t(sa), t(sb), at, bt, "ue8m0", out_dtype=out)
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    da, db = F.decode(ca, at), F.decode(cb, bt)
+    dsa, dsb = F.decode(sa, "ue8m0"), F.decode(sb, "ue8m0")
+    y_ref = G.scaled_matmul(da, db, dsa, dsb)
+    bound = G.scaled_matmul_bound(da, db, dsa, dsb)
+    assert_within(y.float().cpu().numpy(), y_ref, bound, f"mxfp8 {Bn}x{M}x{N}x{K} {at}x{bt} {out} {pattern}",
+                  G.BF16_HALF_ULP if out == torch.bfloat16 else 0.0)
+    return y
+
+
+@pytest.mark.parametrize("Bn,M,N,K", [(1, 128, 128, 128), (2, 200, 136, 256), (1, 64, 256, 96),
+                                      (3, 130, 250, 512), (1, 300, 384, 1024)])
+def test_mxfp8_parity(Bn, M, N, K):
+    run_mx(Bn, M, N, K, "e4m3", "e4m3", torch.float32, seed=M + N + K)
+
+
+@pytest.mark.parametrize("at,bt", [("e5m2", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e5m2")])
+def test_mxfp8_mixed_formats(at, bt):
+    run_mx(2, 160, 192, 256, at, bt, torch.float32, seed=31)
+
+
+@pytest.mark.parametrize("N", [136, 250])
+def test_mxfp8_bf16_output(N):
+    """bf16 output = round-to-nearest-even of the same product in FP32, bit
+    for bit, and within the bound plus bf16's own half-ulp rounding."""
+    y16 = run_mx(2, 200, N, 512, "e5m2", "e5m2", torch.bfloat16, seed=N)
+    y32 = run_mx(2, 200, N, 512, "e5m2", "e5m2", torch.float32, seed=N)
+    assert torch.equal(y16.cpu().view(torch.int16), y32.cpu().to(torch.bfloat16).view(torch.int16))
+
+
+@pytest.mark.parametrize("pattern", ["one_hot_a", "one_hot_b"])
+def test_mxfp8_scale_layout_one_hot(pattern):
+    run_mx(1, 256, 256, 512, "e4m3", "e4m3", torch.float32, seed=41, pattern=pattern)
+
+
+def nv_inputs(Bn, M, N, K, seed, pattern="random"):
+    g = torch.Generator().manual_seed(seed)
+    a = torch.randint(0, 256, (Bn, M, K // 2), generator=g, dtype=torch.int32).numpy().astype(np.uint8)
+    b = torch.randint(0, 256, (Bn, N, K // 2), generator=g, dtype=torch.int32).numpy().astype(np.uint8)
+    sa_v = np.exp2(torch.empty(Bn, M, K // 16).uniform_(-4, 4, generator=g).numpy())
+    sb_v = np.exp2(torch.empty(Bn, N, K // 16).uniform_(-4, 4, generator=g).numpy())
+    sa, sb = F.encode(sa_v, "ue4m3"), F.encode(sb_v, "ue4m3")
+    if pattern == "one_hot_a":
+        ks = K // 16
+        sa = np.zeros_like(sa)
+        for r in range(M):
+            sa[:, r, (r * 7) % ks] = 0x38
+    return a, b, sa, sb
+
+
+@pytest.mark.parametrize("Bn,M,N,K,pattern", [(1, 128, 128, 256, "random"), (2, 200, 136, 512, "random"),
+                                              (1, 64, 128, 64, "random"), (1, 256, 384, 1024, "random"),
+                                              (1, 256, 256, 512, "one_hot_a")])
+def test_nvfp4_parity(Bn, M, N, K, pattern):
+    bsmm = _bsmm()
+    a, b, sa, sb = nv_inputs(Bn, M, N, K, seed=M + K, pattern=pattern)
+    t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()  # noqa: E731
+    y = bsmm.gemm(t(a), t(b), t(sa), t(sb), "e2m1", "e2m1", "ue4m3")
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    da, db = F.decode(F.unpack_e2m1(a), "e2m1"), F.decode(F.unpack_e2m1(b), "e2m1")
+    dsa, dsb = F.decode(sa, "ue4m3"), F.decode(sb, "ue4m3")
+    y_ref = G.scaled_matmul(da, db, dsa, dsb)
+    bound = G.scaled_matmul_bound(da, db, dsa, dsb)
+    assert_within(y.cpu().numpy(), y_ref, bound, f"nvfp4 {Bn}x{M}x{N}x{K} {pattern}")
+
+
+def test_jax_basic_case_padded_to_a_hardware_block():
+    """[1,2,3].[4,5,6] with both scales 0.5 is 8: padded with zero codes to
+    K = 32 (one UE8M0 block, scale 2^-1)."""
+    bsmm = _bsmm()
+    a = np.zeros((1, 1, 32), np.float32); a[0, 0, :3] = [1, 2, 3]
+    b = np.zeros((1, 1, 32), np.float32); b[0, 0, :3] = [4, 5, 6]
+    t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()  # noqa: E731
+    s = np.full((1, 1, 1), 126, np.uint8)
+    y = bsmm.gemm(t(F.encode(a, "e4m3")), t(F.encode(b, "e4m3")), t(s), t(s), "e4m3", "e4m3", "ue8m0")
+    assert y.cpu().item() == 8.0
+
+
+def test_unsupported_block_16_with_ue8m0_is_reported():
+    """The jax cuDNN example's shapes (3,128,64) with (3,128,4) E8M0 scales
+    imply a block of 16, which the hardware MXFP8 path does not take."""
+    bsmm = _bsmm()
+    a = torch.zeros((3, 128, 64), dtype=torch.uint8, device="cuda")
+    s = torch.full((3, 128, 4), 127, dtype=torch.uint8, device="cuda")
+    with pytest.raises(bsmm.BsmmError) as e:
+        bsmm.gemm(a, a, s, s, "e4m3", "e4m3", "ue8m0")
+    assert e.value.status == bsmm.ERR_UNSUPPORTED

@@ -1,0 +1,144 @@
+"""GPU INT8 per-channel matmul and MXFP8 linear backward vs the oracle, and
+the bounded-wait timeout path."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import gemm as G
+from tests.conftest import GOLDEN
+
+pytestmark = pytest.mark.gpu
+
+
+def _bsmm():
+    import block_scaled_precision_gemm_gb300 as bsmm
+    return bsmm
+
+
+def run_int8(x, w):
+    bsmm = _bsmm()
+    out = bsmm.int8_channel(torch.from_numpy(x).cuda(), torch.from_numpy(w).cuda(), return_acc=True)
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    ref = G.int8_channel(x, w)
+    np.testing.assert_array_equal(got["x_q"], ref["x_q"])
+    np.testing.assert_array_equal(got["w_q"], ref["w_q"])
+    np.testing.assert_array_equal(got["x_scales"].view(np.uint32), ref["x_scales"].view(np.uint32))
+    np.testing.assert_array_equal(got["w_scales"].view(np.uint32), ref["w_scales"].view(np.uint32))
+    np.testing.assert_array_equal(got["acc"].astype(np.int64), ref["acc"])
+    # TensorTonic checker: relative 1e-6 of acc*sx*sw in float64; zero sum -> exactly 0
+    y = got["y"].astype(np.float64)
+    assert (np.abs(y - ref["y_ref"]) <= 1e-6 * np.abs(ref["y_ref"])).all()
+    assert (got["y"][ref["acc"] == 0] == 0).all()
+    return got
+
+
+@pytest.mark.parametrize("i", [0, 1, 2])
+def test_int8_worked_examples(i):
+    with open(os.path.join(GOLDEN, "int8_per_channel_examples.json")) as f:
+        ex = json.load(f)["examples"][i]
+    got = run_int8(np.array(ex["x"], np.float32), np.array(ex["w"], np.float32))
+    np.testing.assert_array_equal(got["x_q"], ex["x_q"])
+    np.testing.assert_array_equal(got["w_q"], ex["w_q"])
+    np.testing.assert_allclose(got["y"], ex["y"], rtol=0, atol=0.5e-6)
+
+
+@pytest.mark.parametrize("B,D_in,D_out", [(100, 300, 70), (129, 256, 200), (6, 64, 6), (257, 1000, 130)])
+def test_int8_random_with_zero_lines(B, D_in, D_out):
+    g = torch.Generator().manual_seed(B + D_in)
+    x = torch.randn(B, D_in, generator=g).numpy()
+    w = torch.randn(D_in, D_out, generator=g).numpy()
+    x[B // 2] = 0
+    w[:, D_out // 3] = 0
+    run_int8(x, w)
+
+
+def test_int8_extreme_sums_stay_exact():
+    """All codes +-127: |sum| = D_in * 16129 (the page's constraint scaled
+    to D_in = 4096 is 66,064,384 < 2^31)."""
+    x = np.ones((130, 4096), np.float32)
+    w = np.ones((4096, 129), np.float32)
+    w[:, 1::2] = -1
+    got = run_int8(x, w)
+    assert got["acc"][0, 0] == 4096 * 127 * 127 and got["acc"][0, 1] == -4096 * 127 * 127
+
+
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
+
+
+def run_backward(dY, W, X, fp8="e5m2"):
+    bsmm = _bsmm()
+    tdY, tW, tX = _bf16(dY), _bf16(W), _bf16(X)
+    dX, dW = bsmm.linear_backward(tdY.cuda(), tW.cuda(), tX.cuda(), fp8)
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    ref = G.linear_backward(tdY.float().numpy(), tW.float().numpy(), tX.float().numpy(), fp8)
+    return dX.float().cpu().numpy(), dW.float().cpu().numpy(), ref
+
+
+def test_backward_exact_on_representable_inputs():
+    rng = np.random.default_rng(12)
+    M, N, K = 64, 96, 32
+    dY = rng.integers(-2, 3, (M, N)).astype(np.float32)
+    W = rng.integers(-2, 3, (N, K)).astype(np.float32)
+    X = rng.integers(-2, 3, (M, K)).astype(np.float32)
+    dX, dW, _ = run_backward(dY, W, X)
+    np.testing.assert_array_equal(dX, dY @ W)
+    np.testing.assert_array_equal(dW, dY.T @ X)
+
+
+@pytest.mark.parametrize("M,N,K,fp8", [(128, 96, 160, "e5m2"), (256, 384, 128, "e5m2"), (96, 64, 320, "e4m3")])
+def test_backward_parity(M, N, K, fp8):
+    g = torch.Generator().manual_seed(M + N + K)
+    dY = torch.randn(M, N, generator=g).numpy()
+    W = (torch.randn(N, K, generator=g) * 0.02).numpy()
+    X = (torch.randn(M, K, generator=g) * 0.02).numpy()
+    dX, dW, ref = run_backward(dY, W, X, fp8)
+    for got, y_ref, bound, name in ((dX, ref["dX"], ref["dX_bound"], "dX"), (dW, ref["dW"], ref["dW_bound"], "dW")):
+        ok = G.within_bound(got, y_ref, bound, out_round=G.BF16_HALF_ULP)
+        assert ok.all(), f"{name}: {(~ok).sum()} entries outside the bound"
+
+
+def test_backward_quantized_operands_match_oracle():
+    """The four MXFP8 operands the backward builds (quantizer with the same
+    arguments) are bit-exact against the oracle's."""
+    bsmm = _bsmm()
+    g = torch.Generator().manual_seed(77)
+    M, N, K = 96, 64, 128
+    dY = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)
+    X = (torch.randn(M, K, generator=g) * 0.02).to(torch.bfloat16)
+    ref = G.linear_backward(dY.float().numpy(), W.float().numpy(), X.float().numpy())
+    c, s = bsmm.quantize(X.cuda(), (32, 1), "e5m2", "ue8m0", transpose=True)
+    np.testing.assert_array_equal(c.cpu().numpy(), ref["xt"])
+    np.testing.assert_array_equal(s.cpu().numpy(), ref["xt_s"])
+    c, s = bsmm.quantize(dY.cuda(), (1, 32), "e5m2", "ue8m0")
+    np.testing.assert_array_equal(c.cpu().numpy(), ref["dy_n"])
+    np.testing.assert_array_equal(s.cpu().numpy(), ref["dy_n_s"])
+    c, s = bsmm.quantize(W.cuda(), (32, 1), "e5m2", "ue8m0", transpose=True)
+    np.testing.assert_array_equal(c.cpu().numpy(), ref["wt"])
+    np.testing.assert_array_equal(s.cpu().numpy(), ref["wt_s"])
+    c, s = bsmm.quantize(dY.cuda(), (32, 1), "e5m2", "ue8m0", transpose=True)
+    np.testing.assert_array_equal(c.cpu().numpy(), ref["dyt"])
+    np.testing.assert_array_equal(s.cpu().numpy(), ref["dyt_s"])
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    bsmm = _bsmm()
+    assert bsmm.check_device_status()[0] == 0
+    bsmm.selftest_wait_timeout(20_000_000)  # 20 ms, on a barrier nothing arrives on
+    st, site = bsmm.check_device_status()
+    assert st == bsmm.ERR_TIMEOUT and site == 7
+    assert bsmm.check_device_status()[0] == 0          # cleared
+    # the context is still usable
+    a = torch.zeros((1, 32), dtype=torch.uint8, device="cuda")
+    s = torch.full((1, 1), 127, dtype=torch.uint8, device="cuda")
+    y = bsmm.gemm(a, a, s, s, "e4m3", "e4m3", "ue8m0")
+    assert y.cpu().item() == 0.0

@@ -1,0 +1,101 @@
+"""GPU quantizer vs the oracle: codes and scales must be bit-exact.
+
+Inputs are seeded normals with per-row magnitudes spread over e^[-3,3], plus
+the degenerate cases of the method: an all-zero row and column, negative
+zeros, quotients deep in the subnormal range and one value near the binary32
+maximum."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import quantize as Q
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def make_x(rows, cols, seed, dtype):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, cols, generator=g) * torch.exp(torch.empty(rows, 1).uniform_(-3, 3, generator=g))
+    x[1] = 0.0
+    x[:, 1] = 0.0
+    x[2] *= 1e-36
+    x[3, 5] = 3.0e38
+    x[4, ::7] = -0.0
+    return x.to(DT[dtype])
+
+
+def oracle_quantize(x, block, code, scale, transpose):
+    return Q.quantize(x.float().numpy(), block, code, scale, transpose_out=transpose)
+
+
+def run_case(rows, cols, block, code, scale, dtype, transpose, seed):
+    import block_scaled_precision_gemm_gb300 as bsmm
+    x = make_x(rows, cols, seed, dtype)
+    codes, scales = bsmm.quantize(x.cuda(), block, code, scale, transpose=transpose)
+    torch.cuda.synchronize()
+    rc, rs = oracle_quantize(x, block, code, scale, transpose)
+    got_c = codes.cpu().numpy()
+    if code == "int8":
+        got_c = got_c.astype(np.int8)
+    np.testing.assert_array_equal(got_c, rc)
+    got_s = scales.cpu().numpy()
+    if scale == "f32":
+        np.testing.assert_array_equal(got_s.view(np.uint32), np.asarray(rs, np.float32).view(np.uint32))
+    else:
+        np.testing.assert_array_equal(got_s, rs)
+    assert bsmm.check_device_status()[0] == 0
+
+
+FORMATS = [("e4m3", "f32"), ("e5m2", "f32"), ("int8", "f32"), ("e4m3", "ue8m0"), ("e5m2", "ue8m0"),
+           ("e2m1", "ue8m0"), ("e2m1", "ue4m3"), ("e4m3", "ue4m3")]
+
+
+@pytest.mark.parametrize("code,scale", FORMATS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("bc", [16, 32, 128])
+def test_row_blocks(code, scale, dtype, bc):
+    run_case(160, 384, (1, bc), code, scale, dtype, False, seed=bc)
+
+
+@pytest.mark.parametrize("code,scale", FORMATS)
+@pytest.mark.parametrize("br,rows", [(16, 144), (32, 160), (128, 256)])
+@pytest.mark.parametrize("transpose", [False, True])
+def test_col_blocks(code, scale, br, rows, transpose):
+    run_case(rows, 200, (br, 1), code, scale, "bf16" if br == 32 else "f32", transpose, seed=br + rows)
+
+
+@pytest.mark.parametrize("code,scale", [("e4m3", "f32"), ("e2m1", "ue4m3"), ("e5m2", "ue8m0")])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tile_blocks_128x128(code, scale, dtype):
+    run_case(256, 384, (128, 128), code, scale, dtype, False, seed=7)
+
+
+@pytest.mark.parametrize("code,scale", [("int8", "f32"), ("e4m3", "ue8m0"), ("e2m1", "ue4m3")])
+def test_whole_row_and_column_blocks(code, scale):
+    run_case(37, 250, (1, 250), code, scale, "f32", False, seed=11)
+    run_case(38, 70, (38, 1), code, scale, "f32", False, seed=12)
+    run_case(38, 70, (38, 1), code, scale, "f32", True, seed=13)
+
+
+@pytest.mark.parametrize("block", [(2, 4), (4, 2), (1, 6), (3, 1)])
+def test_other_block_shapes(block):
+    run_case(12, 24, block, "e4m3", "f32", "f32", False, seed=17)
+    if block[1] == 1:
+        run_case(12, 24, block, "e5m2", "ue8m0", "f32", True, seed=18)
+
+
+def test_atrex_recipe_full_width():
+    """The block_scaled_mm activation/weight recipe at n = k = 2048 widths."""
+    run_case(349, 2048, (1, 128), "e4m3", "f32", "f32", False, seed=21)
+    run_case(256, 2048, (128, 128), "e4m3", "f32", "f32", False, seed=22)
+
+
+def test_empty_input_launches_nothing():
+    import block_scaled_precision_gemm_gb300 as bsmm
+    x = torch.empty((0, 128), device="cuda")
+    c, s = bsmm.quantize(x, (1, 128), "e4m3", "f32")
+    assert c.shape == (0, 128) and s.shape == (0, 1)
