@@ -67,10 +67,11 @@ struct Cfg {
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_STG = align1024(OFF_SF + STAGES * SF_BYTES);
   static constexpr int OFF_BAR = OFF_STG + kEpiWarps * kStagingPerWarp;
-  static constexpr int N_BARS = 2 * STAGES + 4 + 1;
+  static constexpr int N_BARS = 2 * STAGES + 2 * 4 + 1;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;  // + alignment slack
-  // tensor-memory columns
-  static constexpr int SF_COL0 = 2 * BN;
+  // tensor-memory columns: NACC accumulators of BN columns, then scale factors
+  static constexpr int NACC = MODE == kF32Scale ? kTmemCols / BN : 2;
+  static constexpr int SF_COL0 = NACC * BN;
   static constexpr int SFA_COLS = ATOMS * 4;
   static constexpr int SFB_COLS = ATOMS * 4 * (BN / 128);
   static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* done = tempty + 2;
+  uint64_t* tempty = tfull + C::NACC;
+  uint64_t* done = tempty + C::NACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int never_abort_storage = 0;  // drains ignore the CTA abort flag
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NACC; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], kEpiWarps);
     }
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          k > 0 ? 1u : 0u);
             tc_commit(&empty[stage]);
             tc_commit(&tfull[tb]);
-            if (++tb == 2) {
+            if (++tb == C::NACC) {
               tb = 0;
               tph ^= 1u;
             }
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (MODE != kF32Scale) {
           if (!ok) break;
           tc_commit(&tfull[tb]);
-          if (++tb == 2) {
+          if (++tb == C::NACC) {
             tb = 0;
             tph ^= 1u;
           }
@@ -313,27 +314,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* sa_row = p.a_scales + static_cast<size_t>(row_ok ? row : 0) * p.kb;
         const float* sb_row = p.b_scales + static_cast<size_t>(col0 / 128) * p.kb;
         float sa_next = row_ok ? __ldg(sa_row) : 0.f;
+        float sb_next = __ldg(sb_row);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          const float s = sa_next * __ldg(sb_row + kt);
-          if (kt + 1 < p.k_tiles) sa_next = row_ok ? __ldg(sa_row + kt + 1) : 0.f;
+          const float s = sa_next * sb_next;
+          if (kt + 1 < p.k_tiles) {
+            sa_next = row_ok ? __ldg(sa_row + kt + 1) : 0.f;
+            sb_next = __ldg(sb_row + kt + 1);
+          }
           if (!mbar_wait(&tfull[tb], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(tb * BN + g * COLS);
+          static_assert(COLS == 64, "promotion epilogue reads two 32-column chunks");
+          uint32_t r0[32], r1[32];
+          tmem_ld32(taddr, r0);
+          tmem_ld32(taddr + 32, r1);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < COLS / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(taddr + 32 * c, r);
-            tmem_wait_ld();
+          for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(r0[j]), s, acc[j]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(__uint_as_float(r[j]), s, acc[32 * c + j]);
-          }
+          for (int j = 0; j < 32; ++j) acc[32 + j] = fmaf(__uint_as_float(r1[j]), s, acc[32 + j]);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[tb]);
-          if (++tb == 2) {
+          if (++tb == C::NACC) {
             tb = 0;
             tph ^= 1u;
           }
@@ -355,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[tb]);
-          if (++tb == 2) {
+          if (++tb == C::NACC) {
             tb = 0;
             tph ^= 1u;
           }

@@ -176,14 +176,21 @@ __global__ void __launch_bounds__(256) quant_rows(QP p) {
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int64_t chunk = nw * 32;
   const bool fp4 = p.code == BSMM_E2M1;
+  // Dense arrays (pitches equal to the widths) need no row/column split.
+  const bool dense = p.ld_x == p.cols && p.ld_codes == p.cols && p.ld_scales * p.bc == p.cols;
+  const int bc_shift = __ffs(p.bc) - 1;  // bc is a power of two
   for (int64_t base = warp * 32; base < total; base += chunk * kRowsUnroll) {
     float v[kRowsUnroll][VEC];
 #pragma unroll
     for (int u = 0; u < kRowsUnroll; ++u) {
       const int64_t vi = base + u * chunk + lane;
       if (vi < total) {
-        const int64_t r = vi / vpr, c = vi - r * vpr;
-        load_vec<In>(reinterpret_cast<const In*>(p.x) + r * p.ld_x + c * VEC, v[u]);
+        int64_t off = vi * VEC;
+        if (!dense) {
+          const int64_t r = vi / vpr, c = vi - r * vpr;
+          off = r * p.ld_x + c * VEC;
+        }
+        load_vec<In>(reinterpret_cast<const In*>(p.x) + off, v[u]);
       } else {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) v[u][i] = 0.f;
@@ -198,10 +205,14 @@ __global__ void __launch_bounds__(256) quant_rows(QP p) {
       for (int o = G >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (vi >= total) continue;
       const Scale sc = make_scale(m, p.code, p.scale);
-      const int64_t r = vi / vpr, c = vi - r * vpr;
-      if ((lane & (G - 1)) == 0) store_scale(p.scales, r * p.ld_scales + (c * VEC) / p.bc, p.scale, sc.stored);
+      int64_t e = vi * VEC, sidx = e >> bc_shift;  // element offset, scale index (dense)
+      if (!dense) {
+        const int64_t r = vi / vpr, c = vi - r * vpr;
+        e = r * p.ld_codes + c * VEC;
+        sidx = r * p.ld_scales + (c * VEC) / p.bc;
+      }
+      if ((lane & (G - 1)) == 0) store_scale(p.scales, sidx, p.scale, sc.stored);
       const uint32_t w0 = encode4(v[u][0], v[u][1], v[u][2], v[u][3], sc.s, p.code);
-      const int64_t e = r * p.ld_codes + c * VEC;  // element offset
       uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
       if constexpr (VEC == 4) {
         if (fp4)
