@@ -26,7 +26,7 @@ import os
 import torch
 
 __all__ = [
-    "BsmmError", "lib", "library_path", "quantize", "gemm", "gemm_grouped", "int8_channel",
+    "BsmmError", "lib", "library_path", "quantize", "gemm", "gemm_noalloc", "gemm_grouped", "int8_channel",
     "linear_backward", "gemm_workspace_size", "int8_channel_workspace_size",
     "linear_backward_workspace_size", "check_device_status", "selftest_wait_timeout",
     "set_wait_timeout_ns", "version",
@@ -69,6 +69,8 @@ _SIGS = {
     "bsmm_gemm_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
     "bsmm_gemm": ([_I64, _I64, _I64, _I64, _P, _INT, _P, _INT, _P, _I64, _P, _I64, _INT, _P, _INT, _P, _SZ, _P],
                   _INT),
+    "bsmm_gemm_noalloc": ([_I64, _I64, _I64, _I64, _P, _INT, _P, _INT, _P, _I64, _P, _I64, _INT, _P, _INT, _P],
+                          _INT),
     "bsmm_gemm_grouped": ([_I64, _I64, _I64, _P, _INT, _P, _INT, _P, _P, _INT, _INT, _P, _P], _INT),
     "bsmm_int8_channel_workspace_size": ([_I64, _I64, _I64], _SZ),
     "bsmm_int8_channel": ([_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _INT),
@@ -206,6 +208,31 @@ def gemm(a, b, a_scales, b_scales, a_type="e4m3", b_type="e4m3", scale="ue8m0", 
                            _ptr(b_scales), b_scales.shape[-1], _scale(scale), _ptr(y),
                            BF16 if y.dtype == torch.bfloat16 else F32, _ptr(workspace), workspace.numel(),
                            _stream(stream)), "bsmm_gemm")
+    return y
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def gemm_noalloc(a, b, a_scales, b_scales, a_type="e4m3", b_type="e4m3", scale="ue8m0", y=None, K=None,
+                 stream=None):
+    """:func:`gemm` through the entry point that allocates nothing: its
+    scratch is a static device array of NOALLOC_SCRATCH_BYTES inside the
+    library (for callers that cannot allocate device memory).  ``y`` must be
+    given; this wrapper allocates nothing either."""
+    for t, n in ((a, "a"), (b, "b"), (a_scales, "a_scales"), (b_scales, "b_scales"), (y, "y")):
+        _dev(t, n)
+    at, bt = _code(a_type), _code(b_type)
+    if a.dim() == 2:
+        a, b, a_scales, b_scales = a[None], b[None], a_scales[None], b_scales[None]
+    Bn, M, ka = a.shape
+    N = b.shape[1]
+    if K is None:
+        K = ka * 2 if at == E2M1 else ka
+    _check(lib().bsmm_gemm_noalloc(Bn, M, N, K, _ptr(a), at, _ptr(b), bt, _ptr(a_scales), a_scales.shape[-1],
+                                   _ptr(b_scales), b_scales.shape[-1], _scale(scale), _ptr(y),
+                                   BF16 if y.dtype == torch.bfloat16 else F32, _stream(stream)),
+           "bsmm_gemm_noalloc")
     return y
 
 

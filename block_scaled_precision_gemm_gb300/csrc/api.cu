@@ -229,6 +229,48 @@ bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K, const void* a,
   return launched(e, "gemm launch");
 }
 
+bsmm_status bsmm_gemm_noalloc(int64_t B, int64_t M, int64_t N, int64_t K, const void* a, bsmm_dtype a_type,
+                              const void* b, bsmm_dtype b_type, const void* a_scales, int64_t K_a,
+                              const void* b_scales, int64_t K_b, bsmm_scale_type scale_type, void* y,
+                              bsmm_dtype y_type, bsmm_stream_t stream) {
+  if (B < 0 || M < 0 || N < 0 || K < 0) return fail(BSMM_ERR_INVALID_ARG, "negative size");
+  if (y_type != BSMM_F32 && y_type != BSMM_BF16) return fail(BSMM_ERR_INVALID_ARG, "y_type must be F32 or BF16");
+  if (!is_scale(scale_type)) return fail(BSMM_ERR_INVALID_ARG, "bad scale_type");
+  if (!is_code(a_type) || !is_code(b_type)) return fail(BSMM_ERR_INVALID_ARG, "bad operand type");
+  if (K_a <= 0 || K_b <= 0 || K % K_a || K % K_b)
+    return fail(BSMM_ERR_SHAPE, "K must be a multiple of K_a and of K_b");
+  if (B == 0 || M == 0 || N == 0) {
+    set_error("");
+    return BSMM_OK;
+  }
+  if (K == 0) return fail(BSMM_ERR_UNSUPPORTED, "K == 0");
+  const int64_t bs_a = K / K_a, bs_b = K / K_b;
+  const bool mx = (a_type == BSMM_E4M3 || a_type == BSMM_E5M2) && (b_type == BSMM_E4M3 || b_type == BSMM_E5M2) &&
+                  scale_type == BSMM_SCALE_UE8M0 && bs_a == 32 && bs_b == 32;
+  const bool nv = a_type == BSMM_E2M1 && b_type == BSMM_E2M1 && scale_type == BSMM_SCALE_UE4M3 && bs_a == 16 &&
+                  bs_b == 16;
+  if (!mx && !nv)
+    return fail(BSMM_ERR_UNSUPPORTED,
+                "supported: E4M3/E5M2 with UE8M0 scales per 32, or E2M1 with UE4M3 scales per 16");
+  if (!a || !b || !a_scales || !b_scales || !y) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
+  if (K % 32) return fail(BSMM_ERR_SHAPE, "K must be a multiple of 32");
+  if (!aligned16(a) || !aligned16(b) || !aligned16(y)) return fail(BSMM_ERR_ALIGNMENT, "a, b, y must be 16-byte aligned");
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2 || B > 65535)
+    return fail(BSMM_ERR_SHAPE, "size beyond the supported range");
+  const size_t need = bsmm_gemm_workspace_size(B, M, N, K, a_type);
+  if (need > BSMM_NOALLOC_SCRATCH_BYTES)
+    return fail(BSMM_ERR_WORKSPACE, "this problem needs " + std::to_string(need) +
+                                        " bytes of scratch; the no-allocation entry point holds at most " +
+                                        std::to_string(BSMM_NOALLOC_SCRATCH_BYTES) +
+                                        " (use bsmm_gemm with a workspace)");
+  MxGemmRequest r{B, M, N, K, a, b, a_type, b_type, static_cast<const uint8_t*>(a_scales),
+                  static_cast<const uint8_t*>(b_scales), nv, y, y_type == BSMM_BF16, nullptr};
+  std::string why;
+  const cudaError_t e = launch_mx_gemm_noalloc(r, reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess && !why.empty()) return fail(BSMM_ERR_CUDA, why);
+  return launched(e, "gemm (no allocation) launch");
+}
+
 bsmm_status bsmm_gemm_grouped(int64_t M, int64_t N, int64_t K, const void* a, bsmm_dtype a_type, const void* b,
                               bsmm_dtype b_type, const float* a_scales, const float* b_scales, int group_n,
                               int group_k, float* y, bsmm_stream_t stream) {

@@ -617,6 +617,50 @@ cudaError_t launch_grouped_gemm(const GroupedGemmRequest& r, cudaStream_t s, std
   return launch_kernel<kF32Scale, BN, 4>(ta, tb, ty, p, ctx, s);
 }
 
+// ---------------------------------------------------------------------------
+// Scratch for callers that cannot allocate device memory
+// ---------------------------------------------------------------------------
+// bsmm_gemm_noalloc keeps the tensor-core scale-factor atoms here instead of
+// in a caller-provided workspace.  Every GPU that loads this library holds
+// the array until the process exits.  All calls share it: each call rewrites
+// every byte it reads (the relayout fills whole atoms), so nothing needs
+// clearing, but calls whose kernels overlap on the GPU race on it.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[BSMM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[64] = {};
+}  // namespace
+
+cudaError_t launch_mx_gemm_noalloc(const MxGemmRequest& r, cudaStream_t s, std::string* why) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) {
+    *why = "device ordinal beyond the library's table";
+    return cudaErrorInvalidDevice;
+  }
+  void* scratch = nullptr;
+  {
+    // Set-up once per device, with that device current: host code only has
+    // a stand-in for the array's name, so its device address is looked up.
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) {
+        *why = std::string("cudaGetSymbolAddress of the scratch array failed: ") + cudaGetErrorString(e);
+        return e;
+      }
+      g_scratch_addr[dev] = p;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  MxGemmRequest rr = r;
+  rr.workspace = scratch;
+  return launch_mx_gemm(rr, s, why);
+}
+
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t s) {
   const DeviceCtx* ctx = device_ctx();
   if (!ctx) return cudaErrorInitializationError;

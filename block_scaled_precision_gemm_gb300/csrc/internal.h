@@ -65,6 +65,8 @@ struct MxGemmRequest {
   void* workspace;
 };
 cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* why);
+// Same, with the scale-factor atoms in the library's static device array.
+cudaError_t launch_mx_gemm_noalloc(const MxGemmRequest& r, cudaStream_t s, std::string* why);
 
 struct GroupedGemmRequest {
   int64_t M, N, K;

@@ -7,10 +7,11 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
- *    never allocates, frees or keeps device memory of its own, apart from a
- *    4-byte device status word per loaded module.  Scratch memory a call needs
- *    is passed in as `workspace`; its size comes from the matching
- *    *_workspace_size() query (0 means no workspace is needed).
+ *    never allocates, frees or keeps device memory of its own, apart from
+ *    static device arrays in the loaded module: a 4-byte status word, and the
+ *    scratch of bsmm_gemm_noalloc.  Scratch memory a call needs is passed in
+ *    as `workspace`; its size comes from the matching *_workspace_size()
+ *    query (0 means no workspace is needed).
  *  - Every call is asynchronous with respect to the host: it validates its
  *    arguments, enqueues kernels on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream) and returns.  Results are ready when the stream
@@ -181,6 +182,39 @@ bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K,
                       const void* a_scales, int64_t K_a, const void* b_scales, int64_t K_b,
                       bsmm_scale_type scale_type, void* y, bsmm_dtype y_type,
                       void* workspace, size_t workspace_bytes, bsmm_stream_t stream);
+
+/* No counterpart on the pages: bsmm_gemm for callers that cannot allocate.
+ *
+ * Some callers cannot call cudaMalloc at all: a plugin running inside a host
+ * framework that owns every device allocation and exposes no allocator to
+ * it, or a service that forbids device allocations after start-up so that
+ * its memory footprint stays fixed.  They cannot provide bsmm_gemm's
+ * workspace, so this variant keeps that scratch (the scales rearranged into
+ * the tensor-core scale-factor layout) in a static device array inside the
+ * library instead: BSMM_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that
+ * loads the library until the process exits.
+ *
+ * Arguments, formats and results are those of bsmm_gemm, without workspace.
+ * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating
+ * library routine).  Its first call on a device looks up the array's device
+ * address once (cudaGetSymbolAddress, with that device current); make that
+ * first call before any stream capture.  Every call shares the one array and
+ * rewrites all of it that it reads, so consecutive calls on one stream are
+ * safe, but calls whose kernels overlap on the GPU (different streams, or
+ * different host threads) race on it and give undefined results.
+ *
+ * Errors: those of bsmm_gemm, and BSMM_ERR_WORKSPACE when the problem needs
+ * more than BSMM_NOALLOC_SCRATCH_BYTES of scratch, i.e. when
+ * bsmm_gemm_workspace_size(B, M, N, K, a_type) exceeds it (e.g. an MXFP8
+ * batch of 8 x 4096 x 4096 x 8192 needs 16 MiB, an NVFP4 16384^3 problem
+ * 32 MiB). */
+#define BSMM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+bsmm_status bsmm_gemm_noalloc(int64_t B, int64_t M, int64_t N, int64_t K,
+                              const void* a, bsmm_dtype a_type, const void* b, bsmm_dtype b_type,
+                              const void* a_scales, int64_t K_a, const void* b_scales, int64_t K_b,
+                              bsmm_scale_type scale_type, void* y, bsmm_dtype y_type,
+                              bsmm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* GEMM with 1 x group_k activation and group_n x group_k weight FP32 scales */
