@@ -32,6 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import workloads as W  # noqa: E402
@@ -142,67 +143,242 @@ class ClockSampler:
 # workloads on the GPU                                                        #
 # --------------------------------------------------------------------------- #
 
-class GroupedSweep:
-    """block_scaled_mm problems: raw float32 a [m,k], b [n,k] resident in HBM;
-    a step quantizes both and runs the FP32-scale GEMM for every problem."""
+def _ev():
+    return torch.cuda.Event(enable_timing=True)
+
+
+class Work:
+    """One configuration: buffers resident in HBM, a step that runs the whole
+    hot path on them, its FLOPs, and an end-to-end variant through pinned host
+    buffers.  ``step(events)`` appends (start, end, flops) around every launch
+    of the dominant call."""
+    peak_kind = "fp8"
+    dtype = "e4m3 (f32 accumulate)"
+
+    def _timed(self, events, flops, fn):
+        if events is None:
+            return fn()
+        e0, e1 = _ev(), _ev()
+        e0.record()
+        r = fn()
+        e1.record()
+        events.append((e0, e1, flops))
+        return r
+
+    def setup_host(self):
+        self.h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in self.inputs]
+        self.h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in self.outputs]
+        self.h2d = sum(t.numel() * t.element_size() for t in self.inputs)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.outputs)
+
+    def step_e2e(self):
+        for d, h in zip(self.inputs, self.h_in):
+            d.copy_(h, non_blocking=True)
+        self.step()
+        for d, h in zip(self.outputs, self.h_out):
+            h.copy_(d, non_blocking=True)
+
+
+class GroupedWork(Work):
+    """block_scaled_mm problems: raw float32 a [m,k], b [n,k] in HBM; a step
+    quantizes both (1x128, 128x128) and runs the FP32-scale GEMM."""
     dominant = "block-scaled FP32-scale GEMM (tc_gemm kF32Scale)"
 
     def __init__(self, workload: W.Workload, device):
         import block_scaled_precision_gemm_gb300 as bsmm
-        self.bsmm = bsmm
-        self.w = workload
-        self.dev = device
+        self.bsmm, self.w = bsmm, workload
         self.items = []
         for p in workload.problems:
             a_raw, b_raw = W.grouped_raw(p, workload.seed, device)
-            it = {
+            self.items.append({
                 "p": p, "a_raw": a_raw, "b_raw": b_raw,
                 "aq": torch.empty((p.m, p.k), dtype=torch.uint8, device=device),
                 "sa": torch.empty((p.m, p.k // p.group_k), dtype=torch.float32, device=device),
                 "bq": torch.empty((p.n, p.k), dtype=torch.uint8, device=device),
                 "sb": torch.empty((p.n // p.group_n, p.k // p.group_k), dtype=torch.float32, device=device),
-                "y": torch.empty((p.m, p.n), dtype=torch.float32, device=device),
-            }
-            self.items.append(it)
+                "y": torch.empty((p.m, p.n), dtype=torch.float32, device=device)})
         self.flops = sum(2.0 * it["p"].m * it["p"].n * it["p"].k for it in self.items)
         self.launches_per_step = 3 * len(self.items)
+        self.inputs = [t for it in self.items for t in (it["a_raw"], it["b_raw"])]
+        self.outputs = [it["y"] for it in self.items]
 
-    def step(self, gemm_events=None):
+    def step(self, events=None):
         b = self.bsmm
         for it in self.items:
             p = it["p"]
             b.quantize(it["a_raw"], (1, p.group_k), "e4m3", "f32", codes=it["aq"], scales=it["sa"])
             b.quantize(it["b_raw"], (p.group_n, p.group_k), "e4m3", "f32", codes=it["bq"], scales=it["sb"])
-            if gemm_events is not None:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-            b.gemm_grouped(it["aq"], it["bq"], it["sa"], it["sb"], p.group_n, p.group_k, y=it["y"])
-            if gemm_events is not None:
-                e1.record()
-                gemm_events.append((e0, e1, 2.0 * p.m * p.n * p.k))
+            self._timed(events, 2.0 * p.m * p.n * p.k, lambda: b.gemm_grouped(
+                it["aq"], it["bq"], it["sa"], it["sb"], p.group_n, p.group_k, y=it["y"]))
 
-    # ---- end to end through host buffers
     def setup_host(self):
+        # one pinned buffer per direction, sized for the largest problem, reused
+        # by every problem (the copies are the step's real traffic)
         max_in = max(it["a_raw"].numel() + it["b_raw"].numel() for it in self.items)
         max_out = max(it["y"].numel() for it in self.items)
-        self.h_in = torch.empty(max_in, dtype=torch.float32, pin_memory=True)
-        self.h_out = torch.empty(max_out, dtype=torch.float32, pin_memory=True)
-        # the host buffer holds real inputs (the largest problem's raw a and b)
+        self.hb_in = torch.empty(max_in, dtype=torch.float32, pin_memory=True)
+        self.hb_out = torch.empty(max_out, dtype=torch.float32, pin_memory=True)
         big = max(self.items, key=lambda it: it["a_raw"].numel())
         na = big["a_raw"].numel()
-        self.h_in[:na].copy_(big["a_raw"].view(-1))
-        self.h_in[na:na + big["b_raw"].numel()].copy_(big["b_raw"].view(-1))
+        self.hb_in[:na].copy_(big["a_raw"].view(-1))
+        self.hb_in[na:na + big["b_raw"].numel()].copy_(big["b_raw"].view(-1))
         self.h2d = sum(4 * (it["a_raw"].numel() + it["b_raw"].numel()) for it in self.items)
         self.d2h = sum(4 * it["y"].numel() for it in self.items)
 
     def step_e2e(self):
         for it in self.items:
             na, nb = it["a_raw"].numel(), it["b_raw"].numel()
-            it["a_raw"].view(-1).copy_(self.h_in[:na], non_blocking=True)
-            it["b_raw"].view(-1).copy_(self.h_in[na:na + nb], non_blocking=True)
+            it["a_raw"].view(-1).copy_(self.hb_in[:na], non_blocking=True)
+            it["b_raw"].view(-1).copy_(self.hb_in[na:na + nb], non_blocking=True)
         self.step()
         for it in self.items:
-            self.h_out[:it["y"].numel()].copy_(it["y"].view(-1), non_blocking=True)
+            self.hb_out[:it["y"].numel()].copy_(it["y"].view(-1), non_blocking=True)
+
+    def config(self):
+        return {"problems": [[p.m, p.n, p.k] for p in self.w.problems], "group_n": 128, "group_k": 128,
+                "step": "quantize a 1x128 + quantize b 128x128 + FP32-scale GEMM, every problem"}
+
+    def input_bytes(self):
+        return sum(it["a_raw"].numel() * 4 for it in self.items)
+
+
+class Int8Work(Work):
+    """TensorTonic INT8 per-channel matmul at B = D_in = D_out = 4096: a step
+    quantizes x per row and w per column and runs the exact int32 matmul."""
+    dominant = "INT8 per-channel call (quantizers + mma.sync s8 GEMM)"
+    peak_kind = "int8"
+    dtype = "int8 (int32 accumulate)"
+
+    def __init__(self, workload, device):
+        import block_scaled_precision_gemm_gb300 as bsmm
+        self.bsmm, self.w = bsmm, workload
+        self.p = p = workload.problems[0]
+        self.x, self.wt = W.int8_raw(p, workload.seed, device)
+        self.out = {"x_q": torch.empty((p.B, p.D_in), dtype=torch.int8, device=device),
+                    "x_scales": torch.empty(p.B, dtype=torch.float32, device=device),
+                    "w_q": torch.empty((p.D_in, p.D_out), dtype=torch.int8, device=device),
+                    "w_scales": torch.empty(p.D_out, dtype=torch.float32, device=device),
+                    "y": torch.empty((p.B, p.D_out), dtype=torch.float32, device=device)}
+        self.ws = torch.empty(bsmm.int8_channel_workspace_size(p.B, p.D_in, p.D_out), dtype=torch.uint8,
+                              device=device)
+        self.flops = 2.0 * p.B * p.D_in * p.D_out
+        self.launches_per_step = 5
+        self.inputs, self.outputs = [self.x, self.wt], [self.out["y"]]
+
+    def step(self, events=None):
+        self._timed(events, self.flops, lambda: self.bsmm.int8_channel(self.x, self.wt, out=self.out,
+                                                                      workspace=self.ws))
+
+    def config(self):
+        p = self.p
+        return {"B": p.B, "D_in": p.D_in, "D_out": p.D_out, "zero_frac": p.zero_frac,
+                "step": "x per-row + w per-column INT8 quantize, int32 matmul, y = a*sx*sw"}
+
+    def input_bytes(self):
+        return 4 * (self.x.numel() + self.wt.numel())
+
+
+class MxWork(Work):
+    """jax.nn.scaled_matmul with the Blackwell formats: MXFP8 B=8,
+    M=N=4096, K=8192 or NVFP4 B=1, M=N=K=16384.  Codes and scales are
+    resident; a step is the library call (scale relayout + GEMM)."""
+
+    def __init__(self, workload, device):
+        import block_scaled_precision_gemm_gb300 as bsmm
+        self.bsmm, self.w = bsmm, workload
+        self.p = p = workload.problems[0]
+        raw = W.batched_raw(p, workload.seed, device)
+        if p.fmt == "mxfp8":
+            # encoding the seeded draws is input preparation (torch's float8 cast)
+            self.a = raw[0].to(torch.float8_e4m3fn).view(torch.uint8)
+            self.b = raw[1].to(torch.float8_e4m3fn).view(torch.uint8)
+            self.sa = (raw[2] + 127).to(torch.uint8)
+            self.sb = (raw[3] + 127).to(torch.uint8)
+            self.types = ("e4m3", "e4m3", "ue8m0")
+            self.dominant = "MXFP8 block-scaled GEMM call (sf_relayout + tc_gemm kMXF8)"
+        else:
+            self.a, self.b = raw[0], raw[1]
+            self.sa = raw[2].to(torch.float8_e4m3fn).view(torch.uint8)
+            self.sb = raw[3].to(torch.float8_e4m3fn).view(torch.uint8)
+            self.types = ("e2m1", "e2m1", "ue4m3")
+            self.peak_kind = "fp4"
+            self.dtype = "e2m1 (f32 accumulate)"
+            self.dominant = "NVFP4 block-scaled GEMM call (sf_relayout + tc_gemm kNVF4)"
+        del raw
+        self.y = torch.empty((p.B, p.M, p.N), dtype=torch.float32, device=device)
+        self.ws = torch.empty(bsmm.gemm_workspace_size(p.B, p.M, p.N, p.K, self.types[0]), dtype=torch.uint8,
+                              device=device)
+        self.flops = 2.0 * p.B * p.M * p.N * p.K
+        self.launches_per_step = 3
+        self.inputs, self.outputs = [self.a, self.b, self.sa, self.sb], [self.y]
+
+    def step(self, events=None):
+        t = self.types
+        self._timed(events, self.flops, lambda: self.bsmm.gemm(self.a, self.b, self.sa, self.sb, t[0], t[1], t[2],
+                                                               y=self.y, workspace=self.ws, K=self.p.K))
+
+    def config(self):
+        p = self.p
+        return {"B": p.B, "M": p.M, "N": p.N, "K": p.K, "format": p.fmt,
+                "step": "scale relayout + block-scaled GEMM, FP32 output"}
+
+    def input_bytes(self):
+        return sum(t.numel() for t in self.inputs)
+
+
+class BackwardWork(Work):
+    """NKI MXFP8 linear backward, M=16384, N=K=8192: a step quantizes dY (along
+    N and along M), W (along N) and X (along M) to E5M2 and runs dX = dY.W and
+    dW = dY^T.X with bf16 outputs."""
+    dominant = "MXFP8 backward call (4 quantizers + 2 x (sf_relayout + tc_gemm kMXF8))"
+    dtype = "e5m2 (f32 accumulate, bf16 out)"
+
+    def __init__(self, workload, device):
+        import block_scaled_precision_gemm_gb300 as bsmm
+        self.bsmm, self.w = bsmm, workload
+        self.p = p = workload.problems[0]
+        self.dY, self.W, self.X = W.backward_raw(p, workload.seed, device)
+        self.dX = torch.empty((p.M, p.K), dtype=torch.bfloat16, device=device)
+        self.dW = torch.empty((p.N, p.K), dtype=torch.bfloat16, device=device)
+        self.ws = torch.empty(bsmm.linear_backward_workspace_size(p.M, p.N, p.K), dtype=torch.uint8,
+                              device=device)
+        self.flops = 2 * 2.0 * p.M * p.N * p.K
+        self.launches_per_step = 8
+        self.inputs, self.outputs = [self.dY, self.W, self.X], [self.dX, self.dW]
+
+    def step(self, events=None):
+        self._timed(events, self.flops, lambda: self.bsmm.linear_backward(
+            self.dY, self.W, self.X, self.p.fp8, dX=self.dX, dW=self.dW, workspace=self.ws))
+
+    def config(self):
+        p = self.p
+        return {"M": p.M, "N": p.N, "K": p.K, "fp8": p.fp8,
+                "step": "4 MXFP8 quantizers + dX = dY.W and dW = dY^T.X, bf16 outputs"}
+
+    def input_bytes(self):
+        return sum(t.numel() * 2 for t in self.inputs)
+
+
+def make_work(workload: W.Workload, device) -> Work:
+    p = workload.problems[0]
+    if isinstance(p, W.Grouped):
+        return GroupedWork(workload, device)
+    if isinstance(p, W.Int8Channel):
+        return Int8Work(workload, device)
+    if isinstance(p, W.Batched):
+        return MxWork(workload, device)
+    return BackwardWork(workload, device)
+
+
+def peak_tflops(peaks, kind):
+    """Dense peak for the path's own dtype: measured bf16 (sustained) times the
+    nominal ratio (FP8 2x, FP4 4x).  INT8 has no measured or usable nominal
+    figure on this part; the bf16 rate is reported as its reference."""
+    base = peaks["bf16_tflops_sustained"]
+    return {"fp8": 2.0 * base, "fp4": 4.0 * base, "int8": base}[kind], {
+        "fp8": "2 x bf16_tflops_sustained (FP8/BF16 nominal ratio 2)",
+        "fp4": "4 x bf16_tflops_sustained (FP4/BF16 nominal ratio 4)",
+        "int8": "bf16_tflops_sustained (no INT8 tcgen05 kind on sm_103a; legacy mma.sync path)"}[kind]
 
 
 def run_gpu(args):
@@ -214,7 +390,7 @@ def run_gpu(args):
     bsmm.lib()
 
     workload = selected_workload(args)
-    wl = GroupedSweep(workload, device)
+    wl = make_work(workload, device)
     torch.cuda.synchronize()
 
     for i in range(args.warmup):
@@ -228,14 +404,14 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError(f"device status {st} (site {site}) after warm-up")
 
-    gemm_events = []
+    events = []
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
-        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_start, e_end = _ev(), _ev()
         e_start.record()
         for _ in range(args.steps):
-            wl.step(gemm_events)
+            wl.step(events)
         e_end.record()
         torch.cuda.synchronize()
         barrier(world)
@@ -243,8 +419,8 @@ def run_gpu(args):
     st, site = bsmm.check_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} (site {site}) in the timed region")
-    gemm_ms = sum(a.elapsed_time(b) for a, b, _ in gemm_events)
-    gemm_flops = sum(f for _, _, f in gemm_events)
+    dom_ms = sum(a.elapsed_time(b) for a, b, _ in events)
+    dom_flops = sum(f for _, _, f in events)
 
     t_max_ms = max_over_ranks(elapsed_ms, world, device)
     total_flops = sum_over_ranks(wl.flops * args.steps, world, device)
@@ -259,7 +435,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         barrier(world)
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b = _ev(), _ev()
         a.record()
         for _ in range(e2e_steps):
             wl.step_e2e()
@@ -271,39 +447,35 @@ def run_gpu(args):
                "d2h_bytes_per_step": wl.d2h, "steps": e2e_steps}
 
     peaks, peak_src = load_peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
-    achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    peak, peak_how = peak_tflops(peaks, wl.peak_kind)
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     roofline = {"kernel": wl.dominant, "bound": "tensor", "achieved": round(achieved, 2),
-                "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
-                "traffic": TRAFFIC_PER_LAUNCH.get(args.workload),
-                "peak_source": f"{peak_src}: 2 x bf16_tflops_sustained (FP8/BF16 nominal ratio 2)",
-                "gemm_share_of_step": round(gemm_ms / elapsed_ms, 4)}
+                "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": TRAFFIC_PER_LAUNCH.get(workload.name),
+                "peak_source": f"{peak_src}: {peak_how}",
+                "share_of_step": round(dom_ms / elapsed_ms, 4)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(workload, min_seconds=args.cpu_seconds)
 
     if rank == 0:
-        clocks = clk.summary()
+        cfg = describe(workload)
+        cfg["l2"] = "inputs larger than L2 (%.2f GB resident inputs per step)" % (wl.input_bytes() / 1e9)
+        cfg["parallelism"] = f"replicas x{world}"
         line = {
             "metric": "block-scaled GEMM TFLOPS (2MNK/t) and % of GB300 dense FP8/FP4 tensor peak",
             "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t_max_ms / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (f32 accumulate)",
-            "data": "synthetic (seeded randn, the atrex-bench input recipe)",
-            "config": {"workload": workload.name,
-                       "problems": [[p.m, p.n, p.k] for p in workload.problems],
-                       "group_n": 128, "group_k": 128,
-                       "step": "quantize a 1x128 + quantize b 128x128 + FP32-scale GEMM, every problem",
-                       "l2": "inputs larger than L2 (raw float32 activations %.1f GB per step)" % (
-                           sum(it["a_raw"].numel() * 4 for it in wl.items) / 1e9),
-                       "parallelism": f"replicas x{world}"},
-            "pct_of_fp8_peak": round(100 * value / fp8_peak, 2),
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded draws with the pages' shapes and distributions)",
+            "config": cfg,
+            "pct_of_peak": round(100 * value / peak, 2),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": wl.launches_per_step * args.steps,
-            "clocks": clocks,
+            "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -319,25 +491,93 @@ TRAFFIC_PER_LAUNCH = {}
 # CPU oracle: baseline leg and the reference arm                              #
 # --------------------------------------------------------------------------- #
 
-def oracle_sample_step(workload: W.Workload, rows: int):
-    """One bounded sample of the workload on the CPU oracle: for every
-    problem, the first ``rows`` activation rows against the first weight
-    group (128 output columns): quantize a and b, then the grouped matmul.
-    Returns the sample's FLOPs."""
+def describe(workload: W.Workload) -> dict:
+    """The configuration keys of a workload (no device needed)."""
+    p = workload.problems[0]
+    cfg = {"workload": workload.name}
+    if isinstance(p, W.Grouped):
+        cfg.update({"problems": [[q.m, q.n, q.k] for q in workload.problems], "group_n": p.group_n,
+                    "group_k": p.group_k,
+                    "step": "quantize a 1x128 + quantize b 128x128 + FP32-scale GEMM, every problem"})
+    elif isinstance(p, W.Int8Channel):
+        cfg.update({"B": p.B, "D_in": p.D_in, "D_out": p.D_out, "zero_frac": p.zero_frac,
+                    "step": "x per-row + w per-column INT8 quantize, int32 matmul, y = a*sx*sw"})
+    elif isinstance(p, W.Batched):
+        cfg.update({"B": p.B, "M": p.M, "N": p.N, "K": p.K, "format": p.fmt,
+                    "step": "scale relayout + block-scaled GEMM, FP32 output"})
+    else:
+        cfg.update({"M": p.M, "N": p.N, "K": p.K, "fp8": p.fp8,
+                    "step": "4 MXFP8 quantizers + dX = dY.W and dW = dY^T.X, bf16 outputs"})
+    return cfg
+
+
+def oracle_sample(workload: W.Workload, rows: int):
+    """A bounded sample of the workload for the CPU oracle.  Returns
+    ``(flops, run, text)``: ``run()`` executes every step of the hot path on
+    the sample (inputs are drawn beforehand, outside the timing)."""
     from oracle import formats as F
     from oracle import gemm as G
     from oracle import quantize as Q
-    flops = 0.0
-    for p in workload.problems:
-        r = min(rows, p.m)
-        g = torch.Generator().manual_seed(p.m)
-        a = torch.randn(r, p.k, generator=g).numpy()
-        b = torch.randn(p.group_n, p.k, generator=g).numpy()
-        ca, sa = Q.quantize(a, (1, p.group_k), "e4m3", "f32")
-        cb, sb = Q.quantize(b, (p.group_n, p.group_k), "e4m3", "f32")
-        G.grouped_matmul(F.decode(ca, "e4m3"), F.decode(cb, "e4m3"), sa, sb, p.group_n, p.group_k)
-        flops += 2.0 * r * p.group_n * p.k
-    return flops
+    p = workload.problems[0]
+    g = torch.Generator().manual_seed(workload.seed)
+    if isinstance(p, W.Grouped):
+        data = []
+        for q in workload.problems:
+            r = min(rows, q.m)
+            data.append((q, torch.randn(r, q.k, generator=g).numpy(), torch.randn(q.group_n, q.k, generator=g).numpy()))
+
+        def run():
+            for q, a, b in data:
+                ca, sa = Q.quantize(a, (1, q.group_k), "e4m3", "f32")
+                cb, sb = Q.quantize(b, (q.group_n, q.group_k), "e4m3", "f32")
+                G.grouped_matmul(F.decode(ca, "e4m3"), F.decode(cb, "e4m3"), sa, sb, q.group_n, q.group_k)
+        flops = sum(2.0 * a.shape[0] * q.group_n * q.k for q, a, _ in data)
+        text = (f"first {rows} activation rows x first 128 output columns of each of the "
+                f"{len(workload.problems)} problems (quantize a, quantize b, grouped matmul)")
+        return flops, run, text
+    if isinstance(p, W.Int8Channel):
+        r = min(rows, p.B)
+        x = torch.randn(r, p.D_in, generator=g).numpy()
+        w = torch.randn(p.D_in, 128, generator=g).numpy()
+        return (2.0 * r * p.D_in * 128, lambda: G.int8_channel(x, w),
+                f"first {r} rows of x x first 128 columns of w (both quantizers, int64 matmul, y)")
+    if isinstance(p, W.Batched):
+        r = min(rows, p.M)
+        if p.fmt == "mxfp8":
+            a = torch.randint(0, 256, (1, r, p.K), generator=g).numpy().astype(np.uint8) & 0x77
+            b = torch.randint(0, 256, (1, 128, p.K), generator=g).numpy().astype(np.uint8) & 0x77
+            sa = torch.randint(121, 134, (1, r, p.K // 32), generator=g).numpy().astype(np.uint8)
+            sb = torch.randint(121, 134, (1, 128, p.K // 32), generator=g).numpy().astype(np.uint8)
+            run = lambda: G.scaled_matmul(F.decode(a, "e4m3"), F.decode(b, "e4m3"), F.decode(sa, "ue8m0"),  # noqa
+                                          F.decode(sb, "ue8m0"))
+        else:
+            a = torch.randint(0, 256, (1, r, p.K // 2), generator=g).numpy().astype(np.uint8)
+            b = torch.randint(0, 256, (1, 128, p.K // 2), generator=g).numpy().astype(np.uint8)
+            sa = torch.randint(0x18, 0x58, (1, r, p.K // 16), generator=g).numpy().astype(np.uint8)
+            sb = torch.randint(0x18, 0x58, (1, 128, p.K // 16), generator=g).numpy().astype(np.uint8)
+            run = lambda: G.scaled_matmul(F.decode(F.unpack_e2m1(a), "e2m1"), F.decode(F.unpack_e2m1(b), "e2m1"),  # noqa
+                                          F.decode(sa, "ue4m3"), F.decode(sb, "ue4m3"))
+        return (2.0 * r * 128 * p.K, run,
+                f"first {r} rows x first 128 columns of batch 0 (decode, scale, float64 matmul)")
+    r = min(rows, p.M)
+    dY_rows = torch.randn(r, p.N, generator=g).numpy()
+    w_cols = (torch.randn(p.N, 128, generator=g) * 0.02).numpy()
+    dY_cols = torch.randn(p.M, 128, generator=g).numpy()
+    x_cols = (torch.randn(p.M, 128, generator=g) * 0.02).numpy()
+
+    def run():
+        # dX[:r, :128]: dY rows along N, W columns along N
+        cq, cs = G.mx_quantize(dY_rows, "cols", p.fp8)
+        wq, ws = G.mx_quantize(w_cols, "rows", p.fp8)
+        G.scaled_matmul(F.decode(cq, p.fp8)[None], F.decode(wq, p.fp8)[None], F.decode(cs, "ue8m0")[None],
+                        F.decode(ws, "ue8m0")[None])
+        # dW[:128, :128]: dY columns along M, X columns along M
+        dq, ds = G.mx_quantize(dY_cols, "rows", p.fp8)
+        xq, xs = G.mx_quantize(x_cols, "rows", p.fp8)
+        G.scaled_matmul(F.decode(dq, p.fp8)[None], F.decode(xq, p.fp8)[None], F.decode(ds, "ue8m0")[None],
+                        F.decode(xs, "ue8m0")[None])
+    return (2.0 * r * p.N * 128 + 2.0 * 128 * p.M * 128, run,
+            f"dX[:{r}, :128] and dW[:128, :128] (all four MXFP8 quantizers on the needed lines, both matmuls)")
 
 
 def cpu_cores():
@@ -348,18 +588,47 @@ def cpu_cores():
 
 
 def cpu_baseline(workload: W.Workload, min_seconds: float = 10.0, rows: int = 256):
-    flops, t0 = 0.0, time.perf_counter()
-    n = 0
+    flops_one, run, text = oracle_sample(workload, rows)
+    flops, n, t0 = 0.0, 0, time.perf_counter()
     while True:
-        flops += oracle_sample_step(workload, rows)
+        run()
+        flops += flops_one
         n += 1
         el = time.perf_counter() - t0
         if el >= min_seconds:
             break
     return {"value": round(flops / el / 1e12, 6), "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{n} passes of: first {rows} activation rows x first 128 output columns of each of the "
-                      f"{len(workload.problems)} problems (quantize a, quantize b, grouped matmul; NumPy float64)",
-            "seconds": round(el, 2)}
+            "sample": f"{n} passes of: {text}; NumPy float64 oracle", "seconds": round(el, 2)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    workload = selected_workload(args)
+    flops_one, run, text = oracle_sample(workload, args.reference_rows)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    el = time.perf_counter() - t0
+    value = flops_one * args.steps / el / 1e12
+    cfg = describe(workload)
+    cfg["sample"] = text
+    line = {
+        "impl": "reference",
+        "metric": "block-scaled GEMM TFLOPS (2MNK/t) and % of GB300 dense FP8/FP4 tensor peak",
+        "value": round(value, 6), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded draws with the pages' shapes and distributions)",
+        "config": cfg,
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": text + " per step"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
 
 
 def selected_workload(args) -> W.Workload:
@@ -369,38 +638,8 @@ def selected_workload(args) -> W.Workload:
     return WORKLOADS_BY_KEY[args.workload]
 
 
-def run_reference(args):
-    rank, world, _ = dist_env()
-    if rank != 0:
-        return
-    workload = selected_workload(args)
-    rows = args.reference_rows
-    for _ in range(args.warmup):
-        oracle_sample_step(workload, rows)
-    t0 = time.perf_counter()
-    flops = 0.0
-    for _ in range(args.steps):
-        flops += oracle_sample_step(workload, rows)
-    el = time.perf_counter() - t0
-    value = flops / el / 1e12
-    sample = (f"first {rows} activation rows x first 128 output columns of each of the "
-              f"{len(workload.problems)} problems per step")
-    line = {
-        "impl": "reference",
-        "metric": "block-scaled GEMM TFLOPS (2MNK/t) and % of GB300 dense FP8/FP4 tensor peak",
-        "value": round(value, 6), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn, the atrex-bench input recipe)",
-        "config": {"workload": workload.name, "problems": [[p.m, p.n, p.k] for p in workload.problems],
-                   "group_n": 128, "group_k": 128, "sample": sample},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": sample},
-        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
-
-
-WORKLOADS_BY_KEY = {"sweep": W.GROUPED_SWEEP, "small": W.GROUPED_SMALL}
+WORKLOADS_BY_KEY = {"sweep": W.GROUPED_SWEEP, "small": W.GROUPED_SMALL, "int8": W.INT8_4096,
+                    "mxfp8": W.MXFP8_BATCHED, "nvfp4": W.NVFP4_SQUARE, "backward": W.BACKWARD}
 
 
 def main(argv=None):

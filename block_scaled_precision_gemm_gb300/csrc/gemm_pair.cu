@@ -1,0 +1,381 @@
+// FP32-scale block GEMM on a CTA pair (tcgen05 .cta_group::2), 256 x 256 tiles.
+//
+// Computes y[m,n] = sum_kb sa[m,kb] * sb[n/128,kb] * (a . b over K block kb)
+// (atrex-bench #002 block_scaled_mm, Reference Implementation) like the
+// single-CTA kernel, but two CTAs of a cluster share one 256 x 256 output
+// tile: CTA r loads rows 128r..128r+127 of the A tile and of the B tile, and
+// the leader (rank 0) issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
+// K = 32), which reads both CTAs' shared memory and writes a 128 x 256 FP32
+// partial into each CTA's tensor memory.  N = 256 instructions keep the tensor
+// pipe busy (N = 128 ones run it at about half rate), and per SM the operands
+// are 32 KB per 128-K block for twice the FLOPs of a 128 x 128 tile.
+//
+// Synchronization across the pair:
+//   full[s]   in the leader, 2 arrivals (leader with expect_tx for both CTAs'
+//             bytes, peer remotely); both CTAs' TMA loads complete on it.
+//   empty[s]  in both CTAs; the leader's MMA commit multicasts to both.
+//   tfull[i]  in both CTAs; multicast commit after each K block's MMAs.
+//   tempty[i] in the leader, 32 arrivals (16 epilogue warps of each CTA).
+// Every wait is bounded; on expiry a CTA records the site and winds down.
+//
+// Epilogue: 16 warps per CTA (four per TMEM lane quarter).  Warp w reads
+// lanes 32*(w%4).. (its 32 rows) and one 64-column quarter of the tile; the
+// running FP32 sum of its 64 columns lives in registers.  Reading every K
+// block's partial out of tensor memory is the other bound of this kernel: one
+// warp moves ~28 B/clk from TMEM, and the promotion needs 128 x 256 x 4 bytes
+// per 128-K block, hence sixteen reading warps.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsmm {
+namespace {
+
+constexpr int PM = 256, PN = 256;          // pair tile
+constexpr int HALF = 128;                  // A rows per CTA
+constexpr int BHALF = PN / 2;              // B rows per CTA
+constexpr int KB = 128;                    // K bytes per stage (128 FP8 elements)
+constexpr int STAGES = 5;
+constexpr int THREADS = 640;               // 4 control warps + 16 epilogue warps
+constexpr int EPI_WARPS = 16;
+constexpr int EPI_COLS = 64;               // columns per epilogue thread
+constexpr int TMEM_COLS = 512;             // two 256-column partial buffers
+constexpr int NACC = 2;
+constexpr int GROUP_M = 16;
+constexpr int A_BYTES = HALF * KB, B_BYTES = BHALF * KB;
+constexpr int STAGE_TX = A_BYTES + B_BYTES;  // per CTA
+constexpr int STG_PER_WARP = 4096;        // one 32-row x 128-byte staging buffer
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr int OFF_STG = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_PER_WARP;
+constexpr int N_BARS = 2 * STAGES + 2 * NACC + 1;
+constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;
+static_assert(SMEM <= 232448, "shared memory budget");
+
+enum Site { kSiteProducer = 11, kSiteMmaTmem = 12, kSiteMmaFull = 13, kSiteEpilogue = 14, kSiteDrain = 15,
+            kSiteDone = 16 };
+
+struct PairParams {
+  int M, N, K;
+  int m_tiles, n_tiles, k_tiles;  // tiles of 256 x 256
+  int num_tiles;
+  const float* a_scales;
+  const float* b_scales;
+  int kb;  // K / 128
+  uint32_t idesc;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void decode_pair_tile(const PairParams& p, int t, int& mb, int& nb) {
+  const int span = GROUP_M * p.n_tiles;
+  const int g = t / span;
+  const int within = t - g * span;
+  const int rows = min(GROUP_M, p.m_tiles - g * GROUP_M);
+  mb = g * GROUP_M + within % rows;
+  nb = within / rows;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_pair_f32scale(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmY, const PairParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + OFF_A;
+  uint8_t* sB = smem + OFF_B;
+  uint8_t* stg = smem + OFF_STG;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + NACC;
+  uint64_t* done = tempty + NACC;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int never_abort_storage = 0;
+  volatile int* never_abort = &never_abort_storage;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 2);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < NACC; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 2 * EPI_WARPS);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialized before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  // 640 threads launch with 96 registers each (61440); the control warpgroup
+  // gives up 40 of its 96, the four epilogue warpgroups take 104 each:
+  // 128 x 56 + 512 x 104 = 60416 <= 61440.
+  if (warp < 4) {
+    setmaxnreg_dec<56>();
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------- producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int t = cid; ok && t < p.num_tiles; t += ncl) {
+        int mb, nb;
+        decode_pair_tile(p, t, mb, nb);
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_TX);
+          tma_load_3d_pair(sA + stage * A_BYTES, &tmA, full_leader, kt * KB, mb * PM + rank * HALF, 0);
+          tma_load_3d_pair(sB + stage * B_BYTES, &tmB, full_leader, kt * KB, nb * PN + rank * BHALF, 0);
+          if (!leader) mbar_arrive_cluster(full_leader);
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every stage this CTA filled must have been released by the leader's
+      // MMA (its multicast arrivals on our empty[] have landed) before any
+      // CTA of the pair winds down.
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          mbar_wait(&empty[s], (last_par >> s) & 1u, p.timeout_ns, ok ? never_abort : abort_flag, p.status,
+                    kSiteDrain);
+      if (leader) {
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1u)
+            mbar_wait(&full[s], (last_par >> s) & 1u, p.timeout_ns, never_abort, p.status, kSiteDrain);
+      } else if (!ok) {
+        // The peer cannot observe the leader's barrier; after giving up, give
+        // its own copies in flight time to land before the CTA winds down.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
+        }
+      }
+    } else if (warp == 1 && lane == 0 && leader) {
+      // ------------------------------------------------------- MMA issuer (leader)
+      int stage = 0, tb = 0;
+      uint32_t phase = 0, tph = 0;
+      bool ok = true;
+      for (int t = cid; ok && t < p.num_tiles; t += ncl) {
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
+          const uint32_t d = tmem + static_cast<uint32_t>(tb * PN);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8f6f4_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
+                            p.idesc, k > 0 ? 1u : 0u);
+          tc_commit_pair_mc(&empty[stage], 0x3);
+          tc_commit_pair_mc(&tfull[tb], 0x3);
+          if (++tb == NACC) {
+            tb = 0;
+            tph ^= 1u;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      tc_commit_pair_mc(done, 0x1);
+      mbar_wait(done, 0, p.timeout_ns, never_abort, p.status, kSiteDone);
+    }
+  } else {
+    setmaxnreg_inc<104>();
+    // --------------------------------------------------------- epilogue (both CTAs)
+    constexpr int COLS = EPI_COLS;
+    const int ew = warp - 4;
+    const int q = warp & 3;   // TMEM lane quarter = the warp's 32 rows
+    const int g = ew >> 2;    // 64-column quarter of the tile
+    uint8_t* my_stg = stg + ew * STG_PER_WARP;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int tb = 0;
+    uint32_t tph = 0;
+    for (int t = cid; t < p.num_tiles; t += ncl) {
+      int mb, nb;
+      decode_pair_tile(p, t, mb, nb);
+      const int row0 = mb * PM + static_cast<int>(rank) * HALF + q * 32;
+      const int row = row0 + lane;
+      const int col0 = nb * PN + g * COLS;
+      const bool row_ok = row < p.M, col_ok = col0 < p.N;  // N % 128 == 0: a quarter is all in or all out
+      const float* sa_row = p.a_scales + static_cast<size_t>(row_ok ? row : 0) * p.kb;
+      const float* sb_row = p.b_scales + static_cast<size_t>(col_ok ? col0 / 128 : 0) * p.kb;
+      float acc[COLS];
+#pragma unroll
+      for (int i = 0; i < COLS; ++i) acc[i] = 0.f;
+      float sa_next = row_ok ? __ldg(sa_row) : 0.f;
+      float sb_next = col_ok ? __ldg(sb_row) : 0.f;
+      bool ok = true;
+      for (int kt = 0; kt < p.k_tiles; ++kt) {
+        const float s = sa_next * sb_next;
+        if (kt + 1 < p.k_tiles) {
+          sa_next = row_ok ? __ldg(sa_row + kt + 1) : 0.f;
+          sb_next = col_ok ? __ldg(sb_row + kt + 1) : 0.f;
+        }
+        if (!mbar_wait(&tfull[tb], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(tb * PN + g * COLS);
+#pragma unroll
+        for (int h = 0; h < COLS / 32; ++h) {  // two loads in flight per wait
+          uint32_t r0[16], r1[16];
+          tmem_ld16(taddr + 32 * h, r0);
+          tmem_ld16(taddr + 32 * h + 16, r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[32 * h + j] = fmaf(__uint_as_float(r0[j]), s, acc[32 * h + j]);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[32 * h + 16 + j] = fmaf(__uint_as_float(r1[j]), s, acc[32 * h + 16 + j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[tb]), 0));
+        if (++tb == NACC) {
+          tb = 0;
+          tph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (row0 >= p.M || !col_ok) continue;  // this warp's box lies outside y
+      // 64 columns of 32 rows leave as two 32 x 32 TMA stores
+#pragma unroll
+      for (int c = 0; c < COLS / 32; ++c) {
+        uint8_t* buf = my_stg;
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float* v = &acc[32 * c + 4 * j];
+          const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
+          *reinterpret_cast<uint4*>(buf + off) =
+              make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmY, buf, col0 + 32 * c, row0, 0);
+          bulk_commit();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no signal may target a CTA that has exited
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
+int g_pair_clusters[64] = {};
+
+}  // namespace
+
+bool grouped_pair_eligible(int64_t M, int64_t N, int64_t K, const DeviceCtx* ctx) {
+  // The pair kernel stores through TMA (N*4 % 16 == 0 holds: N % 128 == 0)
+  // and wants at least one 256 x 256 tile per cluster.
+  const int64_t tiles = ceil_div(M, PM) * ceil_div(N, PN);
+  return K % 128 == 0 && N % 128 == 0 && tiles >= ctx->num_sms / 2;
+}
+
+cudaError_t launch_grouped_gemm_pair(const GroupedGemmRequest& r, cudaStream_t s, std::string* why) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  CUtensorMap ta, tb, ty;
+  if (!make_tmap_3d(&ta, r.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, r.K, r.M, 1, KB, HALF, true) ||
+      !make_tmap_3d(&tb, r.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, r.K, r.N, 1, KB, BHALF, true) ||
+      !make_tmap_3d(&ty, r.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, r.N, r.M, 1, 32, 32, true)) {
+    *why = "cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  PairParams p{};
+  p.M = static_cast<int>(r.M);
+  p.N = static_cast<int>(r.N);
+  p.K = static_cast<int>(r.K);
+  p.m_tiles = static_cast<int>(ceil_div(r.M, PM));
+  p.n_tiles = static_cast<int>(ceil_div(r.N, PN));
+  p.k_tiles = static_cast<int>(r.K / 128);
+  p.num_tiles = p.m_tiles * p.n_tiles;
+  p.a_scales = r.a_scales;
+  p.b_scales = r.b_scales;
+  p.kb = static_cast<int>(r.K / 128);
+  p.status = ctx->status;
+  p.timeout_ns = wait_timeout_ns();
+  // kind::f8f6f4: D = F32, A/B E4M3 = 0 / E5M2 = 1, K-major, N = 256, M = 256 (pair).
+  p.idesc = (1u << 4) | ((r.a_fmt == BSMM_E5M2 ? 1u : 0u) << 7) | ((r.b_fmt == BSMM_E5M2 ? 1u : 0u) << 10) |
+            (static_cast<uint32_t>(PN >> 3) << 17) | (static_cast<uint32_t>(PM >> 4) << 24);
+
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_f32scale, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int& max_clusters = g_pair_clusters[ctx->device];
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * (ctx->num_sms / 2));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_f32scale, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) {
+      *why = "no cluster of two CTAs fits on this device";
+      return cudaErrorInvalidConfiguration;
+    }
+    max_clusters = n;
+  }
+  const int clusters = std::max(1, std::min(p.num_tiles, max_clusters));
+  cfg.gridDim = dim3(2 * clusters);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_f32scale, ta, tb, ty, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace bsmm

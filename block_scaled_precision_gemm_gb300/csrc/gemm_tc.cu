@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -587,6 +588,14 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
 cudaError_t launch_grouped_gemm(const GroupedGemmRequest& r, cudaStream_t s, std::string* why) {
   const DeviceCtx* ctx = device_ctx();
   if (!ctx) return cudaErrorInitializationError;
+  // Kernel choice: CTA-pair 256 x 256 tiles when there is a tile for every
+  // cluster, else one CTA per 128 x 128 tile.  BSMM_GROUPED_KERNEL=pair|single
+  // overrides the choice (pair still needs N % 128 == 0 and K % 128 == 0).
+  const char* force = std::getenv("BSMM_GROUPED_KERNEL");
+  const bool want_pair = force && std::strcmp(force, "pair") == 0;
+  const bool want_single = force && std::strcmp(force, "single") == 0;
+  if (!want_single && (want_pair ? (r.N % 128 == 0 && r.K % 128 == 0) : grouped_pair_eligible(r.M, r.N, r.K, ctx)))
+    return launch_grouped_gemm_pair(r, s, why);
   constexpr int BN = 128;
   CUtensorMap ta, tb, ty;
   if (!make_tmap_3d(&ta, r.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, r.K, r.M, 1, BK_BYTES, BM, true) ||

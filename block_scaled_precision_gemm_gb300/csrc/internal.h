@@ -78,6 +78,10 @@ struct GroupedGemmRequest {
   float* y;
 };
 cudaError_t launch_grouped_gemm(const GroupedGemmRequest& r, cudaStream_t s, std::string* why);
+// 256 x 256 tiles on CTA pairs (gemm_pair.cu); eligible when N and K are
+// multiples of 128 and there is at least one tile per cluster.
+bool grouped_pair_eligible(int64_t M, int64_t N, int64_t K, const DeviceCtx* ctx);
+cudaError_t launch_grouped_gemm_pair(const GroupedGemmRequest& r, cudaStream_t s, std::string* why);
 
 struct Int8Request {
   const float* x;

@@ -63,6 +63,18 @@ def test_grouped_parity(m, n, k):
     assert_within(y, y_ref, bound, f"grouped m={m} n={n} k={k}")
 
 
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+@pytest.mark.parametrize("m,n,k", [(256, 256, 128), (300, 384, 512), (1, 256, 256), (777, 1024, 1024),
+                                   (2000, 2048, 2048)])
+def test_grouped_parity_each_kernel(monkeypatch, kernel, m, n, k):
+    """Both GEMM kernels (CTA-pair 256x256 tiles and single-CTA 128x128
+    tiles) on ragged shapes: an M tail, N % 256 == 128 (a half-empty pair
+    tile), a single row, and several waves of tiles."""
+    monkeypatch.setenv("BSMM_GROUPED_KERNEL", kernel)
+    y, y_ref, bound = run_grouped(*grouped_inputs(m, n, k, seed=3 * m + n))
+    assert_within(y, y_ref, bound, f"grouped[{kernel}] m={m} n={n} k={k}")
+
+
 def test_grouped_e5m2_operands():
     ca, sa, _, _ = grouped_inputs(100, 256, 256, 5, "e5m2")
     _, _, cb, sb = grouped_inputs(100, 256, 256, 6, "e4m3")
