@@ -6,9 +6,9 @@
 // with saturation.  All arithmetic is binary32 with IEEE division.
 //
 // Kernels:
-//   quant_rows   1 x {16,32,64,128} blocks along the contiguous axis; each
-//                block is a group of 2..32 lanes holding 16-byte vectors,
-//                absmax by xor-shuffle; HBM-streaming, unrolled loads.
+//   quant_rows   1 x {16,32,64,128} blocks along the contiguous axis; a
+//                thread owns 16-element slices, 1..8 lanes per block, absmax
+//                by xor-shuffle; HBM-streaming.
 //   quant_cols   {16,32,64,128} x 1 blocks down the columns; a 128 x 64 tile
 //                staged in shared memory, codes written as is or transposed.
 //   quant_tile   128 x 128 blocks (one scale per tile).
@@ -48,6 +48,7 @@ __device__ __forceinline__ float ue4m3_value(uint32_t b) {
 
 struct Scale {
   float s;          // the divisor
+  float inv;        // 1/s when s is a power of two (exact), else 0
   uint32_t stored;  // what is written: binary32 bits or the scale byte
 };
 
@@ -59,6 +60,7 @@ __device__ __forceinline__ Scale make_scale(float absmax, int code, int scale) {
     // FP8/FP4 (atrex-bench): max(absmax/qmax, 1e-10).
     const float s = (code == BSMM_INT8) ? (absmax == 0.f ? 1.f : r) : fmaxf(r, 1e-10f);
     out.s = s;
+    out.inv = 0.f;
     out.stored = __float_as_uint(s);
   } else if (scale == BSMM_SCALE_UE8M0) {
     // Smallest power of two not below r: 2^ceil(log2 r), exponent in [-127,127].
@@ -79,6 +81,9 @@ __device__ __forceinline__ Scale make_scale(float absmax, int code, int scale) {
     }
     out.stored = static_cast<uint32_t>(e + 127);
     out.s = e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+    // 2^-e is exact for e in [-127, 127]; x * 2^-e rounds the same exact
+    // value that x / 2^e does, so multiplying is the IEEE quotient.
+    out.inv = -e >= -126 ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : __uint_as_float(0x00400000u);
   } else {
     // UE4M3: nearest E4M3 value of r; zero block -> 1.0; a scale that rounds
     // to zero -> the smallest subnormal.
@@ -91,6 +96,7 @@ __device__ __forceinline__ Scale make_scale(float absmax, int code, int scale) {
     }
     out.stored = b;
     out.s = ue4m3_value(b);
+    out.inv = 0.f;
   }
   return out;
 }
@@ -101,12 +107,19 @@ __device__ __forceinline__ uint32_t int8_code(float q) {
   return static_cast<uint32_t>(__float2int_rn(clampq(q, 127.f))) & 0xFFu;
 }
 
-// Codes of four consecutive elements: 4 bytes (E4M3/E5M2/INT8, element 0 in
-// the low byte) or 2 bytes (E2M1, element 0 in the low nibble).
-__device__ __forceinline__ uint32_t encode4(float x0, float x1, float x2, float x3, float s, int code) {
-  const float qm = qmax_of(code);
-  const float q0 = clampq(__fdiv_rn(x0, s), qm), q1 = clampq(__fdiv_rn(x1, s), qm);
-  const float q2 = clampq(__fdiv_rn(x2, s), qm), q3 = clampq(__fdiv_rn(x3, s), qm);
+// x / s, correctly rounded: a multiply by the exact reciprocal when s is a
+// power of two (POW2), IEEE division otherwise.
+template <bool POW2>
+__device__ __forceinline__ float quot(float x, const Scale& sc) {
+  if constexpr (POW2)
+    return x * sc.inv;
+  else
+    return __fdiv_rn(x, sc.s);
+}
+
+__device__ __forceinline__ uint32_t pack4(float q0, float q1, float q2, float q3, int code) {
+  // The float conversions saturate (satfinite): for finite quotients that is
+  // clamp(q, +-qmax) followed by nearest-even rounding.  INT8 clamps.
   switch (code) {
     case BSMM_E4M3: return cvt_e4m3x2(q0, q1) | (cvt_e4m3x2(q2, q3) << 16);
     case BSMM_E5M2: return cvt_e5m2x2(q0, q1) | (cvt_e5m2x2(q2, q3) << 16);
@@ -115,9 +128,17 @@ __device__ __forceinline__ uint32_t encode4(float x0, float x1, float x2, float 
   }
 }
 
+// Codes of four consecutive elements: 4 bytes (E4M3/E5M2/INT8, element 0 in
+// the low byte) or 2 bytes (E2M1, element 0 in the low nibble).
+template <bool POW2>
+__device__ __forceinline__ uint32_t encode4(float x0, float x1, float x2, float x3, const Scale& sc, int code) {
+  return pack4(quot<POW2>(x0, sc), quot<POW2>(x1, sc), quot<POW2>(x2, sc), quot<POW2>(x3, sc), code);
+}
+
 // One code (8-bit formats) or one nibble (E2M1).
-__device__ __forceinline__ uint32_t encode1(float x, float s, int code) {
-  const float q = clampq(__fdiv_rn(x, s), qmax_of(code));
+template <bool POW2>
+__device__ __forceinline__ uint32_t encode1(float x, const Scale& sc, int code) {
+  const float q = clampq(quot<POW2>(x, sc), qmax_of(code));
   switch (code) {
     case BSMM_E4M3: return cvt_e4m3x2(q, 0.f) & 0xFFu;
     case BSMM_E5M2: return cvt_e5m2x2(q, 0.f) & 0xFFu;
@@ -163,69 +184,78 @@ __device__ __forceinline__ void load_vec(const void* p, float (&v)[16 / sizeof(I
 // ---------------------------------------------------------------------------
 // 1 x bc blocks along rows
 // ---------------------------------------------------------------------------
-constexpr int kRowsUnroll = 4;
+// A thread owns a slice of 16 consecutive elements of one block; G = bc / 16
+// lanes (1..8) share a block and combine their maxima by xor-shuffle.  Each
+// thread handles two slices per trip (32 elements in flight).
+constexpr int kSlice = 16;
 
 template <typename In>
-__global__ void __launch_bounds__(256) quant_rows(QP p) {
+__device__ __forceinline__ void load_slice(const In* p, float (&v)[kSlice]) {
   constexpr int VEC = 16 / sizeof(In);
-  const int G = p.bc / VEC;  // lanes sharing one block: 2..32, a power of two
-  const int64_t vpr = p.cols / VEC;
-  const int64_t total = p.rows * vpr;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t chunk = nw * 32;
-  const bool fp4 = p.code == BSMM_E2M1;
-  // Dense arrays (pitches equal to the widths) need no row/column split.
-  const bool dense = p.ld_x == p.cols && p.ld_codes == p.cols && p.ld_scales * p.bc == p.cols;
-  const int bc_shift = __ffs(p.bc) - 1;  // bc is a power of two
-  for (int64_t base = warp * 32; base < total; base += chunk * kRowsUnroll) {
-    float v[kRowsUnroll][VEC];
 #pragma unroll
-    for (int u = 0; u < kRowsUnroll; ++u) {
-      const int64_t vi = base + u * chunk + lane;
-      if (vi < total) {
-        int64_t off = vi * VEC;
+  for (int i = 0; i < kSlice / VEC; ++i) {
+    float t[VEC];
+    load_vec<In>(p + i * VEC, t);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) v[i * VEC + k] = t[k];
+  }
+}
+
+template <typename In, bool POW2>
+__global__ void __launch_bounds__(256) quant_rows(QP p) {
+  const int G = p.bc / kSlice;                 // lanes per block: 1, 2, 4 or 8
+  const int64_t spr = p.cols / kSlice;         // slices per row
+  const int64_t total = p.rows * spr;
+  const int lane = threadIdx.x & 31;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const bool fp4 = p.code == BSMM_E2M1;
+  const bool dense = p.ld_x == p.cols && p.ld_codes == p.cols && p.ld_scales * p.bc == p.cols;
+  const int g_shift = __ffs(G) - 1;
+  const In* x = reinterpret_cast<const In*>(p.x);
+  uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
+  // b0 is warp-uniform, so every shuffle sees the whole warp
+  for (int64_t b0 = tid - lane; b0 < total; b0 += 2 * nth) {
+    float v[2][kSlice];
+    int64_t si[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      si[u] = b0 + u * nth + lane;
+      if (si[u] < total) {
+        int64_t off = si[u] * kSlice;
         if (!dense) {
-          const int64_t r = vi / vpr, c = vi - r * vpr;
-          off = r * p.ld_x + c * VEC;
+          const int64_t r = si[u] / spr;
+          off = r * p.ld_x + (si[u] - r * spr) * kSlice;
         }
-        load_vec<In>(reinterpret_cast<const In*>(p.x) + off, v[u]);
+        load_slice<In>(x + off, v[u]);
       } else {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) v[u][i] = 0.f;
+        for (int i = 0; i < kSlice; ++i) v[u][i] = 0.f;
       }
     }
 #pragma unroll
-    for (int u = 0; u < kRowsUnroll; ++u) {
-      const int64_t vi = base + u * chunk + lane;
+    for (int u = 0; u < 2; ++u) {
       float m = 0.f;
 #pragma unroll
-      for (int i = 0; i < VEC; ++i) m = fmaxf(m, fabsf(v[u][i]));
+      for (int i = 0; i < kSlice; ++i) m = fmaxf(m, fabsf(v[u][i]));
       for (int o = G >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (vi >= total) continue;
+      if (si[u] >= total) continue;
       const Scale sc = make_scale(m, p.code, p.scale);
-      int64_t e = vi * VEC, sidx = e >> bc_shift;  // element offset, scale index (dense)
+      int64_t e = si[u] * kSlice, sidx = si[u] >> g_shift;
       if (!dense) {
-        const int64_t r = vi / vpr, c = vi - r * vpr;
-        e = r * p.ld_codes + c * VEC;
-        sidx = r * p.ld_scales + (c * VEC) / p.bc;
+        const int64_t r = si[u] / spr, c = si[u] - r * spr;
+        e = r * p.ld_codes + c * kSlice;
+        sidx = r * p.ld_scales + ((c * kSlice) / p.bc);
       }
       if ((lane & (G - 1)) == 0) store_scale(p.scales, sidx, p.scale, sc.stored);
-      const uint32_t w0 = encode4(v[u][0], v[u][1], v[u][2], v[u][3], sc.s, p.code);
-      uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
-      if constexpr (VEC == 4) {
-        if (fp4)
-          *reinterpret_cast<uint16_t*>(out + e / 2) = static_cast<uint16_t>(w0);
-        else
-          *reinterpret_cast<uint32_t*>(out + e) = w0;
-      } else {
-        const uint32_t w1 = encode4(v[u][4], v[u][5], v[u][6], v[u][7], sc.s, p.code);
-        if (fp4)
-          *reinterpret_cast<uint32_t*>(out + e / 2) = w0 | (w1 << 16);
-        else
-          *reinterpret_cast<uint2*>(out + e) = make_uint2(w0, w1);
-      }
+      uint32_t w[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        w[g] = encode4<POW2>(v[u][4 * g], v[u][4 * g + 1], v[u][4 * g + 2], v[u][4 * g + 3], sc, p.code);
+      if (fp4)
+        *reinterpret_cast<uint2*>(out + e / 2) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+      else
+        *reinterpret_cast<uint4*>(out + e) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
@@ -235,7 +265,7 @@ __global__ void __launch_bounds__(256) quant_rows(QP p) {
 // ---------------------------------------------------------------------------
 constexpr int kColTileR = 128, kColTileC = 64;
 
-template <typename In>
+template <typename In, bool POW2>
 __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok) {
   __shared__ float tile[kColTileR][kColTileC + 1];
   __shared__ float pmax[4][kColTileC];
@@ -248,18 +278,32 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok) {
   // Stage the tile (coalesced along columns).
   if (vec_ok) {
     constexpr int VEC = 16 / sizeof(In);
-    constexpr int VPR = kColTileC / VEC;  // vectors per tile row
-    for (int i = t; i < kColTileR * VPR; i += 256) {
+    constexpr int VPR = kColTileC / VEC;        // vectors per tile row
+    constexpr int NV = kColTileR * VPR / 256;   // vectors per thread
+    uint4 raw[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {  // all loads in flight before any use
+      const int i = t + 256 * j;
       const int rr = i / VPR, cv = i % VPR;
-      float v[VEC];
-      if (rr < nr && cv * VEC < nc) {
-        load_vec<In>(x + (r0 + rr) * p.ld_x + c0 + cv * VEC, v);
+      raw[j] = (rr < nr && cv * VEC < nc)
+                   ? __ldcs(reinterpret_cast<const uint4*>(x + (r0 + rr) * p.ld_x + c0 + cv * VEC))
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int i = t + 256 * j;
+      const int rr = i / VPR, cv = i % VPR;
+      const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+      if constexpr (sizeof(In) == 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tile[rr][cv * 4 + k] = __uint_as_float(w[k]);
       } else {
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) v[k] = 0.f;
+        for (int k = 0; k < 4; ++k) {
+          tile[rr][cv * 8 + 2 * k] = __uint_as_float(w[k] << 16);
+          tile[rr][cv * 8 + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
       }
-#pragma unroll
-      for (int k = 0; k < VEC; ++k) tile[rr][cv * VEC + k] = v[k];
     }
   } else {
     for (int i = t; i < kColTileR * kColTileC; i += 256) {
@@ -268,7 +312,8 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok) {
     }
   }
   __syncthreads();
-  // Thread (col, part) owns rows 32*part .. 32*part+31 of one column.
+  // Thread (col, part) owns rows 32*part .. 32*part+31 of one column, held in
+  // registers from here on.
   const int col = t % kColTileC, part = t / kColTileC;
   const int rbase = part * 32;
   const int br = p.br;
@@ -277,8 +322,10 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok) {
   for (int i = 0; i < 16; ++i) m0 = fmaxf(m0, fabsf(tile[rbase + i][col]));
 #pragma unroll
   for (int i = 16; i < 32; ++i) m1 = fmaxf(m1, fabsf(tile[rbase + i][col]));
-  pmax[part][col] = fmaxf(m0, m1);
-  __syncthreads();
+  if (br > 32) {
+    pmax[part][col] = fmaxf(m0, m1);
+    __syncthreads();
+  }
   const bool active = rbase < nr && col < nc;
   // Scales of the (one or two) blocks this thread's 32 rows belong to.
   float amax_a, amax_b;
@@ -313,11 +360,9 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok) {
     // 32 consecutive output elements of row `gc` of the transposed array.
     uint32_t w[8];
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const float s = (g < 4) ? sa.s : sb.s;
-      w[g] = encode4(tile[rbase + 4 * g][col], tile[rbase + 4 * g + 1][col], tile[rbase + 4 * g + 2][col],
-                     tile[rbase + 4 * g + 3][col], s, p.code);
-    }
+    for (int g = 0; g < 8; ++g)
+      w[g] = encode4<POW2>(tile[rbase + 4 * g][col], tile[rbase + 4 * g + 1][col], tile[rbase + 4 * g + 2][col],
+                     tile[rbase + 4 * g + 3][col], g < 4 ? sa : sb, p.code);
     const int64_t e = (c0 + col) * p.ld_codes + r0 + rbase;
     const bool full32 = rbase + 32 <= nr;  // else only the first 16 rows exist
     if (p.code == BSMM_E2M1) {
@@ -332,9 +377,9 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok) {
     }
   } else {
     // Row-major codes: lanes hold consecutive columns.
+#pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float s = (i < 16) ? sa.s : sb.s;
-      const uint32_t cval = encode1(tile[rbase + i][col], s, p.code);
+      const uint32_t cval = encode1<POW2>(tile[rbase + i][col], i < 16 ? sa : sb, p.code);
       const int64_t e = (r0 + rbase + i) * p.ld_codes + c0 + col;
       const bool ok = active && rbase + i < nr;
       if (p.code == BSMM_E2M1) {
@@ -350,7 +395,7 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok) {
 // ---------------------------------------------------------------------------
 // 128 x 128 blocks
 // ---------------------------------------------------------------------------
-template <typename In>
+template <typename In, bool POW2>
 __global__ void __launch_bounds__(256) quant_tile(QP p) {
   __shared__ float wmax[8];
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
@@ -381,7 +426,7 @@ __global__ void __launch_bounds__(256) quant_tile(QP p) {
   const int64_t e = (r0 + row) * p.ld_codes + c0 + half * 64;
   uint32_t w[16];
 #pragma unroll
-  for (int g = 0; g < 16; ++g) w[g] = encode4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3], sc.s, p.code);
+  for (int g = 0; g < 16; ++g) w[g] = encode4<POW2>(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3], sc, p.code);
   if (p.code == BSMM_E2M1) {
 #pragma unroll
     for (int g = 0; g < 2; ++g)
@@ -398,7 +443,7 @@ __global__ void __launch_bounds__(256) quant_tile(QP p) {
 // ---------------------------------------------------------------------------
 // Whole-row and whole-column blocks, and the generic fallback
 // ---------------------------------------------------------------------------
-template <typename In>
+template <typename In, bool POW2>
 __global__ void __launch_bounds__(256) quant_wrow(QP p) {
   __shared__ float wmax[8];
   const int64_t r = blockIdx.x;
@@ -417,18 +462,18 @@ __global__ void __launch_bounds__(256) quant_wrow(QP p) {
   uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
   if (p.code == BSMM_E2M1) {
     for (int64_t c = 2 * t; c < p.cols; c += 512) {
-      const uint32_t lo = encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code);
-      const uint32_t hi = (c + 1 < p.cols) ? encode1(load1<In>(x, r * p.ld_x + c + 1), sc.s, p.code) : 0u;
+      const uint32_t lo = encode1<POW2>(load1<In>(x, r * p.ld_x + c), sc, p.code);
+      const uint32_t hi = (c + 1 < p.cols) ? encode1<POW2>(load1<In>(x, r * p.ld_x + c + 1), sc, p.code) : 0u;
       out[(r * p.ld_codes + c) / 2] = static_cast<uint8_t>(lo | (hi << 4));
     }
   } else {
     for (int64_t c = t; c < p.cols; c += 256)
-      out[r * p.ld_codes + c] = static_cast<uint8_t>(encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code));
+      out[r * p.ld_codes + c] = static_cast<uint8_t>(encode1<POW2>(load1<In>(x, r * p.ld_x + c), sc, p.code));
   }
 }
 
 // One CTA per 32 columns, 8 warps striding down the rows.
-template <typename In>
+template <typename In, bool POW2>
 __global__ void __launch_bounds__(256) quant_wcol(QP p) {
   __shared__ float wmax[8][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -452,17 +497,17 @@ __global__ void __launch_bounds__(256) quant_wcol(QP p) {
     if (!cok) return;
     if (fp4) {
       for (int64_t r = 2 * warp; r < p.rows; r += 16) {
-        const uint32_t lo = encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code);
-        const uint32_t hi = (r + 1 < p.rows) ? encode1(load1<In>(x, (r + 1) * p.ld_x + c), sc.s, p.code) : 0u;
+        const uint32_t lo = encode1<POW2>(load1<In>(x, r * p.ld_x + c), sc, p.code);
+        const uint32_t hi = (r + 1 < p.rows) ? encode1<POW2>(load1<In>(x, (r + 1) * p.ld_x + c), sc, p.code) : 0u;
         out[(c * p.ld_codes + r) / 2] = static_cast<uint8_t>(lo | (hi << 4));
       }
     } else {
       for (int64_t r = warp; r < p.rows; r += 8)
-        out[c * p.ld_codes + r] = static_cast<uint8_t>(encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code));
+        out[c * p.ld_codes + r] = static_cast<uint8_t>(encode1<POW2>(load1<In>(x, r * p.ld_x + c), sc, p.code));
     }
   } else {
     for (int64_t r = warp; r < p.rows; r += 8) {
-      const uint32_t v = cok ? encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code) : 0u;
+      const uint32_t v = cok ? encode1<POW2>(load1<In>(x, r * p.ld_x + c), sc, p.code) : 0u;
       if (fp4) {
         const uint32_t hi = __shfl_down_sync(0xffffffffu, v, 1);
         if (cok && (lane & 1) == 0) out[(r * p.ld_codes + c) / 2] = static_cast<uint8_t>(v | (hi << 4));
@@ -475,7 +520,7 @@ __global__ void __launch_bounds__(256) quant_wcol(QP p) {
 
 // One thread per block; any block shape that divides the array (E2M1 needs
 // an even block extent along the output's contiguous axis).
-template <typename In>
+template <typename In, bool POW2>
 __global__ void __launch_bounds__(256) quant_any(QP p) {
   const int64_t nbr = p.rows / p.br, nbc = p.cols / p.bc;
   const int64_t bid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -491,7 +536,7 @@ __global__ void __launch_bounds__(256) quant_any(QP p) {
   for (int i = 0; i < p.br; ++i) {
     for (int j = 0; j < p.bc; ++j) {
       const int64_t r = bi * p.br + i, c = bj * p.bc + j;
-      const uint32_t v = encode1(load1<In>(x, r * p.ld_x + c), sc.s, p.code);
+      const uint32_t v = encode1<POW2>(load1<In>(x, r * p.ld_x + c), sc, p.code);
       const int64_t e = p.transpose ? c * p.ld_codes + r : r * p.ld_codes + c;
       if (p.code == BSMM_E2M1) {
         uint8_t& byte = out[e / 2];
@@ -505,7 +550,7 @@ __global__ void __launch_bounds__(256) quant_any(QP p) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-template <typename In>
+template <typename In, bool POW2>
 cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
   const int esz = sizeof(In);
   const bool x_vec = aligned(p.x, 16) && (p.ld_x * esz) % 16 == 0 && p.cols % (16 / esz) == 0;
@@ -513,23 +558,22 @@ cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
   const bool pow2_small = (p.bc == 16 || p.bc == 32 || p.bc == 64 || p.bc == 128);
   const bool pow2_small_r = (p.br == 16 || p.br == 32 || p.br == 64 || p.br == 128);
   if (p.br == 1 && pow2_small && !p.transpose && x_vec && codes16) {
-    const int64_t vecs = p.rows * (p.cols / (16 / esz));
-    int64_t blocks = ceil_div(vecs, 256 * kRowsUnroll);
+    int64_t blocks = ceil_div(p.rows * (p.cols / kSlice), 256 * 2);
     blocks = std::min<int64_t>(blocks, static_cast<int64_t>(ctx->num_sms) * 8);
-    quant_rows<In><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(p);
+    quant_rows<In, POW2><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(p);
   } else if (p.bc == 1 && pow2_small_r && (!p.transpose || (codes16 && p.ld_codes % 32 == 0))) {
     dim3 grid(static_cast<unsigned>(ceil_div(p.cols, kColTileC)), static_cast<unsigned>(ceil_div(p.rows, kColTileR)));
-    quant_cols<In><<<grid, 256, 0, s>>>(p, x_vec ? 1 : 0);
+    quant_cols<In, POW2><<<grid, 256, 0, s>>>(p, x_vec ? 1 : 0);
   } else if (p.br == 128 && p.bc == 128 && !p.transpose && x_vec && codes16) {
     dim3 grid(static_cast<unsigned>(p.cols / 128), static_cast<unsigned>(p.rows / 128));
-    quant_tile<In><<<grid, 256, 0, s>>>(p);
+    quant_tile<In, POW2><<<grid, 256, 0, s>>>(p);
   } else if (p.br == 1 && p.bc == p.cols && !p.transpose) {
-    quant_wrow<In><<<static_cast<unsigned>(p.rows), 256, 0, s>>>(p);
+    quant_wrow<In, POW2><<<static_cast<unsigned>(p.rows), 256, 0, s>>>(p);
   } else if (p.bc == 1 && p.br == p.rows) {
-    quant_wcol<In><<<static_cast<unsigned>(ceil_div(p.cols, 32)), 256, 0, s>>>(p);
+    quant_wcol<In, POW2><<<static_cast<unsigned>(ceil_div(p.cols, 32)), 256, 0, s>>>(p);
   } else {
     const int64_t nblk = (p.rows / p.br) * (p.cols / p.bc);
-    quant_any<In><<<static_cast<unsigned>(ceil_div(nblk, 256)), 256, 0, s>>>(p);
+    quant_any<In, POW2><<<static_cast<unsigned>(ceil_div(nblk, 256)), 256, 0, s>>>(p);
   }
   return cudaGetLastError();
 }
@@ -541,7 +585,11 @@ cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s) {
   if (!ctx) return cudaErrorInitializationError;
   QP p{q.x, q.rows, q.cols, q.ld_x, q.br, q.bc, q.code, q.scale, q.transpose ? 1 : 0,
        q.codes, q.ld_codes, q.scales, q.ld_scales};
-  return q.x_bf16 ? dispatch<__nv_bfloat16>(p, ctx, s) : dispatch<float>(p, ctx, s);
+  // UE8M0 scales are powers of two: the codes divide by multiplying with the
+  // exact reciprocal.
+  const bool pow2 = q.scale == BSMM_SCALE_UE8M0;
+  if (q.x_bf16) return pow2 ? dispatch<__nv_bfloat16, true>(p, ctx, s) : dispatch<__nv_bfloat16, false>(p, ctx, s);
+  return pow2 ? dispatch<float, true>(p, ctx, s) : dispatch<float, false>(p, ctx, s);
 }
 
 }  // namespace bsmm
