@@ -182,7 +182,7 @@ class Work:
 class GroupedWork(Work):
     """block_scaled_mm problems: raw float32 a [m,k], b [n,k] in HBM; a step
     quantizes both (1x128, 128x128) and runs the FP32-scale GEMM."""
-    dominant = "block-scaled FP32-scale GEMM (tc_gemm kF32Scale)"
+    dominant = "block-scaled FP32-scale GEMM (tc_gemm_pair kPairF32; tc_gemm kF32Scale below one tile per cluster)"
 
     def __init__(self, workload: W.Workload, device):
         import block_scaled_precision_gemm_gb300 as bsmm
@@ -295,7 +295,7 @@ class MxWork(Work):
             self.sa = (raw[2] + 127).to(torch.uint8)
             self.sb = (raw[3] + 127).to(torch.uint8)
             self.types = ("e4m3", "e4m3", "ue8m0")
-            self.dominant = "MXFP8 block-scaled GEMM call (sf_relayout + tc_gemm kMXF8)"
+            self.dominant = "MXFP8 block-scaled GEMM call (sf_relayout + tc_gemm_pair kPairMXF8)"
         else:
             self.a, self.b = raw[0], raw[1]
             self.sa = raw[2].to(torch.float8_e4m3fn).view(torch.uint8)
@@ -303,7 +303,7 @@ class MxWork(Work):
             self.types = ("e2m1", "e2m1", "ue4m3")
             self.peak_kind = "fp4"
             self.dtype = "e2m1 (f32 accumulate)"
-            self.dominant = "NVFP4 block-scaled GEMM call (sf_relayout + tc_gemm kNVF4)"
+            self.dominant = "NVFP4 block-scaled GEMM call (sf_relayout + tc_gemm_pair kPairNVF4)"
         del raw
         self.y = torch.empty((p.B, p.M, p.N), dtype=torch.float32, device=device)
         self.ws = torch.empty(bsmm.gemm_workspace_size(p.B, p.M, p.N, p.K, self.types[0]), dtype=torch.uint8,
@@ -330,7 +330,7 @@ class BackwardWork(Work):
     """NKI MXFP8 linear backward, M=16384, N=K=8192: a step quantizes dY (along
     N and along M), W (along N) and X (along M) to E5M2 and runs dX = dY.W and
     dW = dY^T.X with bf16 outputs."""
-    dominant = "MXFP8 backward call (4 quantizers + 2 x (sf_relayout + tc_gemm kMXF8))"
+    dominant = "MXFP8 backward call (4 quantizers + 2 x (sf_relayout + tc_gemm_pair kPairMXF8))"
     dtype = "e5m2 (f32 accumulate, bf16 out)"
 
     def __init__(self, workload, device):

@@ -1,29 +1,41 @@
-// FP32-scale block GEMM on a CTA pair (tcgen05 .cta_group::2), 256 x 256 tiles.
+// Block-scaled GEMMs on a CTA pair (tcgen05 .cta_group::2), 256 x 256 tiles.
 //
-// Computes y[m,n] = sum_kb sa[m,kb] * sb[n/128,kb] * (a . b over K block kb)
-// (atrex-bench #002 block_scaled_mm, Reference Implementation) like the
-// single-CTA kernel, but two CTAs of a cluster share one 256 x 256 output
-// tile: CTA r loads rows 128r..128r+127 of the A tile and of the B tile, and
-// the leader (rank 0) issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
-// K = 32), which reads both CTAs' shared memory and writes a 128 x 256 FP32
-// partial into each CTA's tensor memory.  N = 256 instructions keep the tensor
-// pipe busy (N = 128 ones run it at about half rate), and per SM the operands
-// are 32 KB per 128-K block for twice the FLOPs of a 128 x 128 tile.
+// Two CTAs of a cluster share one 256 x 256 output tile: CTA r loads rows
+// 128r..128r+127 of the A tile and of the B tile, the leader (rank 0) issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 256), which reads both CTAs' shared
+// memory and writes a 128 x 256 FP32 result into each CTA's tensor memory.
+// N = 256 instructions keep the tensor pipe busy (N = 128 ones run it at about
+// half rate), and per SM the operands are 32 KB per 128-byte K block for twice
+// the FLOPs of a 128 x 128 tile on one CTA.  Three modes:
+//
+//   kPairF32   y = sum_kb sa[m,kb] * sb[n/128,kb] * (a . b over K block kb)
+//              (atrex-bench #002 block_scaled_mm, Reference Implementation):
+//              kind::f8f6f4, one FP32 partial per 128-K block in one of two
+//              256-column TMEM buffers, promoted into registers by the epilogue.
+//   kPairMXF8  jax.nn.scaled_matmul with MXFP8 (Notes, cuDNN on Blackwell):
+//              kind::mxf8f6f4.block_scale.block32, UE8M0 scale per 32 K.
+//   kPairNVF4  the same with NVFP4: kind::mxf4nvf4.block_scale.block16, packed
+//              E2M1 operands, UE4M3 scale per 16 K.
+// In the block-scaled modes the result accumulates over all of K in one
+// 256-column TMEM buffer; each stage's scale-factor atoms are copied into TMEM
+// with tcgen05.cp.cta_group::2, which moves each CTA's own shared memory into
+// its own tensor memory, so each CTA holds the scales of its 128 A rows and of
+// all 256 B rows.
 //
 // Synchronization across the pair:
 //   full[s]   in the leader, 2 arrivals (leader with expect_tx for both CTAs'
 //             bytes, peer remotely); both CTAs' TMA loads complete on it.
 //   empty[s]  in both CTAs; the leader's MMA commit multicasts to both.
-//   tfull[i]  in both CTAs; multicast commit after each K block's MMAs.
+//   tfull[i]  in both CTAs; multicast commit when a TMEM buffer is ready.
 //   tempty[i] in the leader, 32 arrivals (16 epilogue warps of each CTA).
+// Cross-CTA arrivals are relaxed: each follows tcgen05.wait::ld or a TMA issue,
+// and a release at cluster scope costs the arriving thread ~1.2k cycles.
 // Every wait is bounded; on expiry a CTA records the site and winds down.
 //
-// Epilogue: 16 warps per CTA (four per TMEM lane quarter).  Warp w reads
-// lanes 32*(w%4).. (its 32 rows) and one 64-column quarter of the tile; the
-// running FP32 sum of its 64 columns lives in registers.  Reading every K
-// block's partial out of tensor memory is the other bound of this kernel: one
-// warp moves ~28 B/clk from TMEM, and the promotion needs 128 x 256 x 4 bytes
-// per 128-K block, hence sixteen reading warps.
+// Epilogue: 16 warps per CTA (four per TMEM lane quarter).  Warp w reads lanes
+// 32*(w%4).. (its 32 rows) and one 64-column quarter of the tile.  In kPairF32
+// reading every K block's partial out of tensor memory is the other bound of
+// this kernel: one warp moves ~28 B/clk from TMEM, hence sixteen reading warps.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -35,61 +47,96 @@
 namespace bsmm {
 namespace {
 
+enum PairMode { kPairF32 = 0, kPairMXF8 = 1, kPairNVF4 = 2 };
+
 constexpr int PM = 256, PN = 256;          // pair tile
-constexpr int HALF = 128;                  // A rows per CTA
-constexpr int BHALF = PN / 2;              // B rows per CTA
-constexpr int KB = 128;                    // K bytes per stage (128 FP8 elements)
-constexpr int STAGES = 5;
+constexpr int HALF = 128;                  // A rows and B rows per CTA
+constexpr int KB = 128;                    // K bytes per stage
 constexpr int THREADS = 640;               // 4 control warps + 16 epilogue warps
 constexpr int EPI_WARPS = 16;
 constexpr int EPI_COLS = 64;               // columns per epilogue thread
-constexpr int TMEM_COLS = 512;             // two 256-column partial buffers
-constexpr int NACC = 2;
+constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
-constexpr int A_BYTES = HALF * KB, B_BYTES = BHALF * KB;
-constexpr int STAGE_TX = A_BYTES + B_BYTES;  // per CTA
-constexpr int STG_PER_WARP = 4096;        // one 32-row x 128-byte staging buffer
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_STG = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_PER_WARP;
-constexpr int N_BARS = 2 * STAGES + 2 * NACC + 1;
-constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;
-static_assert(SMEM <= 232448, "shared memory budget");
+constexpr int A_BYTES = HALF * KB, B_BYTES = HALF * KB;
+constexpr int STG_PER_WARP = 4096;         // one 32-row x 128-byte staging buffer
+
+template <int MODE>
+struct PCfg {
+  static constexpr int ATOMS = MODE == kPairMXF8 ? 1 : (MODE == kPairNVF4 ? 4 : 0);  // per K block per 128 rows
+  static constexpr int STAGES = MODE == kPairF32 ? 5 : 4;
+  static constexpr int SFA_BYTES = ATOMS * 512;      // this CTA's 128 A rows
+  static constexpr int SFB_BYTES = 2 * ATOMS * 512;  // all 256 B rows
+  static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + SF_BYTES;  // per CTA
+  static constexpr int NACC = MODE == kPairF32 ? 2 : 1;
+  static constexpr int SF_COL0 = NACC * PN;
+  static constexpr int SFA_COLS = ATOMS * 4;
+  static constexpr int SFB_COLS = 2 * ATOMS * 4;
+  static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_STG = (OFF_SF + STAGES * SF_BYTES + 1023) / 1024 * 1024;
+  static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_PER_WARP;
+  static constexpr int N_BARS = 2 * STAGES + 2 * NACC + 1;
+  static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
+};
 
 enum Site { kSiteProducer = 11, kSiteMmaTmem = 12, kSiteMmaFull = 13, kSiteEpilogue = 14, kSiteDrain = 15,
             kSiteDone = 16 };
 
 struct PairParams {
   int M, N, K;
-  int m_tiles, n_tiles, k_tiles;  // tiles of 256 x 256
-  int num_tiles;
+  int batches;
+  int m_tiles, n_tiles, k_tiles;  // tiles of 256 x 256, K blocks of 128 bytes
+  int num_tiles;                  // over all batches
+  // kPairF32
   const float* a_scales;
   const float* b_scales;
   int kb;  // K / 128
+  // block-scaled: atoms [batch][row tile of 128][K atom] of 512 B, read
+  // through 2-D tensor maps of 128-byte rows (an atom is 4 rows)
+  int sfa_rt, sfb_rt, ks4;
+  int y_bf16;
   uint32_t idesc;
   int* status;
   uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ void decode_pair_tile(const PairParams& p, int t, int& mb, int& nb) {
+__device__ __forceinline__ void decode_pair_tile(const PairParams& p, int t, int& b, int& mb, int& nb) {
+  const int per_batch = p.m_tiles * p.n_tiles;
+  b = t / per_batch;
+  const int r = t - b * per_batch;
   const int span = GROUP_M * p.n_tiles;
-  const int g = t / span;
-  const int within = t - g * span;
+  const int g = r / span;
+  const int within = r - g * span;
   const int rows = min(GROUP_M, p.m_tiles - g * GROUP_M);
   mb = g * GROUP_M + within % rows;
   nb = within / rows;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2_pair(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    tc_gemm_pair_f32scale(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmY, const PairParams p) {
+    tc_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmSFA,
+                 const __grid_constant__ CUtensorMap tmSFB, const PairParams p) {
+  using C = PCfg<MODE>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int NACC = C::NACC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem + OFF_A;
-  uint8_t* sB = smem + OFF_B;
-  uint8_t* stg = smem + OFF_STG;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sB = smem + C::OFF_B;
+  uint8_t* sSF = smem + C::OFF_SF;
+  uint8_t* stg = smem + C::OFF_STG;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + NACC;
@@ -139,17 +186,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
       for (int t = cid; ok && t < p.num_tiles; t += ncl) {
-        int mb, nb;
-        decode_pair_tile(p, t, mb, nb);
+        int b, mb, nb;
+        decode_pair_tile(p, t, b, mb, nb);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteProducer)) {
             ok = false;
             break;
           }
           const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_TX);
-          tma_load_3d_pair(sA + stage * A_BYTES, &tmA, full_leader, kt * KB, mb * PM + rank * HALF, 0);
-          tma_load_3d_pair(sB + stage * B_BYTES, &tmB, full_leader, kt * KB, nb * PN + rank * BHALF, 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_TX);
+          tma_load_3d_pair(sA + stage * A_BYTES, &tmA, full_leader, kt * KB, mb * PM + rank * HALF, b);
+          tma_load_3d_pair(sB + stage * B_BYTES, &tmB, full_leader, kt * KB, nb * PN + rank * HALF, b);
+          if constexpr (MODE != kPairF32) {
+            // atoms as rows of 128 bytes: atom j of row tile rt of batch b
+            // starts at row 4 * ((b * rt_count + rt) * ks4 + j)
+            uint8_t* sf = sSF + stage * C::SF_BYTES;
+            const int a_row = 4 * ((b * p.sfa_rt + 2 * mb + static_cast<int>(rank)) * p.ks4 + kt * C::ATOMS);
+            tma_load_3d_pair(sf, &tmSFA, full_leader, 0, a_row, 0);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int b_row = 4 * ((b * p.sfb_rt + 2 * nb + r) * p.ks4 + kt * C::ATOMS);
+              tma_load_3d_pair(sf + C::SFA_BYTES + r * C::ATOMS * 512, &tmSFB, full_leader, 0, b_row, 0);
+            }
+          }
           if (!leader) mbar_arrive_cluster(full_leader);
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -183,12 +242,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0, tph = 0;
       bool ok = true;
       for (int t = cid; ok && t < p.num_tiles; t += ncl) {
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
-            ok = false;
-            break;
-          }
+        if constexpr (MODE != kPairF32) {
+          if (!mbar_wait(&tempty[0], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) break;
           tc_fence_after();
+        }
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if constexpr (MODE == kPairF32) {
+            if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
             ok = false;
             break;
@@ -197,20 +262,54 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
           const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
           const uint32_t d = tmem + static_cast<uint32_t>(tb * PN);
+          if constexpr (MODE == kPairF32) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f8f6f4_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
-                            p.idesc, k > 0 ? 1u : 0u);
-          tc_commit_pair_mc(&empty[stage], 0x3);
-          tc_commit_pair_mc(&tfull[tb], 0x3);
-          if (++tb == NACC) {
-            tb = 0;
-            tph ^= 1u;
+            for (int k = 0; k < 4; ++k)
+              mma_f8f6f4_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
+                              p.idesc, k > 0 ? 1u : 0u);
+            tc_commit_pair_mc(&empty[stage], 0x3);
+            tc_commit_pair_mc(&tfull[tb], 0x3);
+            if (++tb == NACC) {
+              tb = 0;
+              tph ^= 1u;
+            }
+          } else {
+            const uint32_t sfa_t = tmem + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
+            const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+            const uint32_t sf_s = smem_u32(sSF + stage * C::SF_BYTES);
+            // A atom i (K sub-block i) -> columns sfa_t + 4i; B atom (row tile
+            // r, K sub-block i) -> columns sfb_t + 4*(2i + r).
+#pragma unroll
+            for (int i = 0; i < C::ATOMS; ++i) tc_cp_sf_pair(sfa_t + 4 * i, smem_desc(sf_s + 512 * i, 0, 128, 0));
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+              for (int i = 0; i < C::ATOMS; ++i)
+                tc_cp_sf_pair(sfb_t + 4 * (2 * i + r),
+                              smem_desc(sf_s + C::SFA_BYTES + 512 * (r * C::ATOMS + i), 0, 128, 0));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = smem_desc(a_base + 32 * k, 16, 1024, 2);
+              const uint64_t bd = smem_desc(b_base + 32 * k, 16, 1024, 2);
+              const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
+              if constexpr (MODE == kPairMXF8) {
+                const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+                mma_mxf8_pair(d, ad, bd, idesc, sfa_t, sfb_t, acc);
+              } else {
+                mma_nvf4_pair(d, ad, bd, p.idesc, sfa_t + 4 * k, sfb_t + 8 * k, acc);
+              }
+            }
+            tc_commit_pair_mc(&empty[stage], 0x3);
           }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
+        }
+        if constexpr (MODE != kPairF32) {
+          if (!ok) break;
+          tc_commit_pair_mc(&tfull[0], 0x3);
+          tph ^= 1u;
         }
       }
       tc_commit_pair_mc(done, 0x1);
@@ -228,70 +327,115 @@ __global__ void __launch_bounds__(THREADS, 1)
     int tb = 0;
     uint32_t tph = 0;
     for (int t = cid; t < p.num_tiles; t += ncl) {
-      int mb, nb;
-      decode_pair_tile(p, t, mb, nb);
+      int b, mb, nb;
+      decode_pair_tile(p, t, b, mb, nb);
       const int row0 = mb * PM + static_cast<int>(rank) * HALF + q * 32;
       const int row = row0 + lane;
       const int col0 = nb * PN + g * COLS;
-      const bool row_ok = row < p.M, col_ok = col0 < p.N;  // N % 128 == 0: a quarter is all in or all out
-      const float* sa_row = p.a_scales + static_cast<size_t>(row_ok ? row : 0) * p.kb;
-      const float* sb_row = p.b_scales + static_cast<size_t>(col_ok ? col0 / 128 : 0) * p.kb;
+      const bool col_ok = col0 < p.N;
       float acc[COLS];
-#pragma unroll
-      for (int i = 0; i < COLS; ++i) acc[i] = 0.f;
-      float sa_next = row_ok ? __ldg(sa_row) : 0.f;
-      float sb_next = col_ok ? __ldg(sb_row) : 0.f;
       bool ok = true;
-      for (int kt = 0; kt < p.k_tiles; ++kt) {
-        const float s = sa_next * sb_next;
-        if (kt + 1 < p.k_tiles) {
-          sa_next = row_ok ? __ldg(sa_row + kt + 1) : 0.f;
-          sb_next = col_ok ? __ldg(sb_row + kt + 1) : 0.f;
+      if constexpr (MODE == kPairF32) {
+        const bool row_ok = row < p.M;  // N % 128 == 0: a quarter is all in or all out
+        const float* sa_row = p.a_scales + static_cast<size_t>(row_ok ? row : 0) * p.kb;
+        const float* sb_row = p.b_scales + static_cast<size_t>(col_ok ? col0 / 128 : 0) * p.kb;
+#pragma unroll
+        for (int i = 0; i < COLS; ++i) acc[i] = 0.f;
+        float sa_next = row_ok ? __ldg(sa_row) : 0.f;
+        float sb_next = col_ok ? __ldg(sb_row) : 0.f;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          const float s = sa_next * sb_next;
+          if (kt + 1 < p.k_tiles) {
+            sa_next = row_ok ? __ldg(sa_row + kt + 1) : 0.f;
+            sb_next = col_ok ? __ldg(sb_row + kt + 1) : 0.f;
+          }
+          if (!mbar_wait(&tfull[tb], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(tb * PN + g * COLS);
+#pragma unroll
+          for (int h = 0; h < COLS / 32; ++h) {  // two loads in flight per wait
+            uint32_t r0[16], r1[16];
+            tmem_ld16(taddr + 32 * h, r0);
+            tmem_ld16(taddr + 32 * h + 16, r1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[32 * h + j] = fmaf(__uint_as_float(r0[j]), s, acc[32 * h + j]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[32 * h + 16 + j] = fmaf(__uint_as_float(r1[j]), s, acc[32 * h + 16 + j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[tb]), 0));
+          if (++tb == NACC) {
+            tb = 0;
+            tph ^= 1u;
+          }
         }
-        if (!mbar_wait(&tfull[tb], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
+      } else {
+        if (!mbar_wait(&tfull[0], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
           ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(tb * PN + g * COLS);
+        } else {
+          tc_fence_after();
+          const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(g * COLS);
 #pragma unroll
-        for (int h = 0; h < COLS / 32; ++h) {  // two loads in flight per wait
-          uint32_t r0[16], r1[16];
-          tmem_ld16(taddr + 32 * h, r0);
-          tmem_ld16(taddr + 32 * h + 16, r1);
-          tmem_wait_ld();
+          for (int h = 0; h < COLS / 32; ++h) {
+            uint32_t r0[16], r1[16];
+            tmem_ld16(taddr + 32 * h, r0);
+            tmem_ld16(taddr + 32 * h + 16, r1);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[32 * h + j] = fmaf(__uint_as_float(r0[j]), s, acc[32 * h + j]);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) acc[32 * h + 16 + j] = fmaf(__uint_as_float(r1[j]), s, acc[32 * h + 16 + j]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[tb]), 0));
-        if (++tb == NACC) {
-          tb = 0;
+            for (int j = 0; j < 16; ++j) {
+              acc[32 * h + j] = __uint_as_float(r0[j]);
+              acc[32 * h + 16 + j] = __uint_as_float(r1[j]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[0]), 0));
           tph ^= 1u;
         }
       }
       if (!ok) break;
       if (row0 >= p.M || !col_ok) continue;  // this warp's box lies outside y
-      // 64 columns of 32 rows leave as two 32 x 32 TMA stores
+      if (!p.y_bf16) {
+        // 64 FP32 columns of 32 rows leave as two 32 x 32 TMA stores
 #pragma unroll
-      for (int c = 0; c < COLS / 32; ++c) {
-        uint8_t* buf = my_stg;
+        for (int c = 0; c < COLS / 32; ++c) {
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float* v = &acc[32 * c + 4 * j];
+            const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
+            *reinterpret_cast<uint4*>(my_stg + off) = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                                                                 __float_as_uint(v[2]), __float_as_uint(v[3]));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmY, my_stg, col0 + 32 * c, row0, b);
+            bulk_commit();
+          }
+        }
+      } else {
+        // 64 bf16 columns (128 bytes) of 32 rows: one TMA store
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float* v = &acc[32 * c + 4 * j];
+          const float* v = &acc[8 * j];
           const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
-          *reinterpret_cast<uint4*>(buf + off) =
-              make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+          *reinterpret_cast<uint4*>(my_stg + off) =
+              make_uint4(pack_bf16x2_pair(v[0], v[1]), pack_bf16x2_pair(v[2], v[3]), pack_bf16x2_pair(v[4], v[5]),
+                         pack_bf16x2_pair(v[6], v[7]));
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&tmY, buf, col0 + 32 * c, row0, 0);
+          tma_store_3d(&tmY, my_stg, col0, row0, b);
           bulk_commit();
         }
       }
@@ -308,15 +452,64 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-int g_pair_clusters[64] = {};
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+int g_pair_clusters[3][64] = {};  // max co-resident clusters per mode and device
+
+template <int MODE>
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const CUtensorMap& tsa,
+                        const CUtensorMap& tsb, const PairParams& p, const DeviceCtx* ctx, cudaStream_t s,
+                        std::string* why) {
+  using C = PCfg<MODE>;
+  auto kern = tc_gemm_pair<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (ctx->device < 0 || ctx->device >= 64) {
+    *why = "device ordinal beyond the library's table";
+    return cudaErrorInvalidDevice;
+  }
+  int& max_clusters = g_pair_clusters[MODE][ctx->device];
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * (ctx->num_sms / 2));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) {
+      *why = "no cluster of two CTAs fits on this device";
+      return cudaErrorInvalidConfiguration;
+    }
+    max_clusters = n;
+  }
+  const int clusters = std::max(1, std::min(p.num_tiles, max_clusters));
+  cfg.gridDim = dim3(2 * clusters);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, tsa, tsb, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+uint32_t f8_code(int dtype) { return dtype == BSMM_E5M2 ? 1u : 0u; }
+
+// Tiles of 256 x 256 over all batches.
+int64_t pair_tiles(int64_t B, int64_t M, int64_t N) { return B * ceil_div(M, PM) * ceil_div(N, PN); }
 
 }  // namespace
 
 bool grouped_pair_eligible(int64_t M, int64_t N, int64_t K, const DeviceCtx* ctx) {
   // The pair kernel stores through TMA (N*4 % 16 == 0 holds: N % 128 == 0)
   // and wants at least one 256 x 256 tile per cluster.
-  const int64_t tiles = ceil_div(M, PM) * ceil_div(N, PN);
-  return K % 128 == 0 && N % 128 == 0 && tiles >= ctx->num_sms / 2;
+  return K % 128 == 0 && N % 128 == 0 && pair_tiles(1, M, N) >= ctx->num_sms / 2;
 }
 
 cudaError_t launch_grouped_gemm_pair(const GroupedGemmRequest& r, cudaStream_t s, std::string* why) {
@@ -324,7 +517,7 @@ cudaError_t launch_grouped_gemm_pair(const GroupedGemmRequest& r, cudaStream_t s
   if (!ctx) return cudaErrorInitializationError;
   CUtensorMap ta, tb, ty;
   if (!make_tmap_3d(&ta, r.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, r.K, r.M, 1, KB, HALF, true) ||
-      !make_tmap_3d(&tb, r.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, r.K, r.N, 1, KB, BHALF, true) ||
+      !make_tmap_3d(&tb, r.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, r.K, r.N, 1, KB, HALF, true) ||
       !make_tmap_3d(&ty, r.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, r.N, r.M, 1, 32, 32, true)) {
     *why = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
@@ -333,6 +526,7 @@ cudaError_t launch_grouped_gemm_pair(const GroupedGemmRequest& r, cudaStream_t s
   p.M = static_cast<int>(r.M);
   p.N = static_cast<int>(r.N);
   p.K = static_cast<int>(r.K);
+  p.batches = 1;
   p.m_tiles = static_cast<int>(ceil_div(r.M, PM));
   p.n_tiles = static_cast<int>(ceil_div(r.N, PN));
   p.k_tiles = static_cast<int>(r.K / 128);
@@ -343,39 +537,63 @@ cudaError_t launch_grouped_gemm_pair(const GroupedGemmRequest& r, cudaStream_t s
   p.status = ctx->status;
   p.timeout_ns = wait_timeout_ns();
   // kind::f8f6f4: D = F32, A/B E4M3 = 0 / E5M2 = 1, K-major, N = 256, M = 256 (pair).
-  p.idesc = (1u << 4) | ((r.a_fmt == BSMM_E5M2 ? 1u : 0u) << 7) | ((r.b_fmt == BSMM_E5M2 ? 1u : 0u) << 10) |
-            (static_cast<uint32_t>(PN >> 3) << 17) | (static_cast<uint32_t>(PM >> 4) << 24);
+  p.idesc = (1u << 4) | (f8_code(r.a_fmt) << 7) | (f8_code(r.b_fmt) << 10) | (static_cast<uint32_t>(PN >> 3) << 17) |
+            (static_cast<uint32_t>(PM >> 4) << 24);
+  // no scale-factor atoms in this mode: the operand maps stand in, unread
+  return launch_pair<kPairF32>(ta, tb, ty, ta, tb, p, ctx, s, why);
+}
 
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_f32scale, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int& max_clusters = g_pair_clusters[ctx->device];
-  if (max_clusters == 0) {
-    cfg.gridDim = dim3(2 * (ctx->num_sms / 2));
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_f32scale, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n <= 0) {
-      *why = "no cluster of two CTAs fits on this device";
-      return cudaErrorInvalidConfiguration;
-    }
-    max_clusters = n;
+bool mx_pair_eligible(const MxGemmRequest& r, const DeviceCtx* ctx) {
+  // TMA output stores need 16-byte rows and base; at least one tile per cluster.
+  const int esz = r.y_bf16 ? 2 : 4;
+  return (r.N * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(r.y) % 16 == 0 &&
+         pair_tiles(r.B, r.M, r.N) >= ctx->num_sms / 2;
+}
+
+cudaError_t launch_mx_gemm_pair(const MxGemmRequest& r, const MxAtoms& at, cudaStream_t s, std::string* why) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  const bool nv = r.nvf4;
+  const int atoms = nv ? 4 : 1;
+  const int64_t kbytes = nv ? r.K / 2 : r.K;
+  const int64_t sfa_rows = r.B * static_cast<int64_t>(at.sfa_rt) * at.ks4 * 4;  // 128-byte rows
+  const int64_t sfb_rows = r.B * static_cast<int64_t>(at.sfb_rt) * at.ks4 * 4;
+  CUtensorMap ta, tb, ty, tsa, tsb;
+  const bool ok =
+      make_tmap_3d(&ta, r.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, r.M, r.B, KB, HALF, true) &&
+      make_tmap_3d(&tb, r.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, r.N, r.B, KB, HALF, true) &&
+      make_tmap_3d(&ty, r.y, r.y_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   r.y_bf16 ? 2 : 4, r.N, r.M, r.B, r.y_bf16 ? 64 : 32, 32, true) &&
+      make_tmap_3d(&tsa, at.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, sfa_rows, 1, 128, 4 * atoms, false) &&
+      make_tmap_3d(&tsb, at.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, sfb_rows, 1, 128, 4 * atoms, false);
+  if (!ok) {
+    *why = "cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
   }
-  const int clusters = std::max(1, std::min(p.num_tiles, max_clusters));
-  cfg.gridDim = dim3(2 * clusters);
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_f32scale, ta, tb, ty, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  PairParams p{};
+  p.M = static_cast<int>(r.M);
+  p.N = static_cast<int>(r.N);
+  p.K = static_cast<int>(r.K);
+  p.batches = static_cast<int>(r.B);
+  p.m_tiles = static_cast<int>(ceil_div(r.M, PM));
+  p.n_tiles = static_cast<int>(ceil_div(r.N, PN));
+  p.k_tiles = at.k_tiles;
+  p.num_tiles = static_cast<int>(pair_tiles(r.B, r.M, r.N));
+  p.sfa_rt = at.sfa_rt;
+  p.sfb_rt = at.sfb_rt;
+  p.ks4 = at.ks4;
+  p.y_bf16 = r.y_bf16 ? 1 : 0;
+  p.status = ctx->status;
+  p.timeout_ns = wait_timeout_ns();
+  if (nv) {
+    // kind::mxf4nvf4: E2M1 = 1 for A and B, UE4M3 scales (bit 23 = 0), N = 256, M = 256 (pair).
+    p.idesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(PN >> 3) << 17) | (static_cast<uint32_t>(PM >> 4) << 24);
+    return launch_pair<kPairNVF4>(ta, tb, ty, tsa, tsb, p, ctx, s, why);
+  }
+  // kind::mxf8f6f4: E4M3 = 0 / E5M2 = 1, UE8M0 scales (bit 23 = 1), N = 256, M = 256 (pair).
+  p.idesc = (f8_code(r.a_fmt) << 7) | (f8_code(r.b_fmt) << 10) | (static_cast<uint32_t>(PN >> 3) << 17) | (1u << 23) |
+            (static_cast<uint32_t>(PM >> 4) << 24);
+  return launch_pair<kPairMXF8>(ta, tb, ty, tsa, tsb, p, ctx, s, why);
 }
 
 }  // namespace bsmm

@@ -548,6 +548,19 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
+  // Kernel choice: CTA-pair 256 x 256 tiles when there is a tile for every
+  // cluster, else one CTA per 128 x 128 tile.  BSMM_MX_KERNEL=pair|single
+  // overrides the choice (pair still needs TMA-storable output rows).
+  const char* force = std::getenv("BSMM_MX_KERNEL");
+  const bool want_pair = force && std::strcmp(force, "pair") == 0;
+  const bool want_single = force && std::strcmp(force, "single") == 0;
+  const int esz = r.y_bf16 ? 2 : 4;
+  const bool storable = (r.N * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(r.y) % 16 == 0;
+  if (!want_single && (want_pair ? storable : mx_pair_eligible(r, ctx))) {
+    const MxAtoms at{sfa, sfb, rt_rows(r.M), rt_rows(r.N), ks4, static_cast<int>(k_tiles)};
+    return launch_mx_gemm_pair(r, at, s, why);
+  }
+
   const int64_t kbytes = nv ? r.K / 2 : r.K;
   CUtensorMap ta, tb, ty;
   if (!make_tmap_3d(&ta, r.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, r.M, r.B, BK_BYTES, BM, true) ||

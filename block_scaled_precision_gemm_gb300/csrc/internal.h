@@ -67,6 +67,17 @@ struct MxGemmRequest {
 cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* why);
 // Same, with the scale-factor atoms in the library's static device array.
 cudaError_t launch_mx_gemm_noalloc(const MxGemmRequest& r, cudaStream_t s, std::string* why);
+// Scale-factor atoms already laid out by launch_mx_gemm: [batch][row tile of
+// 128 (sfa_rt / sfb_rt of them, an even count)][K atom (ks4)] x 512 bytes.
+struct MxAtoms {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int sfa_rt, sfb_rt, ks4, k_tiles;
+};
+// 256 x 256 tiles on CTA pairs (gemm_pair.cu); eligible when the output rows
+// suit TMA stores and there is at least one tile per cluster.
+bool mx_pair_eligible(const MxGemmRequest& r, const DeviceCtx* ctx);
+cudaError_t launch_mx_gemm_pair(const MxGemmRequest& r, const MxAtoms& at, cudaStream_t s, std::string* why);
 
 struct GroupedGemmRequest {
   int64_t M, N, K;

@@ -179,6 +179,25 @@ def test_mxfp8_scale_layout_one_hot(pattern):
     run_mx(1, 256, 256, 512, "e4m3", "e4m3", torch.float32, seed=41, pattern=pattern)
 
 
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+@pytest.mark.parametrize("Bn,M,N,K,at,bt,out,pattern", [
+    (1, 256, 256, 128, "e4m3", "e4m3", torch.float32, "random"),
+    (2, 300, 384, 512, "e4m3", "e4m3", torch.float32, "random"),
+    (1, 64, 256, 96, "e4m3", "e4m3", torch.float32, "random"),
+    (3, 130, 136, 256, "e5m2", "e4m3", torch.float32, "random"),
+    (2, 520, 264, 384, "e4m3", "e5m2", torch.bfloat16, "random"),
+    (1, 1, 512, 256, "e4m3", "e4m3", torch.bfloat16, "random"),
+    (1, 512, 512, 1024, "e4m3", "e4m3", torch.float32, "one_hot_a"),
+    (1, 512, 512, 1024, "e4m3", "e4m3", torch.float32, "one_hot_b"),
+])
+def test_mxfp8_each_kernel(monkeypatch, kernel, Bn, M, N, K, at, bt, out, pattern):
+    """The CTA-pair (256 x 256 tiles) and one-CTA (128 x 128) kernels, each
+    forced, on ragged M/N/K, batches, both FP8 formats, bf16 output and
+    one-hot scale layouts (a misplaced scale byte selects the wrong block)."""
+    monkeypatch.setenv("BSMM_MX_KERNEL", kernel)
+    run_mx(Bn, M, N, K, at, bt, out, seed=7 * M + N + K, pattern=pattern)
+
+
 def nv_inputs(Bn, M, N, K, seed, pattern="random"):
     g = torch.Generator().manual_seed(seed)
     a = torch.randint(0, 256, (Bn, M, K // 2), generator=g, dtype=torch.int32).numpy().astype(np.uint8)
@@ -209,6 +228,15 @@ def test_nvfp4_parity(Bn, M, N, K, pattern):
     y_ref = G.scaled_matmul(da, db, dsa, dsb)
     bound = G.scaled_matmul_bound(da, db, dsa, dsb)
     assert_within(y.cpu().numpy(), y_ref, bound, f"nvfp4 {Bn}x{M}x{N}x{K} {pattern}")
+
+
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+@pytest.mark.parametrize("Bn,M,N,K,pattern", [(1, 256, 256, 256, "random"), (2, 200, 136, 512, "random"),
+                                              (1, 64, 128, 64, "random"), (3, 300, 520, 768, "random"),
+                                              (1, 512, 384, 1024, "one_hot_a")])
+def test_nvfp4_each_kernel(monkeypatch, kernel, Bn, M, N, K, pattern):
+    monkeypatch.setenv("BSMM_MX_KERNEL", kernel)
+    test_nvfp4_parity(Bn, M, N, K, pattern)
 
 
 def test_jax_basic_case_padded_to_a_hardware_block():
