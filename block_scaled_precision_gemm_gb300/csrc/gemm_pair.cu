@@ -333,18 +333,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int row = row0 + lane;
       const int col0 = nb * PN + g * COLS;
       const bool col_ok = col0 < p.N;
-      float acc[COLS];
+      // column pairs: the promotion runs as packed two-lane FP32 FMAs, each
+      // lane an ordinary round-to-nearest fused multiply-add
+      float2 acc[COLS / 2];
       bool ok = true;
       if constexpr (MODE == kPairF32) {
         const bool row_ok = row < p.M;  // N % 128 == 0: a quarter is all in or all out
         const float* sa_row = p.a_scales + static_cast<size_t>(row_ok ? row : 0) * p.kb;
         const float* sb_row = p.b_scales + static_cast<size_t>(col_ok ? col0 / 128 : 0) * p.kb;
 #pragma unroll
-        for (int i = 0; i < COLS; ++i) acc[i] = 0.f;
+        for (int i = 0; i < COLS / 2; ++i) acc[i] = make_float2(0.f, 0.f);
         float sa_next = row_ok ? __ldg(sa_row) : 0.f;
         float sb_next = col_ok ? __ldg(sb_row) : 0.f;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           const float s = sa_next * sb_next;
+          const float2 s2 = make_float2(s, s);
           if (kt + 1 < p.k_tiles) {
             sa_next = row_ok ? __ldg(sa_row + kt + 1) : 0.f;
             sb_next = col_ok ? __ldg(sb_row + kt + 1) : 0.f;
@@ -362,9 +365,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld16(taddr + 32 * h + 16, r1);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[32 * h + j] = fmaf(__uint_as_float(r0[j]), s, acc[32 * h + j]);
+            for (int j = 0; j < 8; ++j)
+              acc[16 * h + j] = __ffma2_rn(make_float2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1])), s2,
+                                           acc[16 * h + j]);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[32 * h + 16 + j] = fmaf(__uint_as_float(r1[j]), s, acc[32 * h + 16 + j]);
+            for (int j = 0; j < 8; ++j)
+              acc[16 * h + 8 + j] = __ffma2_rn(
+                  make_float2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1])), s2, acc[16 * h + 8 + j]);
           }
           tc_fence_before();
           __syncwarp();
@@ -387,9 +394,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld16(taddr + 32 * h + 16, r1);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              acc[32 * h + j] = __uint_as_float(r0[j]);
-              acc[32 * h + 16 + j] = __uint_as_float(r1[j]);
+            for (int j = 0; j < 8; ++j) {
+              acc[16 * h + j] = make_float2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+              acc[16 * h + 8 + j] = make_float2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
             }
           }
           tc_fence_before();
@@ -408,10 +415,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float* v = &acc[32 * c + 4 * j];
+            const float2 v0 = acc[16 * c + 2 * j], v1 = acc[16 * c + 2 * j + 1];
             const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
-            *reinterpret_cast<uint4*>(my_stg + off) = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
-                                                                 __float_as_uint(v[2]), __float_as_uint(v[3]));
+            *reinterpret_cast<uint4*>(my_stg + off) =
+                make_uint4(__float_as_uint(v0.x), __float_as_uint(v0.y), __float_as_uint(v1.x), __float_as_uint(v1.y));
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -426,11 +433,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float* v = &acc[8 * j];
+          const float2* v = &acc[4 * j];
           const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
           *reinterpret_cast<uint4*>(my_stg + off) =
-              make_uint4(pack_bf16x2_pair(v[0], v[1]), pack_bf16x2_pair(v[2], v[3]), pack_bf16x2_pair(v[4], v[5]),
-                         pack_bf16x2_pair(v[6], v[7]));
+              make_uint4(pack_bf16x2_pair(v[0].x, v[0].y), pack_bf16x2_pair(v[1].x, v[1].y),
+                         pack_bf16x2_pair(v[2].x, v[2].y), pack_bf16x2_pair(v[3].x, v[3].y));
         }
         fence_proxy_async_smem();
         __syncwarp();

@@ -333,10 +333,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(taddr, r0);
           tmem_ld32(taddr + 32, r1);
           tmem_wait_ld();
+          // packed two-lane FP32 FMAs (each lane an ordinary fmaf): half the
+          // instructions of the promotion, which bounds this loop
+          const float2 s2 = make_float2(s, s);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(r0[j]), s, acc[j]);
+          for (int j = 0; j < 16; ++j) {
+            const float2 v = __ffma2_rn(make_float2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1])), s2,
+                                        make_float2(acc[2 * j], acc[2 * j + 1]));
+            acc[2 * j] = v.x;
+            acc[2 * j + 1] = v.y;
+          }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[32 + j] = fmaf(__uint_as_float(r1[j]), s, acc[32 + j]);
+          for (int j = 0; j < 16; ++j) {
+            const float2 v = __ffma2_rn(make_float2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1])), s2,
+                                        make_float2(acc[32 + 2 * j], acc[32 + 2 * j + 1]));
+            acc[32 + 2 * j] = v.x;
+            acc[32 + 2 * j + 1] = v.y;
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[tb]);
