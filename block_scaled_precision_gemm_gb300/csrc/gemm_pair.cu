@@ -34,8 +34,13 @@
 //
 // Epilogue: 16 warps per CTA (four per TMEM lane quarter).  Warp w reads lanes
 // 32*(w%4).. (its 32 rows) and one 64-column quarter of the tile.  In kPairF32
-// reading every K block's partial out of tensor memory is the other bound of
-// this kernel: one warp moves ~28 B/clk from TMEM, hence sixteen reading warps.
+// the per-K-block promotion (packed FP32 FMAs) is this kernel's bound, so the
+// epilogue warps do nothing else: at a tile's end each writes its 32 x 64
+// result into its own 8 KB of shared memory and moves on to the next tile,
+// while the two otherwise idle control warps copy the staged results out with
+// coalesced global stores (through the TMA unit those stores delayed the
+// operand loads) and warm L2 with the next tile's A-scale rows.  The block-
+// scaled modes drain the accumulator once per tile and store through TMA.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -58,12 +63,14 @@ constexpr int EPI_COLS = 64;               // columns per epilogue thread
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
 constexpr int A_BYTES = HALF * KB, B_BYTES = HALF * KB;
-constexpr int STG_PER_WARP = 4096;         // one 32-row x 128-byte staging buffer
 
 template <int MODE>
 struct PCfg {
   static constexpr int ATOMS = MODE == kPairMXF8 ? 1 : (MODE == kPairNVF4 ? 4 : 0);  // per K block per 128 rows
-  static constexpr int STAGES = MODE == kPairF32 ? 5 : 4;
+  static constexpr int STAGES = MODE == kPairF32 ? 3 : 4;
+  // output staging per epilogue warp: 32 rows x 128 bytes per 32-column chunk
+  // (kPairF32 stages both chunks of a tile; the TMA-store path reuses one)
+  static constexpr int STG_PER_WARP = MODE == kPairF32 ? 8192 : 4096;
   static constexpr int SFA_BYTES = ATOMS * 512;      // this CTA's 128 A rows
   static constexpr int SFB_BYTES = 2 * ATOMS * 512;  // all 256 B rows
   static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
@@ -78,14 +85,14 @@ struct PCfg {
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_STG = (OFF_SF + STAGES * SF_BYTES + 1023) / 1024 * 1024;
   static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_PER_WARP;
-  static constexpr int N_BARS = 2 * STAGES + 2 * NACC + 1;
+  static constexpr int N_BARS = 2 * STAGES + 2 * NACC + 3;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
 };
 
 enum Site { kSiteProducer = 11, kSiteMmaTmem = 12, kSiteMmaFull = 13, kSiteEpilogue = 14, kSiteDrain = 15,
-            kSiteDone = 16 };
+            kSiteDone = 16, kSiteStore = 17, kSiteStaging = 18 };
 
 struct PairParams {
   int M, N, K;
@@ -100,6 +107,7 @@ struct PairParams {
   // through 2-D tensor maps of 128-byte rows (an atom is 4 rows)
   int sfa_rt, sfb_rt, ks4;
   int y_bf16;
+  float* y;  // kPairF32 output [M][N], written by the copy warps
   uint32_t idesc;
   int* status;
   uint64_t timeout_ns;
@@ -141,7 +149,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + NACC;
   uint64_t* done = tempty + NACC;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* stg_full = done + 1;   // kPairF32: the 16 epilogue warps staged a tile
+  uint64_t* stg_empty = done + 2;  // kPairF32: both copy warps emptied the staging
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int never_abort_storage = 0;
   volatile int* never_abort = &never_abort_storage;
@@ -161,6 +171,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&tempty[i], 2 * EPI_WARPS);
     }
     mbar_init(done, 1);
+    mbar_init(stg_full, EPI_WARPS);
+    mbar_init(stg_empty, 2);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -314,6 +326,53 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_commit_pair_mc(done, 0x1);
       mbar_wait(done, 0, p.timeout_ns, never_abort, p.status, kSiteDone);
+    } else if (MODE == kPairF32 && warp >= 2) {
+      // ------------------------------------------------ output copy (both CTAs)
+      // Warp 2 copies the staging of epilogue warps 0-7, warp 3 that of 8-15:
+      // per 32-column chunk, each instruction moves four rows of 128 bytes
+      // (lane l: row 4j + l/8, 16-byte unit l%8), so every global store
+      // writes four whole 128-byte lines.
+      const int cw = warp - 2;
+      uint32_t sph = 0;
+      for (int t = cid; t < p.num_tiles; t += ncl) {
+        int b, mb, nb;
+        decode_pair_tile(p, t, b, mb, nb);
+        if (t + ncl < p.num_tiles) {  // the A-scale rows of this CTA's next tile, 64 per warp
+          int b2, mb2, nb2;
+          decode_pair_tile(p, t + ncl, b2, mb2, nb2);
+          for (int i = lane; i < 64; i += 32) {
+            const int r = mb2 * PM + static_cast<int>(rank) * HALF + cw * 64 + i;
+            if (r < p.M) {
+              const char* pa = reinterpret_cast<const char*>(p.a_scales + static_cast<size_t>(r) * p.kb);
+              for (int off = 0; off < p.kb * 4; off += 128) prefetch_l2(pa + off);
+            }
+          }
+        }
+        if (!mbar_wait(stg_full, sph, p.timeout_ns, abort_flag, p.status, kSiteStore)) break;
+        for (int i = 0; i < EPI_WARPS / 2; ++i) {
+          const int ew = cw * (EPI_WARPS / 2) + i;
+          const int row0 = mb * PM + static_cast<int>(rank) * HALF + (ew & 3) * 32;
+          const int col0 = nb * PN + (ew >> 2) * EPI_COLS;
+          if (row0 >= p.M || col0 >= p.N) continue;
+          const uint8_t* src = stg + ew * C::STG_PER_WARP;
+          const int u = lane & 7;
+#pragma unroll 1
+          for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + (lane >> 3);
+            const uint32_t soff = r * 128 + ((u ^ (r & 7)) * 16);
+            const uint4 v0 = *reinterpret_cast<const uint4*>(src + soff);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(src + 4096 + soff);
+            if (row0 + r < p.M) {
+              float* dst = p.y + (static_cast<size_t>(b) * p.M + row0 + r) * p.N + col0 + 4 * u;
+              *reinterpret_cast<uint4*>(dst) = v0;
+              *reinterpret_cast<uint4*>(dst + 32) = v1;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(stg_empty);
+        sph ^= 1u;
+      }
     }
   } else {
     setmaxnreg_inc<104>();
@@ -322,7 +381,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int ew = warp - 4;
     const int q = warp & 3;   // TMEM lane quarter = the warp's 32 rows
     const int g = ew >> 2;    // 64-column quarter of the tile
-    uint8_t* my_stg = stg + ew * STG_PER_WARP;
+    uint8_t* my_stg = stg + ew * C::STG_PER_WARP;
+    uint32_t sph = 0;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int tb = 0;
     uint32_t tph = 0;
@@ -406,6 +466,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (!ok) break;
+      if constexpr (MODE == kPairF32) {
+        // the previous tile's staging has been copied out (a tile ago)
+        if (!mbar_wait(stg_empty, sph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteStaging)) break;
+        if (row0 < p.M && col_ok) {
+#pragma unroll
+          for (int c = 0; c < COLS / 32; ++c)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float2 v0 = acc[16 * c + 2 * j], v1 = acc[16 * c + 2 * j + 1];
+              const uint32_t off = c * 4096 + lane * 128 + ((j ^ (lane & 7)) * 16);
+              *reinterpret_cast<uint4*>(my_stg + off) = make_uint4(__float_as_uint(v0.x), __float_as_uint(v0.y),
+                                                                   __float_as_uint(v1.x), __float_as_uint(v1.y));
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(stg_full);
+        sph ^= 1u;
+        continue;
+      }
       if (row0 >= p.M || !col_ok) continue;  // this warp's box lies outside y
       if (!p.y_bf16) {
         // 64 FP32 columns of 32 rows leave as two 32 x 32 TMA stores
@@ -541,6 +620,7 @@ cudaError_t launch_grouped_gemm_pair(const GroupedGemmRequest& r, cudaStream_t s
   p.a_scales = r.a_scales;
   p.b_scales = r.b_scales;
   p.kb = static_cast<int>(r.K / 128);
+  p.y = r.y;
   p.status = ctx->status;
   p.timeout_ns = wait_timeout_ns();
   // kind::f8f6f4: D = F32, A/B E4M3 = 0 / E5M2 = 1, K-major, N = 256, M = 256 (pair).
