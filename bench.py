@@ -245,7 +245,7 @@ class GroupedWork(Work):
 class Int8Work(Work):
     """TensorTonic INT8 per-channel matmul at B = D_in = D_out = 4096: a step
     quantizes x per row and w per column and runs the exact int32 matmul."""
-    dominant = "INT8 per-channel call (quantizers + mma.sync s8 GEMM)"
+    dominant = "INT8 per-channel call (quantizers + tc_gemm_pair kPairI8: exact int sums on bf16 tensor cores)"
     peak_kind = "int8"
     dtype = "int8 (int32 accumulate)"
 
@@ -373,12 +373,13 @@ def make_work(workload: W.Workload, device) -> Work:
 def peak_tflops(peaks, kind):
     """Dense peak for the path's own dtype: measured bf16 (sustained) times the
     nominal ratio (FP8 2x, FP4 4x).  INT8 has no measured or usable nominal
-    figure on this part; the bf16 rate is reported as its reference."""
+    figure on this part: its exact matmul runs on the bf16 tensor cores, so the
+    bf16 rate is its peak."""
     base = peaks["bf16_tflops_sustained"]
     return {"fp8": 2.0 * base, "fp4": 4.0 * base, "int8": base}[kind], {
         "fp8": "2 x bf16_tflops_sustained (FP8/BF16 nominal ratio 2)",
         "fp4": "4 x bf16_tflops_sustained (FP4/BF16 nominal ratio 4)",
-        "int8": "bf16_tflops_sustained (no INT8 tcgen05 kind on sm_103a; legacy mma.sync path)"}[kind]
+        "int8": "bf16_tflops_sustained (the INT8 matmul runs exactly on the bf16 tensor cores)"}[kind]
 
 
 def run_gpu(args):

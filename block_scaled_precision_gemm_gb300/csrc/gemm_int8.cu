@@ -3,24 +3,35 @@
 // line -> 1), codes clip(round(v/s), +-127), a = sum_i x_q*w_q exact in int32,
 // y = float(a) * s_x[b] * s_w[j].
 //
-// tcgen05 has no integer MMA kind on sm_103a, so the matmul runs on the
-// warp-level integer MMA (mma.sync m16n8k32 s8.s8.s32), which accumulates
-// exactly in int32.  Kernels:
+// tcgen05 has no integer MMA kind on sm_103a, and GB300's integer tensor
+// rate is far below its 16-bit one.  Codes in [-127, 127] are exact in bf16
+// and their products exact in FP32, so the matmul runs on the bf16 tensor
+// cores (tc_gemm_pair kPairI8 in gemm_pair.cu): FP32 sums over chunks of
+// 1024 products stay below 2^24 in magnitude, hence exact integers, and are
+// added in int32.  Kernels here:
 //   i8_quant_rows   one CTA per row of x: absmax, scale, codes into x_q and a
-//                   zero-padded copy [B, Kp] the matmul reads.
+//                   zero-padded K-major copy [B, Kp] the matmul reads (bf16,
+//                   or int8 for the fallback below).
 //   i8_colmax       column maxima of w, split over row chunks, combined with
 //                   an integer atomicMax on the (non-negative) float bits.
 //   i8_quant_cols   codes of w in the page's layout [D_in, D_out] and
 //                   transposed [D_out, Kp] through a shared-memory tile.
-//   i8_gemm         128x128 CTA tile, 8 warps of 64x32, 128-byte K steps,
+//   i8_gemm         fallback for outputs TMA cannot store (D_out % 4 != 0 or
+//                   unaligned y): the warp-level integer MMA (mma.sync
+//                   m16n8k32 s8.s8.s32, exact int32), 128x128 CTA tile,
 //                   4-stage cp.async pipeline, XOR-swizzled shared memory.
+#include <cuda_bf16.h>
+
+#include <cstdlib>
+#include <cstring>
+
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace bsmm {
 namespace {
 
-constexpr int kKpAlign = 128;  // padded K (bytes per operand row)
+constexpr int kKpAlign = 128;  // padded K, elements per operand row (int8: 128-byte rows; bf16: 4 K blocks)
 
 __device__ __forceinline__ float i8_scale(float absmax) {
   return absmax == 0.f ? 1.f : __fdiv_rn(absmax, 127.f);
@@ -29,10 +40,22 @@ __device__ __forceinline__ int8_t i8_code(float v, float s) {
   const float q = fminf(fmaxf(__fdiv_rn(v, s), -127.f), 127.f);
   return static_cast<int8_t>(__float2int_rn(q));
 }
+template <typename Pad>
+__device__ __forceinline__ Pad pad_code(int8_t q);
+template <>
+__device__ __forceinline__ int8_t pad_code<int8_t>(int8_t q) {
+  return q;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 pad_code<__nv_bfloat16>(int8_t q) {
+  return __int2bfloat16_rn(q);  // exact: |q| <= 127 < 2^8
+}
 
+// Pad is int8_t (fallback matmul) or __nv_bfloat16 (tensor-core matmul).
+template <typename Pad>
 __global__ void __launch_bounds__(256) i8_quant_rows(const float* __restrict__ x, int64_t D, int64_t Kp,
                                                      int8_t* __restrict__ xq, float* __restrict__ xs,
-                                                     int8_t* __restrict__ xq_pad) {
+                                                     Pad* __restrict__ xq_pad) {
   __shared__ float wmax[8];
   const int64_t r = blockIdx.x;
   const float* row = x + r * D;
@@ -49,7 +72,7 @@ __global__ void __launch_bounds__(256) i8_quant_rows(const float* __restrict__ x
   for (int64_t c = threadIdx.x; c < Kp; c += 256) {
     const int8_t q = c < D ? i8_code(__ldg(row + c), s) : int8_t(0);
     if (c < D) xq[r * D + c] = q;
-    xq_pad[r * Kp + c] = q;
+    xq_pad[r * Kp + c] = pad_code<Pad>(q);
   }
 }
 
@@ -75,10 +98,11 @@ __global__ void __launch_bounds__(256) i8_colmax(const float* __restrict__ w, in
 
 // 64 x 64 tiles of w (rows i over Kp, columns j): codes into w_q[i][j] and
 // wqT[j][i]; rows i >= D_in give zero codes in wqT (the K padding).
+template <typename Pad>
 __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w, int64_t D_in, int64_t D_out,
                                                      int64_t Kp, const unsigned* __restrict__ colmax,
                                                      int8_t* __restrict__ wq, float* __restrict__ ws,
-                                                     int8_t* __restrict__ wqT) {
+                                                     Pad* __restrict__ wqT) {
   __shared__ int8_t tile[64][64 + 4];
   const int64_t i0 = static_cast<int64_t>(blockIdx.y) * 64, j0 = static_cast<int64_t>(blockIdx.x) * 64;
   const int t = threadIdx.x;
@@ -103,15 +127,29 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
   if (jrow < D_out) {
     const int64_t ibase = i0 + part * 16;
     if (ibase < Kp) {
-      uint32_t word[4];
+      if constexpr (sizeof(Pad) == 1) {
+        uint32_t word[4];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        word[g] = 0;
+        for (int g = 0; g < 4; ++g) {
+          word[g] = 0;
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          word[g] |= static_cast<uint32_t>(static_cast<uint8_t>(tile[part * 16 + 4 * g + b][jt])) << (8 * b);
+          for (int b = 0; b < 4; ++b)
+            word[g] |= static_cast<uint32_t>(static_cast<uint8_t>(tile[part * 16 + 4 * g + b][jt])) << (8 * b);
+        }
+        *reinterpret_cast<uint4*>(wqT + jrow * Kp + ibase) = make_uint4(word[0], word[1], word[2], word[3]);
+      } else {
+        uint32_t word[8];  // 16 bf16 codes, two per word
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const __nv_bfloat16 lo = __int2bfloat16_rn(tile[part * 16 + 2 * g][jt]);
+          const __nv_bfloat16 hi = __int2bfloat16_rn(tile[part * 16 + 2 * g + 1][jt]);
+          word[g] = static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(wqT + jrow * Kp + ibase);
+        dst[0] = make_uint4(word[0], word[1], word[2], word[3]);
+        dst[1] = make_uint4(word[4], word[5], word[6], word[7]);
       }
-      *reinterpret_cast<uint4*>(wqT + jrow * Kp + ibase) = make_uint4(word[0], word[1], word[2], word[3]);
     }
   }
 }
@@ -253,23 +291,34 @@ __global__ void __launch_bounds__(256) i8_gemm(const int8_t* __restrict__ A, con
 }  // namespace
 
 size_t int8_workspace_bytes(int64_t B, int64_t D_in, int64_t D_out) {
+  // room for the bf16 operand copies (the fallback's int8 copies fit inside)
   const int64_t Kp = ceil_div(D_in, kKpAlign) * kKpAlign;
-  return align_up(static_cast<size_t>(D_out) * 4, 256) + align_up(static_cast<size_t>(B) * Kp, 256) +
-         align_up(static_cast<size_t>(D_out) * Kp, 256);
+  return align_up(static_cast<size_t>(D_out) * 4, 256) + align_up(static_cast<size_t>(B) * Kp * 2, 256) +
+         align_up(static_cast<size_t>(D_out) * Kp * 2, 256);
 }
 
 cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   const DeviceCtx* ctx = device_ctx();
   if (!ctx) return cudaErrorInitializationError;
-  const int64_t Kp = ceil_div(r.D_in, kKpAlign) * kKpAlign;
+  const int64_t Kp = ceil_div(r.D_in, kKpAlign) * kKpAlign;  // elements
   uint8_t* ws = reinterpret_cast<uint8_t*>(r.workspace);
   unsigned* colmax = reinterpret_cast<unsigned*>(ws);
-  int8_t* xq_pad = reinterpret_cast<int8_t*>(ws + align_up(static_cast<size_t>(r.D_out) * 4, 256));
-  int8_t* wqT = xq_pad + align_up(static_cast<size_t>(r.B) * Kp, 256);
+  uint8_t* xpad = ws + align_up(static_cast<size_t>(r.D_out) * 4, 256);
+  uint8_t* wpadT = xpad + align_up(static_cast<size_t>(r.B) * Kp * 2, 256);
+  // The tensor-core path stores y (and the int32 sums) through TMA: 16-byte
+  // rows and bases.  BSMM_INT8_KERNEL=mma forces the fallback.
+  const char* force = std::getenv("BSMM_INT8_KERNEL");
+  const bool tc = !(force && std::strcmp(force, "mma") == 0) && (r.D_out * 4) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(r.y) % 16 == 0 && reinterpret_cast<uintptr_t>(r.acc) % 16 == 0;
 
   cudaError_t e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(r.D_out) * 4, s);
   if (e != cudaSuccess) return e;
-  i8_quant_rows<<<static_cast<unsigned>(r.B), 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xq_pad);
+  if (tc)
+    i8_quant_rows<__nv_bfloat16><<<static_cast<unsigned>(r.B), 256, 0, s>>>(
+        r.x, r.D_in, Kp, r.x_q, r.x_scales, reinterpret_cast<__nv_bfloat16*>(xpad));
+  else
+    i8_quant_rows<int8_t><<<static_cast<unsigned>(r.B), 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales,
+                                                                     reinterpret_cast<int8_t*>(xpad));
   {
     const int rows_per_cta = 256;
     dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 32)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
@@ -277,16 +326,28 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   }
   {
     dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 64)), static_cast<unsigned>(Kp / 64));
-    i8_quant_cols<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales, wqT);
+    if (tc)
+      i8_quant_cols<__nv_bfloat16><<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales,
+                                                        reinterpret_cast<__nv_bfloat16*>(wpadT));
+    else
+      i8_quant_cols<int8_t><<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales,
+                                                 reinterpret_cast<int8_t*>(wpadT));
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (tc) {
+    std::string why;
+    e = launch_int8_gemm_pair(r, xpad, wpadT, Kp, s, &why);
+    if (e != cudaSuccess && !why.empty()) set_error(why);
+    return e;
+  }
   const int smem = GSTAGES * G_STAGE_BYTES;
   e = cudaFuncSetAttribute(i8_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, GN)), static_cast<unsigned>(ceil_div(r.B, GM)));
-  i8_gemm<<<grid, 256, smem, s>>>(xq_pad, wqT, static_cast<int>(r.B), static_cast<int>(r.D_out),
-                                  static_cast<int>(Kp), r.x_scales, r.w_scales, r.y, r.acc);
+  i8_gemm<<<grid, 256, smem, s>>>(reinterpret_cast<const int8_t*>(xpad), reinterpret_cast<const int8_t*>(wpadT),
+                                  static_cast<int>(r.B), static_cast<int>(r.D_out), static_cast<int>(Kp), r.x_scales,
+                                  r.w_scales, r.y, r.acc);
   return cudaGetLastError();
 }
 

@@ -52,7 +52,7 @@
 namespace bsmm {
 namespace {
 
-enum PairMode { kPairF32 = 0, kPairMXF8 = 1, kPairNVF4 = 2 };
+enum PairMode { kPairF32 = 0, kPairMXF8 = 1, kPairNVF4 = 2, kPairI8 = 3 };
 
 constexpr int PM = 256, PN = 256;          // pair tile
 constexpr int HALF = 128;                  // A rows and B rows per CTA
@@ -75,7 +75,7 @@ struct PCfg {
   static constexpr int SFB_BYTES = 2 * ATOMS * 512;  // all 256 B rows
   static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + SF_BYTES;  // per CTA
-  static constexpr int NACC = MODE == kPairF32 ? 2 : 1;
+  static constexpr int NACC = (MODE == kPairF32 || MODE == kPairI8) ? 2 : 1;
   static constexpr int SF_COL0 = NACC * PN;
   static constexpr int SFA_COLS = ATOMS * 4;
   static constexpr int SFB_COLS = 2 * ATOMS * 4;
@@ -108,6 +108,12 @@ struct PairParams {
   int sfa_rt, sfb_rt, ks4;
   int y_bf16;
   float* y;  // kPairF32 output [M][N], written by the copy warps
+  // kPairI8: per-row and per-column scales, K blocks per exact FP32 chunk,
+  // whether the int32 sums are stored (through tmSFA)
+  const float* sx;
+  const float* sw;
+  int chunk;
+  int store_acc;
   uint32_t idesc;
   int* status;
   uint64_t timeout_ns;
@@ -128,6 +134,36 @@ __device__ __forceinline__ void decode_pair_tile(const PairParams& p, int t, int
 __device__ __forceinline__ uint32_t pack_bf16x2_pair(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Two int32 sums kept in the bits of a float2, plus two exact FP32 integers.
+__device__ __forceinline__ float2 iadd_f2(float2 acc, uint32_t p0, uint32_t p1) {
+  return make_float2(__int_as_float(__float_as_int(acc.x) + __float2int_rn(__uint_as_float(p0))),
+                     __int_as_float(__float_as_int(acc.y) + __float2int_rn(__uint_as_float(p1))));
+}
+
+// A warp's 32 rows x 64 columns of 32-bit values leave through `map` as two
+// 32 x 32 TMA stores from the warp's 4 KB staging buffer (128B-swizzled rows).
+__device__ __forceinline__ void store_box_f32(const CUtensorMap* map, uint8_t* stg, const float2 (&acc)[EPI_COLS / 2],
+                                              int col0, int row0, int z, int lane) {
+#pragma unroll
+  for (int c = 0; c < EPI_COLS / 32; ++c) {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 v0 = acc[16 * c + 2 * j], v1 = acc[16 * c + 2 * j + 1];
+      const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
+      *reinterpret_cast<uint4*>(stg + off) =
+          make_uint4(__float_as_uint(v0.x), __float_as_uint(v0.y), __float_as_uint(v1.x), __float_as_uint(v1.y));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(map, stg, col0 + 32 * c, row0, z);
+      bulk_commit();
+    }
+  }
 }
 
 template <int MODE>
@@ -209,7 +245,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_TX);
           tma_load_3d_pair(sA + stage * A_BYTES, &tmA, full_leader, kt * KB, mb * PM + rank * HALF, b);
           tma_load_3d_pair(sB + stage * B_BYTES, &tmB, full_leader, kt * KB, nb * PN + rank * HALF, b);
-          if constexpr (MODE != kPairF32) {
+          if constexpr (C::ATOMS > 0) {  // block-scaled modes: this stage's scale-factor atoms
             // atoms as rows of 128 bytes: atom j of row tile rt of batch b
             // starts at row 4 * ((b * rt_count + rt) * ks4 + j)
             uint8_t* sf = sSF + stage * C::SF_BYTES;
@@ -253,13 +289,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0, tb = 0;
       uint32_t phase = 0, tph = 0;
       bool ok = true;
+      // K blocks accumulated per TMEM buffer: one (kPairF32), a chunk
+      // (kPairI8) or all of K (block-scaled)
+      const int per_buf = MODE == kPairF32 ? 1 : (MODE == kPairI8 ? p.chunk : p.k_tiles);
       for (int t = cid; ok && t < p.num_tiles; t += ncl) {
-        if constexpr (MODE != kPairF32) {
-          if (!mbar_wait(&tempty[0], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) break;
-          tc_fence_after();
-        }
+        int kc = 0;  // K blocks already in the current buffer
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if constexpr (MODE == kPairF32) {
+          if (kc == 0) {
             if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
               ok = false;
               break;
@@ -280,11 +316,13 @@ __global__ void __launch_bounds__(THREADS, 1)
               mma_f8f6f4_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
                               p.idesc, k > 0 ? 1u : 0u);
             tc_commit_pair_mc(&empty[stage], 0x3);
-            tc_commit_pair_mc(&tfull[tb], 0x3);
-            if (++tb == NACC) {
-              tb = 0;
-              tph ^= 1u;
-            }
+          } else if constexpr (MODE == kPairI8) {
+            // bf16 codes: a 128-byte K block is 64 elements, four K = 16 MMAs
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f16_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
+                           p.idesc, (kc > 0 || k > 0) ? 1u : 0u);
+            tc_commit_pair_mc(&empty[stage], 0x3);
           } else {
             const uint32_t sfa_t = tmem + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
@@ -317,11 +355,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             stage = 0;
             phase ^= 1u;
           }
-        }
-        if constexpr (MODE != kPairF32) {
-          if (!ok) break;
-          tc_commit_pair_mc(&tfull[0], 0x3);
-          tph ^= 1u;
+          if (++kc == per_buf || kt + 1 == p.k_tiles) {  // the buffer is complete
+            tc_commit_pair_mc(&tfull[tb], 0x3);
+            kc = 0;
+            if (++tb == NACC) {
+              tb = 0;
+              tph ^= 1u;
+            }
+          }
         }
       }
       tc_commit_pair_mc(done, 0x1);
@@ -441,6 +482,38 @@ __global__ void __launch_bounds__(THREADS, 1)
             tph ^= 1u;
           }
         }
+      } else if constexpr (MODE == kPairI8) {
+        // int32 sums in the bits of acc: each chunk's FP32 partial is an
+        // exact integer below 2^24, converted exactly and added
+#pragma unroll
+        for (int i = 0; i < COLS / 2; ++i) acc[i] = make_float2(0.f, 0.f);  // int 0 has the same bits
+        for (int kt = 0; kt < p.k_tiles; kt += p.chunk) {
+          if (!mbar_wait(&tfull[tb], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(tb * PN + g * COLS);
+#pragma unroll
+          for (int h = 0; h < COLS / 32; ++h) {
+            uint32_t r0[16], r1[16];
+            tmem_ld16(taddr + 32 * h, r0);
+            tmem_ld16(taddr + 32 * h + 16, r1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              acc[16 * h + j] = iadd_f2(acc[16 * h + j], r0[2 * j], r0[2 * j + 1]);
+              acc[16 * h + 8 + j] = iadd_f2(acc[16 * h + 8 + j], r1[2 * j], r1[2 * j + 1]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[tb]), 0));
+          if (++tb == NACC) {
+            tb = 0;
+            tph ^= 1u;
+          }
+        }
       } else {
         if (!mbar_wait(&tfull[0], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
           ok = false;
@@ -486,6 +559,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         continue;
       }
       if (row0 >= p.M || !col_ok) continue;  // this warp's box lies outside y
+      if constexpr (MODE == kPairI8) {
+        if (p.store_acc) store_box_f32(&tmSFA, my_stg, acc, col0, row0, b, lane);  // int32 bits as they are
+        // y = (float(acc) * s_x[row]) * s_w[col], in that order
+        const float sxr = row < p.M ? __ldg(p.sx + row) : 0.f;
+#pragma unroll
+        for (int i = 0; i < COLS / 2; ++i) {
+          const int c = col0 + 2 * i;
+          const float w0 = c < p.N ? __ldg(p.sw + c) : 0.f;
+          const float w1 = c + 1 < p.N ? __ldg(p.sw + c + 1) : 0.f;
+          acc[i] = make_float2((static_cast<float>(__float_as_int(acc[i].x)) * sxr) * w0,
+                               (static_cast<float>(__float_as_int(acc[i].y)) * sxr) * w1);
+        }
+        store_box_f32(&tmY, my_stg, acc, col0, row0, b, lane);
+        continue;
+      }
       if (!p.y_bf16) {
         // 64 FP32 columns of 32 rows leave as two 32 x 32 TMA stores
 #pragma unroll
@@ -541,7 +629,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-int g_pair_clusters[3][64] = {};  // max co-resident clusters per mode and device
+int g_pair_clusters[4][64] = {};  // max co-resident clusters per mode and device
 
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const CUtensorMap& tsa,
@@ -681,6 +769,44 @@ cudaError_t launch_mx_gemm_pair(const MxGemmRequest& r, const MxAtoms& at, cudaS
   p.idesc = (f8_code(r.a_fmt) << 7) | (f8_code(r.b_fmt) << 10) | (static_cast<uint32_t>(PN >> 3) << 17) | (1u << 23) |
             (static_cast<uint32_t>(PM >> 4) << 24);
   return launch_pair<kPairMXF8>(ta, tb, ty, tsa, tsb, p, ctx, s, why);
+}
+
+cudaError_t launch_int8_gemm_pair(const Int8Request& r, const void* xb, const void* wbT, int64_t Kp, cudaStream_t s,
+                                  std::string* why) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  // The bf16 operands are moved as bytes: a 128-byte K block is 64 codes.
+  CUtensorMap ta, tb, ty, tacc;
+  bool ok = make_tmap_3d(&ta, xb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Kp * 2, r.B, 1, KB, HALF, true) &&
+            make_tmap_3d(&tb, wbT, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Kp * 2, r.D_out, 1, KB, HALF, true) &&
+            make_tmap_3d(&ty, r.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, r.D_out, r.B, 1, 32, 32, true);
+  if (ok && r.acc) ok = make_tmap_3d(&tacc, r.acc, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, r.D_out, r.B, 1, 32, 32, true);
+  if (!ok) {
+    *why = "cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  if (!r.acc) tacc = ty;  // not read: store_acc = 0
+  PairParams p{};
+  p.M = static_cast<int>(r.B);
+  p.N = static_cast<int>(r.D_out);
+  p.K = static_cast<int>(r.D_in);
+  p.batches = 1;
+  p.m_tiles = static_cast<int>(ceil_div(r.B, PM));
+  p.n_tiles = static_cast<int>(ceil_div(r.D_out, PN));
+  p.k_tiles = static_cast<int>(Kp / 64);
+  p.num_tiles = p.m_tiles * p.n_tiles;
+  p.sx = r.x_scales;
+  p.sw = r.w_scales;
+  // |code product| <= 127^2, so 16 K blocks (1024 products) sum to at most
+  // 16,516,096 < 2^24 in magnitude: every FP32 partial is an exact integer.
+  p.chunk = 16;
+  p.store_acc = r.acc ? 1 : 0;
+  p.status = ctx->status;
+  p.timeout_ns = wait_timeout_ns();
+  // kind::f16: D = F32 (bits 4-5 = 1), A = B = BF16 (bits 7-9, 10-12 = 1), K-major, N = 256, M = 256 (pair).
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(PN >> 3) << 17) |
+            (static_cast<uint32_t>(PM >> 4) << 24);
+  return launch_pair<kPairI8>(ta, tb, ty, tacc, ta, p, ctx, s, why);
 }
 
 }  // namespace bsmm

@@ -108,6 +108,11 @@ struct Int8Request {
 };
 size_t int8_workspace_bytes(int64_t B, int64_t D_in, int64_t D_out);
 cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s);
+// The exact INT8 matmul on bf16 tensor cores (gemm_pair.cu): xb [B, Kp] and
+// wbT [D_out, Kp] are bf16 codes, K-major, zero beyond D_in (Kp % 64 == 0);
+// writes r.y and, if non-null, r.acc.
+cudaError_t launch_int8_gemm_pair(const Int8Request& r, const void* xb, const void* wbT, int64_t Kp, cudaStream_t s,
+                                  std::string* why);
 
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t s);
 

@@ -252,9 +252,15 @@ bsmm_status bsmm_gemm_grouped(int64_t M, int64_t N, int64_t K, const void* a, bs
  *   [D_in, D_out] (the page's layout), w_scales [D_out], y [B, D_out].
  *   acc      optional int32 [B, D_out] output of the exact integer sums
  *            (NULL to skip).
- *   workspace  at least bsmm_int8_channel_workspace_size() bytes (holds the
- *            transposed weight codes the matmul reads).
+ *   workspace  at least bsmm_int8_channel_workspace_size() bytes (holds
+ *            K-padded, K-major copies of both operands' codes for the
+ *            matmul).
  *   D_in must be a multiple of 16.
+ * The integer sums are exact for any codes: the matmul runs on the bf16
+ * tensor cores (codes and their products are exact there) and adds FP32
+ * partials of at most 1024 products, each an exact integer below 2^24, in
+ * int32.  Where y or acc cannot be stored through TMA (D_out % 4 != 0, or a
+ * base not 16-byte aligned) the warp-level integer MMA computes the sums.
  */
 size_t bsmm_int8_channel_workspace_size(int64_t B, int64_t D_in, int64_t D_out);
 

@@ -69,6 +69,36 @@ def test_int8_extreme_sums_stay_exact():
     assert got["acc"][0, 0] == 4096 * 127 * 127 and got["acc"][0, 1] == -4096 * 127 * 127
 
 
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
+@pytest.mark.parametrize("B,D_in,D_out", [(100, 300, 72), (6, 64, 8), (257, 1000, 132), (300, 4133, 264),
+                                          (520, 2048, 516), (1, 128, 4)])
+def test_int8_each_kernel(monkeypatch, kernel, B, D_in, D_out):
+    """The bf16 tensor-core path (exact FP32 chunks of 1024 products added in
+    int32) and the mma.sync fallback, each forced, on ragged B / D_in / D_out
+    with D_out % 4 == 0 (the tensor-core path's TMA stores)."""
+    if kernel == "mma":
+        monkeypatch.setenv("BSMM_INT8_KERNEL", "mma")
+    g = torch.Generator().manual_seed(B * 7 + D_in)
+    x = torch.randn(B, D_in, generator=g).numpy()
+    w = torch.randn(D_in, D_out, generator=g).numpy()
+    x[B // 3] = 0
+    w[:, D_out // 2] = 0
+    run_int8(x, w)
+
+
+@pytest.mark.parametrize("D_in", [4096, 4096 + 1000])
+def test_int8_extreme_sums_tensor_core_path(D_in):
+    """Codes all +-127 on the tensor-core path: every 1024-product chunk sums
+    to +-16,516,096, within 2^24 of zero by 260,120, and the int32 totals
+    reach +-D_in * 16129."""
+    x = np.ones((260, D_in), np.float32)
+    x[1::2] = -1
+    w = np.ones((D_in, 132), np.float32)
+    w[:, 1::2] = -1
+    got = run_int8(x, w)
+    assert got["acc"][0, 0] == D_in * 127 * 127 and got["acc"][1, 0] == -D_in * 127 * 127
+
+
 def _bf16(a):
     return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
 
