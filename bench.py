@@ -225,14 +225,45 @@ class GroupedWork(Work):
         self.h2d = sum(4 * (it["a_raw"].numel() + it["b_raw"].numel()) for it in self.items)
         self.d2h = sum(4 * it["y"].numel() for it in self.items)
 
+    E2E_ROWS = 65536  # activation rows per pipelined chunk
+
     def step_e2e(self):
+        """The same step from pinned host buffers, pipelined over row chunks of
+        each problem on three streams: copy in, compute, copy out.  Each row's
+        quantization and output depend on that row alone, so the chunked
+        calls give exactly the unchunked results."""
+        b = self.bsmm
+        cur = torch.cuda.current_stream()
+        if not hasattr(self, "s_in"):
+            self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        s_in, s_out = self.s_in, self.s_out
+        s_in.wait_stream(cur)   # the previous step has finished reading the inputs
+        cur.wait_stream(s_out)  # ... and copying the outputs out
         for it in self.items:
+            p = it["p"]
             na, nb = it["a_raw"].numel(), it["b_raw"].numel()
-            it["a_raw"].view(-1).copy_(self.hb_in[:na], non_blocking=True)
-            it["b_raw"].view(-1).copy_(self.hb_in[na:na + nb], non_blocking=True)
-        self.step()
-        for it in self.items:
-            self.hb_out[:it["y"].numel()].copy_(it["y"].view(-1), non_blocking=True)
+            with torch.cuda.stream(s_in):
+                it["b_raw"].view(-1).copy_(self.hb_in[na:na + nb], non_blocking=True)
+            for r0 in range(0, p.m, self.E2E_ROWS):
+                r1 = min(p.m, r0 + self.E2E_ROWS)
+                lo, hi = r0 * p.k, r1 * p.k
+                with torch.cuda.stream(s_in):
+                    it["a_raw"].view(-1)[lo:hi].copy_(self.hb_in[lo:hi], non_blocking=True)
+                    ev_in = torch.cuda.Event()
+                    ev_in.record()
+                cur.wait_event(ev_in)
+                if r0 == 0:
+                    b.quantize(it["b_raw"], (p.group_n, p.group_k), "e4m3", "f32", codes=it["bq"], scales=it["sb"])
+                b.quantize(it["a_raw"][r0:r1], (1, p.group_k), "e4m3", "f32", codes=it["aq"][r0:r1],
+                           scales=it["sa"][r0:r1])
+                b.gemm_grouped(it["aq"][r0:r1], it["bq"], it["sa"][r0:r1], it["sb"], p.group_n, p.group_k,
+                               y=it["y"][r0:r1])
+                ev_c = torch.cuda.Event()
+                ev_c.record()
+                s_out.wait_event(ev_c)
+                with torch.cuda.stream(s_out):
+                    self.hb_out[r0 * p.n:r1 * p.n].copy_(it["y"][r0:r1].view(-1), non_blocking=True)
+        cur.wait_stream(s_out)
 
     def config(self):
         return {"problems": [[p.m, p.n, p.k] for p in self.w.problems], "group_n": 128, "group_k": 128,
@@ -372,13 +403,13 @@ def make_work(workload: W.Workload, device) -> Work:
 
 def peak_tflops(peaks, kind):
     """Dense peak for the path's own dtype: measured bf16 (sustained) times the
-    nominal ratio (FP8 2x, FP4 4x).  INT8 has no measured or usable nominal
+    nominal dense ratio on GB300 (FP8 4.5/2.25 = 2x, FP4 13.5/2.25 = 6x).  INT8 has no measured or usable nominal
     figure on this part: its exact matmul runs on the bf16 tensor cores, so the
     bf16 rate is its peak."""
     base = peaks["bf16_tflops_sustained"]
-    return {"fp8": 2.0 * base, "fp4": 4.0 * base, "int8": base}[kind], {
-        "fp8": "2 x bf16_tflops_sustained (FP8/BF16 nominal ratio 2)",
-        "fp4": "4 x bf16_tflops_sustained (FP4/BF16 nominal ratio 4)",
+    return {"fp8": 2.0 * base, "fp4": 6.0 * base, "int8": base}[kind], {
+        "fp8": "2 x bf16_tflops_sustained (FP8/BF16 nominal dense ratio 4.5/2.25)",
+        "fp4": "6 x bf16_tflops_sustained (FP4/BF16 nominal dense ratio 13.5/2.25)",
         "int8": "bf16_tflops_sustained (the INT8 matmul runs exactly on the bf16 tensor cores)"}[kind]
 
 

@@ -178,3 +178,30 @@ def test_linear_backward_sampled(device):
     _check(np.array(got), np.array(ref), np.array(bnd), "dW", G.BF16_HALF_ULP)
     del wl
     _free()
+
+
+def test_e2e_pipelined_chunks_match_the_plain_step(device):
+    """bench.py's end-to-end step splits each problem into row chunks over
+    three streams; every output row depends on its own row alone, so the
+    results must equal the plain step's bit for bit."""
+    wl_spec = W.Workload("chunked e2e check", 5, (W.Grouped(1000, 256, 384), W.Grouped(3000, 512, 256)))
+    wl = bench.GroupedWork(wl_spec, device)
+    wl.E2E_ROWS = 256
+    wl.setup_host()
+    # the host input buffer holds the largest problem's raw inputs; give every
+    # problem those values so the two runs see the same data
+    for it in wl.items:
+        na, nb = it["a_raw"].numel(), it["b_raw"].numel()
+        it["a_raw"].view(-1).copy_(wl.hb_in[:na])
+        it["b_raw"].view(-1).copy_(wl.hb_in[na:na + nb])
+    wl.step()
+    torch.cuda.synchronize()
+    ref = [it["y"].clone() for it in wl.items]
+    for it in wl.items:
+        it["y"].zero_()
+    wl.step_e2e()
+    torch.cuda.synchronize()
+    for it, r in zip(wl.items, ref):
+        assert torch.equal(it["y"].view(torch.int32), r.view(torch.int32))
+    del wl
+    _free()
