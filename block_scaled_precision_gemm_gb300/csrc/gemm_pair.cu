@@ -286,44 +286,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     } else if (warp == 1 && lane == 0 && leader) {
       // ------------------------------------------------------- MMA issuer (leader)
-      int stage = 0, tb = 0;
-      uint32_t phase = 0, tph = 0;
-      bool ok = true;
-      // K blocks accumulated per TMEM buffer: one (kPairF32), a chunk
-      // (kPairI8) or all of K (block-scaled)
-      const int per_buf = MODE == kPairF32 ? 1 : (MODE == kPairI8 ? p.chunk : p.k_tiles);
-      for (int t = cid; ok && t < p.num_tiles; t += ncl) {
-        int kc = 0;  // K blocks already in the current buffer
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (kc == 0) {
-            if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
+      if constexpr (C::ATOMS > 0) {
+        // Block-scaled: one accumulator over all of K per tile; each stage's
+        // scale factors are copied into tensor memory ahead of its MMAs.
+        int stage = 0;
+        uint32_t phase = 0, tph = 0;
+        bool ok = true;
+        for (int t = cid; ok && t < p.num_tiles; t += ncl) {
+          if (!mbar_wait(&tempty[0], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) break;
+          tc_fence_after();
+          for (int kt = 0; kt < p.k_tiles; ++kt) {
+            if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
               ok = false;
               break;
             }
             tc_fence_after();
-          }
-          if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
-          const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
-          const uint32_t d = tmem + static_cast<uint32_t>(tb * PN);
-          if constexpr (MODE == kPairF32) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f8f6f4_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
-                              p.idesc, k > 0 ? 1u : 0u);
-            tc_commit_pair_mc(&empty[stage], 0x3);
-          } else if constexpr (MODE == kPairI8) {
-            // bf16 codes: a 128-byte K block is 64 elements, four K = 16 MMAs
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f16_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
-                           p.idesc, (kc > 0 || k > 0) ? 1u : 0u);
-            tc_commit_pair_mc(&empty[stage], 0x3);
-          } else {
+            const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
+            const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
             const uint32_t sfa_t = tmem + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
             const uint32_t sf_s = smem_u32(sSF + stage * C::SF_BYTES);
@@ -344,23 +323,71 @@ __global__ void __launch_bounds__(THREADS, 1)
               const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
               if constexpr (MODE == kPairMXF8) {
                 const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
-                mma_mxf8_pair(d, ad, bd, idesc, sfa_t, sfb_t, acc);
+                mma_mxf8_pair(tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
               } else {
-                mma_nvf4_pair(d, ad, bd, p.idesc, sfa_t + 4 * k, sfb_t + 8 * k, acc);
+                mma_nvf4_pair(tmem, ad, bd, p.idesc, sfa_t + 4 * k, sfb_t + 8 * k, acc);
               }
             }
             tc_commit_pair_mc(&empty[stage], 0x3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (++kc == per_buf || kt + 1 == p.k_tiles) {  // the buffer is complete
-            tc_commit_pair_mc(&tfull[tb], 0x3);
-            kc = 0;
-            if (++tb == NACC) {
-              tb = 0;
-              tph ^= 1u;
+          if (!ok) break;
+          tc_commit_pair_mc(&tfull[0], 0x3);
+          tph ^= 1u;
+        }
+      } else {
+        int stage = 0, tb = 0;
+        uint32_t phase = 0, tph = 0;
+        bool ok = true;
+        // K blocks accumulated per TMEM buffer: one (kPairF32) or a chunk
+        // (kPairI8)
+        const int per_buf = MODE == kPairF32 ? 1 : p.chunk;
+        for (int t = cid; ok && t < p.num_tiles; t += ncl) {
+          int kc = 0;  // K blocks already in the current buffer
+          for (int kt = 0; kt < p.k_tiles; ++kt) {
+            if (kc == 0) {
+              if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
+            const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
+            const uint32_t d = tmem + static_cast<uint32_t>(tb * PN);
+            if constexpr (MODE == kPairF32) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_f8f6f4_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
+                                p.idesc, k > 0 ? 1u : 0u);
+              tc_commit_pair_mc(&empty[stage], 0x3);
+            } else if constexpr (MODE == kPairI8) {
+              // bf16 codes: a 128-byte K block is 64 elements, four K = 16 MMAs
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_f16_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
+                             p.idesc, (kc > 0 || k > 0) ? 1u : 0u);
+              tc_commit_pair_mc(&empty[stage], 0x3);
+            }
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            if (++kc == per_buf || kt + 1 == p.k_tiles) {  // the buffer is complete
+              tc_commit_pair_mc(&tfull[tb], 0x3);
+              kc = 0;
+              if (++tb == NACC) {
+                tb = 0;
+                tph ^= 1u;
+              }
             }
           }
         }

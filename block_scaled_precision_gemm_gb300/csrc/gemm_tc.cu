@@ -458,30 +458,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 // tensor-core scale-factor layout: atom (b, row tile rt, K atom j) is 512
 // bytes; byte (r%32)*16 + ((r%128)/32)*4 + (kb%4) holds the scale of row
 // rt*128 + r for K block 4j + kb%4.  Missing rows / blocks get `pad`.
+// A thread owns word w of eight consecutive atoms j0..j0+7 of one row tile:
+// it reads the 32 scale bytes of row rt*128 + (w>>2) + 32*(w&3) for K blocks
+// 4*j0 .. 4*j0+31 (two 16-byte loads when in range and aligned) and writes
+// one word to each atom; a warp's stores to an atom are 128 contiguous bytes.
+// The 16-byte loads need KS % 16 == 0 and a 16-byte aligned base; otherwise
+// (and at the K tail) the bytes are read one by one.
 __global__ void __launch_bounds__(256) sf_relayout(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst,
                                                    int nb, int R, int KS, int RT, int KS4, uint32_t pad) {
-  const int64_t total = static_cast<int64_t>(nb) * RT * KS4 * 128;
+  const int groups = (KS4 + 7) / 8;  // groups of eight atoms per row tile
+  const int64_t total = static_cast<int64_t>(nb) * RT * groups * 128;
+  const uint32_t pad4 = pad * 0x01010101u;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int w = static_cast<int>(idx & 127);
-    const int64_t atom = idx >> 7;
-    const int j = static_cast<int>(atom % KS4);
-    const int64_t t2 = atom / KS4;
+    const int64_t t = idx >> 7;
+    const int jg = static_cast<int>(t % groups);
+    const int64_t t2 = t / groups;
     const int rt = static_cast<int>(t2 % RT);
     const int64_t b = t2 / RT;
     const int r = rt * 128 + (w >> 2) + 32 * (w & 3);
-    uint32_t word = pad * 0x01010101u;
-    if (r < R) {
-      const uint8_t* row = src + (b * R + r) * static_cast<int64_t>(KS);
-      word = 0;
+    const int kb0 = 32 * jg;
+    uint32_t word[8];
+    if (r >= R) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int kb = 4 * j + i;
-        const uint32_t v = kb < KS ? row[kb] : pad;
-        word |= v << (8 * i);
+      for (int i = 0; i < 8; ++i) word[i] = pad4;
+    } else {
+      const uint8_t* row = src + (b * R + r) * static_cast<int64_t>(KS);
+      if (kb0 + 32 <= KS && (KS & 15) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(row + kb0));
+        const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(row + kb0 + 16));
+        word[0] = v0.x; word[1] = v0.y; word[2] = v0.z; word[3] = v0.w;
+        word[4] = v1.x; word[5] = v1.y; word[6] = v1.z; word[7] = v1.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t v = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int kb = kb0 + 4 * i + k;
+            v |= static_cast<uint32_t>(kb < KS ? row[kb] : pad) << (8 * k);
+          }
+          word[i] = v;
+        }
       }
     }
-    dst[idx] = word;
+    uint32_t* out = dst + ((b * RT + rt) * static_cast<int64_t>(KS4) + 8 * jg) * 128 + w;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (8 * jg + i < KS4) out[i * 128] = word[i];
   }
 }
 
@@ -546,14 +571,14 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
   const uint32_t pad = nv ? 0u : 127u;
   {
     const int RT = rt_rows(r.M);
-    const int64_t words = r.B * RT * static_cast<int64_t>(ks4) * 128;
+    const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
     const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
     sf_relayout<<<blocks, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
                                        static_cast<int>(r.M), KS, RT, ks4, pad);
   }
   {
     const int RT = rt_rows(r.N);
-    const int64_t words = r.B * RT * static_cast<int64_t>(ks4) * 128;
+    const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
     const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
     sf_relayout<<<blocks, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
                                        static_cast<int>(r.N), KS, RT, ks4, pad);

@@ -260,3 +260,23 @@ def test_unsupported_block_16_with_ue8m0_is_reported():
     with pytest.raises(bsmm.BsmmError) as e:
         bsmm.gemm(a, a, s, s, "e4m3", "e4m3", "ue8m0")
     assert e.value.status == bsmm.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("offset", [1, 4])
+def test_mxfp8_scales_at_unaligned_base(offset):
+    """Scale arrays whose base is not 16-byte aligned (a view into a larger
+    buffer) take the relayout's byte path and give the same result."""
+    bsmm = _bsmm()
+    Bn, M, N, K = 1, 256, 256, 1024
+    ca, cb, sa, sb = mx_inputs(Bn, M, N, K, "e4m3", "e4m3", seed=77)
+    t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()  # noqa: E731
+    big_a = torch.zeros(sa.size + offset, dtype=torch.uint8, device="cuda")
+    big_b = torch.zeros(sb.size + offset, dtype=torch.uint8, device="cuda")
+    va = big_a[offset:].view(sa.shape)
+    vb = big_b[offset:].view(sb.shape)
+    va.copy_(t(sa))
+    vb.copy_(t(sb))
+    y = bsmm.gemm(t(ca), t(cb), va, vb, "e4m3", "e4m3", "ue8m0")
+    y_ref = bsmm.gemm(t(ca), t(cb), t(sa), t(sb), "e4m3", "e4m3", "ue8m0")
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
