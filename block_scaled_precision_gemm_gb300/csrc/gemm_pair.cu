@@ -301,25 +301,25 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
-            const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
+            // descriptors for the stage's first bytes, stepped by constants
+            const uint64_t a_d = smem_desc(smem_u32(sA + stage * A_BYTES), 16, 1024, 2);
+            const uint64_t b_d = smem_desc(smem_u32(sB + stage * B_BYTES), 16, 1024, 2);
+            const uint64_t sf_d = smem_desc(smem_u32(sSF + stage * C::SF_BYTES), 0, 128, 0);
             const uint32_t sfa_t = tmem + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-            const uint32_t sf_s = smem_u32(sSF + stage * C::SF_BYTES);
             // A atom i (K sub-block i) -> columns sfa_t + 4i; B atom (row tile
             // r, K sub-block i) -> columns sfb_t + 4*(2i + r).
 #pragma unroll
-            for (int i = 0; i < C::ATOMS; ++i) tc_cp_sf_pair(sfa_t + 4 * i, smem_desc(sf_s + 512 * i, 0, 128, 0));
+            for (int i = 0; i < C::ATOMS; ++i) tc_cp_sf_pair(sfa_t + 4 * i, desc_add(sf_d, 512 * i));
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
               for (int i = 0; i < C::ATOMS; ++i)
-                tc_cp_sf_pair(sfb_t + 4 * (2 * i + r),
-                              smem_desc(sf_s + C::SFA_BYTES + 512 * (r * C::ATOMS + i), 0, 128, 0));
+                tc_cp_sf_pair(sfb_t + 4 * (2 * i + r), desc_add(sf_d, C::SFA_BYTES + 512 * (r * C::ATOMS + i)));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = smem_desc(a_base + 32 * k, 16, 1024, 2);
-              const uint64_t bd = smem_desc(b_base + 32 * k, 16, 1024, 2);
+              const uint64_t ad = desc_add(a_d, 32 * k);
+              const uint64_t bd = desc_add(b_d, 32 * k);
               const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
               if constexpr (MODE == kPairMXF8) {
                 const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
@@ -360,21 +360,19 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
-            const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
+            const uint64_t a_d = smem_desc(smem_u32(sA + stage * A_BYTES), 16, 1024, 2);
+            const uint64_t b_d = smem_desc(smem_u32(sB + stage * B_BYTES), 16, 1024, 2);
             const uint32_t d = tmem + static_cast<uint32_t>(tb * PN);
             if constexpr (MODE == kPairF32) {
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_f8f6f4_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
-                                p.idesc, k > 0 ? 1u : 0u);
+                mma_f8f6f4_pair(d, desc_add(a_d, 32 * k), desc_add(b_d, 32 * k), p.idesc, k > 0 ? 1u : 0u);
               tc_commit_pair_mc(&empty[stage], 0x3);
             } else if constexpr (MODE == kPairI8) {
               // bf16 codes: a 128-byte K block is 64 elements, four K = 16 MMAs
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_f16_pair(d, smem_desc(a_base + 32 * k, 16, 1024, 2), smem_desc(b_base + 32 * k, 16, 1024, 2),
-                             p.idesc, (kc > 0 || k > 0) ? 1u : 0u);
+                mma_f16_pair(d, desc_add(a_d, 32 * k), desc_add(b_d, 32 * k), p.idesc, (kc > 0 || k > 0) ? 1u : 0u);
               tc_commit_pair_mc(&empty[stage], 0x3);
             }
             if (++stage == STAGES) {

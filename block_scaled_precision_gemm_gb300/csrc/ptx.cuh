@@ -163,6 +163,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// The descriptor of the address `bytes` (a multiple of 16) further on.
+// Shared addresses stay below 2^18, so the 14-bit address field never
+// carries into the fields above it.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // D[tmem] (+)= A[smem] * B[smem]^T, FP8 operands, no block scale.
 __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                            uint32_t accumulate) {
