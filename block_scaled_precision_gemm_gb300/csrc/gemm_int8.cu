@@ -76,6 +76,103 @@ __global__ void __launch_bounds__(256) i8_quant_rows(const float* __restrict__ x
   }
 }
 
+// The tensor-core path's row quantizer when a row fits in registers (D % 4
+// == 0, x 16-byte and x_q 4-byte aligned, D <= 1024 V): each of 256 threads
+// keeps V float4 of the row, so x is read once, and the codes leave as
+// 4-byte (int8) and 8-byte (bf16) stores.
+template <int V>
+__global__ void __launch_bounds__(256) i8_quant_rows_reg(const float* __restrict__ x, int64_t D, int64_t Kp,
+                                                         int8_t* __restrict__ xq, float* __restrict__ xs,
+                                                         __nv_bfloat16* __restrict__ xb) {
+  __shared__ float wmax[8];
+  const int64_t r = blockIdx.x;
+  const float4* row = reinterpret_cast<const float4*>(x + r * D);
+  const int n4 = static_cast<int>(D / 4);
+  float4 v[V];
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int c4 = threadIdx.x + 256 * i;
+    v[i] = c4 < n4 ? __ldg(row + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+  }
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = wmax[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
+  const float s = i8_scale(m);
+  if (threadIdx.x == 0) xs[r] = s;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int c4 = threadIdx.x + 256 * i;
+    if (c4 < n4) {
+      const int8_t q0 = i8_code(v[i].x, s), q1 = i8_code(v[i].y, s), q2 = i8_code(v[i].z, s), q3 = i8_code(v[i].w, s);
+      *reinterpret_cast<char4*>(xq + r * D + 4 * c4) = make_char4(q0, q1, q2, q3);
+      const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(q0))) |
+                          (static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(q1))) << 16);
+      const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(q2))) |
+                          (static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(q3))) << 16);
+      *reinterpret_cast<uint2*>(xb + r * Kp + 4 * c4) = make_uint2(lo, hi);
+    }
+  }
+  for (int64_t c = D + threadIdx.x; c < Kp; c += 256) xb[r * Kp + c] = __int2bfloat16_rn(0);
+}
+
+// Column maxima, four columns per thread (D_out % 4 == 0, w 16-byte
+// aligned): grid (ceil(D_out/128), row chunks), 8 warps stride rows with four
+// 16-byte loads in flight per thread.
+__global__ void __launch_bounds__(256) i8_colmax4(const float* __restrict__ w, int64_t D_in, int64_t D_out,
+                                                  int rows_per_cta, unsigned* __restrict__ colmax) {
+  __shared__ float4 wm[8][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t c4 = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  const int64_t n4 = D_out / 4;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_cta;
+  const int64_t r1 = (D_in < r0 + rows_per_cta) ? D_in : r0 + rows_per_cta;
+  float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c4 < n4) {
+    const float4* base = reinterpret_cast<const float4*>(w) + c4;
+    int64_t r = r0 + warp;
+    for (; r + 24 < r1; r += 32) {
+      float4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) t[u] = __ldg(base + (r + 8 * u) * n4);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        m.x = fmaxf(m.x, fabsf(t[u].x));
+        m.y = fmaxf(m.y, fabsf(t[u].y));
+        m.z = fmaxf(m.z, fabsf(t[u].z));
+        m.w = fmaxf(m.w, fabsf(t[u].w));
+      }
+    }
+    for (; r < r1; r += 8) {
+      const float4 t = __ldg(base + r * n4);
+      m.x = fmaxf(m.x, fabsf(t.x));
+      m.y = fmaxf(m.y, fabsf(t.y));
+      m.z = fmaxf(m.z, fabsf(t.z));
+      m.w = fmaxf(m.w, fabsf(t.w));
+    }
+  }
+  wm[warp][lane] = m;
+  __syncthreads();
+  if (warp == 0 && c4 < n4) {
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      m.x = fmaxf(m.x, wm[i][lane].x);
+      m.y = fmaxf(m.y, wm[i][lane].y);
+      m.z = fmaxf(m.z, wm[i][lane].z);
+      m.w = fmaxf(m.w, wm[i][lane].w);
+    }
+    unsigned* cm = colmax + 4 * c4;
+    atomicMax(cm + 0, __float_as_uint(m.x));  // non-negative floats order like their bits
+    atomicMax(cm + 1, __float_as_uint(m.y));
+    atomicMax(cm + 2, __float_as_uint(m.z));
+    atomicMax(cm + 3, __float_as_uint(m.w));
+  }
+}
+
 // grid (ceil(D_out/32), row chunks); lane = column, 8 warps stride rows.
 __global__ void __launch_bounds__(256) i8_colmax(const float* __restrict__ w, int64_t D_in, int64_t D_out,
                                                  int rows_per_cta, unsigned* __restrict__ colmax) {
@@ -110,12 +207,19 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
   const int64_t j = j0 + jj;
   const float s = j < D_out ? i8_scale(__uint_as_float(colmax[j])) : 1.f;
   if (blockIdx.y == 0 && ig == 0 && j < D_out) ws[j] = s;
+  float v[16];  // all sixteen loads in flight before any arithmetic
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int64_t i = i0 + ig * 16 + k;
+    v[k] = (i < D_in && j < D_out) ? __ldg(w + i * D_out + j) : 0.f;
+  }
+#pragma unroll
   for (int k = 0; k < 16; ++k) {
     const int ii = ig * 16 + k;
     const int64_t i = i0 + ii;
     int8_t q = 0;
     if (i < D_in && j < D_out) {
-      q = i8_code(__ldg(w + i * D_out + j), s);
+      q = i8_code(v[k], s);
       wq[i * D_out + j] = q;
     }
     tile[ii][jj] = q;
@@ -313,13 +417,29 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
 
   cudaError_t e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(r.D_out) * 4, s);
   if (e != cudaSuccess) return e;
-  if (tc)
-    i8_quant_rows<__nv_bfloat16><<<static_cast<unsigned>(r.B), 256, 0, s>>>(
-        r.x, r.D_in, Kp, r.x_q, r.x_scales, reinterpret_cast<__nv_bfloat16*>(xpad));
+  const bool rows_vec = (r.D_in % 4) == 0 && (reinterpret_cast<uintptr_t>(r.x) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(r.x_q) & 3) == 0 && r.D_in <= 8192;
+  __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xpad);
+  const unsigned nrows = static_cast<unsigned>(r.B);
+  if (tc && rows_vec) {
+    if (r.D_in <= 1024)
+      i8_quant_rows_reg<1><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
+    else if (r.D_in <= 2048)
+      i8_quant_rows_reg<2><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
+    else if (r.D_in <= 4096)
+      i8_quant_rows_reg<4><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
+    else
+      i8_quant_rows_reg<8><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
+  } else if (tc)
+    i8_quant_rows<__nv_bfloat16><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
   else
     i8_quant_rows<int8_t><<<static_cast<unsigned>(r.B), 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales,
                                                                      reinterpret_cast<int8_t*>(xpad));
-  {
+  if ((r.D_out % 4) == 0 && (reinterpret_cast<uintptr_t>(r.w) & 15) == 0) {
+    const int rows_per_cta = 256;
+    dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 128)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
+    i8_colmax4<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
+  } else {
     const int rows_per_cta = 256;
     dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 32)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
     i8_colmax<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
