@@ -266,130 +266,143 @@ __global__ void __launch_bounds__(256) quant_rows(QP p) {
 constexpr int kColTileR = 128, kColTileC = 64;
 
 template <typename In, bool POW2>
-__global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok) {
+// Persistent: CTA b takes tiles b, b + gridDim.x, ... (column tiles fastest);
+// on the vector path the next tile's raw data is loaded into registers while
+// the current one is reduced and encoded.
+__global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok, int tiles_c, int64_t n_tiles) {
   __shared__ float tile[kColTileR][kColTileC + 1];
   __shared__ float pmax[4][kColTileC];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColTileR;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kColTileC;
-  const int nr = static_cast<int>(p.rows - r0 < kColTileR ? p.rows - r0 : kColTileR);
-  const int nc = static_cast<int>(p.cols - c0 < kColTileC ? p.cols - c0 : kColTileC);
   const int t = threadIdx.x;
   const In* x = reinterpret_cast<const In*>(p.x);
-  // Stage the tile (coalesced along columns).
-  if (vec_ok) {
-    constexpr int VEC = 16 / sizeof(In);
-    constexpr int VPR = kColTileC / VEC;        // vectors per tile row
-    constexpr int NV = kColTileR * VPR / 256;   // vectors per thread
-    uint4 raw[NV];
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {  // all loads in flight before any use
-      const int i = t + 256 * j;
-      const int rr = i / VPR, cv = i % VPR;
-      raw[j] = (rr < nr && cv * VEC < nc)
-                   ? __ldcs(reinterpret_cast<const uint4*>(x + (r0 + rr) * p.ld_x + c0 + cv * VEC))
-                   : make_uint4(0u, 0u, 0u, 0u);
-    }
+  constexpr int VEC = 16 / sizeof(In);
+  constexpr int VPR = kColTileC / VEC;        // vectors per tile row
+  constexpr int NV = kColTileR * VPR / 256;   // vectors per thread
+  uint4 raw[NV];
+  auto fetch = [&](int64_t tt) {  // all loads in flight before any use
+    const int64_t fr0 = (tt / tiles_c) * kColTileR, fc0 = (tt % tiles_c) * kColTileC;
+    const int fnr = static_cast<int>(p.rows - fr0 < kColTileR ? p.rows - fr0 : kColTileR);
+    const int fnc = static_cast<int>(p.cols - fc0 < kColTileC ? p.cols - fc0 : kColTileC);
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int i = t + 256 * j;
       const int rr = i / VPR, cv = i % VPR;
-      const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-      if constexpr (sizeof(In) == 4) {
+      raw[j] = (rr < fnr && cv * VEC < fnc)
+                   ? __ldcs(reinterpret_cast<const uint4*>(x + (fr0 + rr) * p.ld_x + fc0 + cv * VEC))
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if (vec_ok && blockIdx.x < n_tiles) fetch(blockIdx.x);
+  for (int64_t tt = blockIdx.x; tt < n_tiles; tt += gridDim.x) {
+    const int64_t r0 = (tt / tiles_c) * kColTileR;
+    const int64_t c0 = (tt % tiles_c) * kColTileC;
+    const int nr = static_cast<int>(p.rows - r0 < kColTileR ? p.rows - r0 : kColTileR);
+    const int nc = static_cast<int>(p.cols - c0 < kColTileC ? p.cols - c0 : kColTileC);
+    __syncthreads();  // every thread is done with the previous tile's shared data
+    // Stage the tile (coalesced along columns).
+    if (vec_ok) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tile[rr][cv * 4 + k] = __uint_as_float(w[k]);
+      for (int j = 0; j < NV; ++j) {
+        const int i = t + 256 * j;
+        const int rr = i / VPR, cv = i % VPR;
+        const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+        if constexpr (sizeof(In) == 4) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tile[rr][cv * 4 + k] = __uint_as_float(w[k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            tile[rr][cv * 8 + 2 * k] = __uint_as_float(w[k] << 16);
+            tile[rr][cv * 8 + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+          }
+        }
+      }
+    } else {
+      for (int i = t; i < kColTileR * kColTileC; i += 256) {
+        const int rr = i / kColTileC, cc = i % kColTileC;
+        tile[rr][cc] = (rr < nr && cc < nc) ? load1<In>(x, (r0 + rr) * p.ld_x + c0 + cc) : 0.f;
+      }
+    }
+    __syncthreads();
+    if (vec_ok && tt + gridDim.x < n_tiles) fetch(tt + gridDim.x);
+    // Thread (col, part) owns rows 32*part .. 32*part+31 of one column, held in
+    // registers from here on.
+    const int col = t % kColTileC, part = t / kColTileC;
+    const int rbase = part * 32;
+    const int br = p.br;
+    float m0 = 0.f, m1 = 0.f;  // maxima of the two 16-row halves
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m0 = fmaxf(m0, fabsf(tile[rbase + i][col]));
+#pragma unroll
+    for (int i = 16; i < 32; ++i) m1 = fmaxf(m1, fabsf(tile[rbase + i][col]));
+    if (br > 32) {
+      pmax[part][col] = fmaxf(m0, m1);
+      __syncthreads();
+    }
+    const bool active = rbase < nr && col < nc;
+    // Scales of the (one or two) blocks this thread's 32 rows belong to.
+    float amax_a, amax_b;
+    if (br == 16) {
+      amax_a = m0;
+      amax_b = m1;
+    } else if (br == 32) {
+      amax_a = amax_b = fmaxf(m0, m1);
+    } else if (br == 64) {
+      const int pp = part & ~1;
+      amax_a = amax_b = fmaxf(pmax[pp][col], pmax[pp + 1][col]);
+    } else {
+      amax_a = amax_b = fmaxf(fmaxf(pmax[0][col], pmax[1][col]), fmaxf(pmax[2][col], pmax[3][col]));
+    }
+    const Scale sa = make_scale(amax_a, p.code, p.scale);
+    const Scale sb = (br == 16) ? make_scale(amax_b, p.code, p.scale) : sa;
+    if (active) {
+      const int64_t gc = c0 + col;
+      const int64_t blk0 = (r0 + rbase) / br;
+      const bool writes_a = (rbase % br) == 0;
+      if (p.transpose) {
+        if (writes_a) store_scale(p.scales, gc * p.ld_scales + blk0, p.scale, sa.stored);
+        if (br == 16) store_scale(p.scales, gc * p.ld_scales + blk0 + 1, p.scale, sb.stored);
       } else {
+        if (writes_a) store_scale(p.scales, blk0 * p.ld_scales + gc, p.scale, sa.stored);
+        if (br == 16) store_scale(p.scales, (blk0 + 1) * p.ld_scales + gc, p.scale, sb.stored);
+      }
+    }
+    uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
+    if (p.transpose) {
+      if (!active) continue;
+      // 32 consecutive output elements of row `gc` of the transposed array.
+      uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          tile[rr][cv * 8 + 2 * k] = __uint_as_float(w[k] << 16);
-          tile[rr][cv * 8 + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      for (int g = 0; g < 8; ++g)
+        w[g] = encode4<POW2>(tile[rbase + 4 * g][col], tile[rbase + 4 * g + 1][col], tile[rbase + 4 * g + 2][col],
+                       tile[rbase + 4 * g + 3][col], g < 4 ? sa : sb, p.code);
+      const int64_t e = (c0 + col) * p.ld_codes + r0 + rbase;
+      const bool full32 = rbase + 32 <= nr;  // else only the first 16 rows exist
+      if (p.code == BSMM_E2M1) {
+        if (full32)
+          *reinterpret_cast<uint4*>(out + e / 2) =
+              make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16), w[6] | (w[7] << 16));
+        else
+          *reinterpret_cast<uint2*>(out + e / 2) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+      } else {
+        *reinterpret_cast<uint4*>(out + e) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (full32) *reinterpret_cast<uint4*>(out + e + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    } else {
+      // Row-major codes: lanes hold consecutive columns.
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t cval = encode1<POW2>(tile[rbase + i][col], i < 16 ? sa : sb, p.code);
+        const int64_t e = (r0 + rbase + i) * p.ld_codes + c0 + col;
+        const bool ok = active && rbase + i < nr;
+        if (p.code == BSMM_E2M1) {
+          const uint32_t hi = __shfl_down_sync(0xffffffffu, cval, 1);
+          if (ok && (col & 1) == 0) out[e / 2] = static_cast<uint8_t>(cval | (hi << 4));
+        } else if (ok) {
+          out[e] = static_cast<uint8_t>(cval);
         }
       }
     }
-  } else {
-    for (int i = t; i < kColTileR * kColTileC; i += 256) {
-      const int rr = i / kColTileC, cc = i % kColTileC;
-      tile[rr][cc] = (rr < nr && cc < nc) ? load1<In>(x, (r0 + rr) * p.ld_x + c0 + cc) : 0.f;
-    }
-  }
-  __syncthreads();
-  // Thread (col, part) owns rows 32*part .. 32*part+31 of one column, held in
-  // registers from here on.
-  const int col = t % kColTileC, part = t / kColTileC;
-  const int rbase = part * 32;
-  const int br = p.br;
-  float m0 = 0.f, m1 = 0.f;  // maxima of the two 16-row halves
-#pragma unroll
-  for (int i = 0; i < 16; ++i) m0 = fmaxf(m0, fabsf(tile[rbase + i][col]));
-#pragma unroll
-  for (int i = 16; i < 32; ++i) m1 = fmaxf(m1, fabsf(tile[rbase + i][col]));
-  if (br > 32) {
-    pmax[part][col] = fmaxf(m0, m1);
-    __syncthreads();
-  }
-  const bool active = rbase < nr && col < nc;
-  // Scales of the (one or two) blocks this thread's 32 rows belong to.
-  float amax_a, amax_b;
-  if (br == 16) {
-    amax_a = m0;
-    amax_b = m1;
-  } else if (br == 32) {
-    amax_a = amax_b = fmaxf(m0, m1);
-  } else if (br == 64) {
-    const int pp = part & ~1;
-    amax_a = amax_b = fmaxf(pmax[pp][col], pmax[pp + 1][col]);
-  } else {
-    amax_a = amax_b = fmaxf(fmaxf(pmax[0][col], pmax[1][col]), fmaxf(pmax[2][col], pmax[3][col]));
-  }
-  const Scale sa = make_scale(amax_a, p.code, p.scale);
-  const Scale sb = (br == 16) ? make_scale(amax_b, p.code, p.scale) : sa;
-  if (active) {
-    const int64_t gc = c0 + col;
-    const int64_t blk0 = (r0 + rbase) / br;
-    const bool writes_a = (rbase % br) == 0;
-    if (p.transpose) {
-      if (writes_a) store_scale(p.scales, gc * p.ld_scales + blk0, p.scale, sa.stored);
-      if (br == 16) store_scale(p.scales, gc * p.ld_scales + blk0 + 1, p.scale, sb.stored);
-    } else {
-      if (writes_a) store_scale(p.scales, blk0 * p.ld_scales + gc, p.scale, sa.stored);
-      if (br == 16) store_scale(p.scales, (blk0 + 1) * p.ld_scales + gc, p.scale, sb.stored);
-    }
-  }
-  uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
-  if (p.transpose) {
-    if (!active) return;
-    // 32 consecutive output elements of row `gc` of the transposed array.
-    uint32_t w[8];
-#pragma unroll
-    for (int g = 0; g < 8; ++g)
-      w[g] = encode4<POW2>(tile[rbase + 4 * g][col], tile[rbase + 4 * g + 1][col], tile[rbase + 4 * g + 2][col],
-                     tile[rbase + 4 * g + 3][col], g < 4 ? sa : sb, p.code);
-    const int64_t e = (c0 + col) * p.ld_codes + r0 + rbase;
-    const bool full32 = rbase + 32 <= nr;  // else only the first 16 rows exist
-    if (p.code == BSMM_E2M1) {
-      if (full32)
-        *reinterpret_cast<uint4*>(out + e / 2) =
-            make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16), w[6] | (w[7] << 16));
-      else
-        *reinterpret_cast<uint2*>(out + e / 2) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
-    } else {
-      *reinterpret_cast<uint4*>(out + e) = make_uint4(w[0], w[1], w[2], w[3]);
-      if (full32) *reinterpret_cast<uint4*>(out + e + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-  } else {
-    // Row-major codes: lanes hold consecutive columns.
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t cval = encode1<POW2>(tile[rbase + i][col], i < 16 ? sa : sb, p.code);
-      const int64_t e = (r0 + rbase + i) * p.ld_codes + c0 + col;
-      const bool ok = active && rbase + i < nr;
-      if (p.code == BSMM_E2M1) {
-        const uint32_t hi = __shfl_down_sync(0xffffffffu, cval, 1);
-        if (ok && (col & 1) == 0) out[e / 2] = static_cast<uint8_t>(cval | (hi << 4));
-      } else if (ok) {
-        out[e] = static_cast<uint8_t>(cval);
-      }
-    }
-  }
+  }  // tiles
 }
 
 // ---------------------------------------------------------------------------
@@ -562,8 +575,11 @@ cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
     blocks = std::min<int64_t>(blocks, static_cast<int64_t>(ctx->num_sms) * 8);
     quant_rows<In, POW2><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(p);
   } else if (p.bc == 1 && pow2_small_r && (!p.transpose || (codes16 && p.ld_codes % 32 == 0))) {
-    dim3 grid(static_cast<unsigned>(ceil_div(p.cols, kColTileC)), static_cast<unsigned>(ceil_div(p.rows, kColTileR)));
-    quant_cols<In, POW2><<<grid, 256, 0, s>>>(p, x_vec ? 1 : 0);
+    const int tiles_c = static_cast<int>(ceil_div(p.cols, kColTileC));
+    const int64_t n_tiles = static_cast<int64_t>(tiles_c) * ceil_div(p.rows, kColTileR);
+    const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 6);
+    quant_cols<In, POW2><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, 0, s>>>(p, x_vec ? 1 : 0, tiles_c,
+                                                                                      n_tiles);
   } else if (p.br == 128 && p.bc == 128 && !p.transpose && x_vec && codes16) {
     dim3 grid(static_cast<unsigned>(p.cols / 128), static_cast<unsigned>(p.rows / 128));
     quant_tile<In, POW2><<<grid, 256, 0, s>>>(p);
