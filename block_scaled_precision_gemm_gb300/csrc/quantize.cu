@@ -269,9 +269,22 @@ template <typename In, bool POW2>
 // Persistent: CTA b takes tiles b, b + gridDim.x, ... (column tiles fastest);
 // on the vector path the next tile's raw data is loaded into registers while
 // the current one is reduced and encoded.
-__global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok, int tiles_c, int64_t n_tiles) {
-  __shared__ float tile[kColTileR][kColTileC + 1];
+// The tile keeps the input type: FP32 as words (65 per row), bf16 as
+// packed pairs (33 words per row).  Either stride leaves the row-wise vector
+// stores and the column reads free of bank conflicts, and bf16 tiles take
+// half the shared memory and traffic.
+__global__ void __launch_bounds__(256, 3) quant_cols(QP p, int vec_ok, int tiles_c, int64_t n_tiles) {
+  constexpr int kRowWords = sizeof(In) == 4 ? kColTileC + 1 : kColTileC / 2 + 1;
+  __shared__ __align__(16) uint32_t tile_w[kColTileR * kRowWords];
   __shared__ float pmax[4][kColTileC];
+  auto tile_val = [&](int r, int c) -> float {
+    if constexpr (sizeof(In) == 4) {
+      return __uint_as_float(tile_w[r * kRowWords + c]);
+    } else {
+      const uint32_t wv = tile_w[r * kRowWords + (c >> 1)];
+      return __uint_as_float((c & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
+    }
+  };
   const int t = threadIdx.x;
   const In* x = reinterpret_cast<const In*>(p.x);
   constexpr int VEC = 16 / sizeof(In);
@@ -305,21 +318,17 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok, int tiles_c,
         const int i = t + 256 * j;
         const int rr = i / VPR, cv = i % VPR;
         const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-        if constexpr (sizeof(In) == 4) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tile[rr][cv * 4 + k] = __uint_as_float(w[k]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            tile[rr][cv * 8 + 2 * k] = __uint_as_float(w[k] << 16);
-            tile[rr][cv * 8 + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-          }
-        }
+        for (int k = 0; k < 4; ++k) tile_w[rr * kRowWords + cv * 4 + k] = w[k];  // 4 floats or 8 bf16
       }
     } else {
       for (int i = t; i < kColTileR * kColTileC; i += 256) {
         const int rr = i / kColTileC, cc = i % kColTileC;
-        tile[rr][cc] = (rr < nr && cc < nc) ? load1<In>(x, (r0 + rr) * p.ld_x + c0 + cc) : 0.f;
+        const float v = (rr < nr && cc < nc) ? load1<In>(x, (r0 + rr) * p.ld_x + c0 + cc) : 0.f;
+        if constexpr (sizeof(In) == 4)
+          tile_w[rr * kRowWords + cc] = __float_as_uint(v);
+        else  // v is a bf16 value: its top 16 bits are the code
+          reinterpret_cast<uint16_t*>(tile_w)[rr * 2 * kRowWords + cc] = static_cast<uint16_t>(__float_as_uint(v) >> 16);
       }
     }
     __syncthreads();
@@ -329,11 +338,14 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok, int tiles_c,
     const int col = t % kColTileC, part = t / kColTileC;
     const int rbase = part * 32;
     const int br = p.br;
+    float v[32];  // read once from shared memory
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = tile_val(rbase + i, col);
     float m0 = 0.f, m1 = 0.f;  // maxima of the two 16-row halves
 #pragma unroll
-    for (int i = 0; i < 16; ++i) m0 = fmaxf(m0, fabsf(tile[rbase + i][col]));
+    for (int i = 0; i < 16; ++i) m0 = fmaxf(m0, fabsf(v[i]));
 #pragma unroll
-    for (int i = 16; i < 32; ++i) m1 = fmaxf(m1, fabsf(tile[rbase + i][col]));
+    for (int i = 16; i < 32; ++i) m1 = fmaxf(m1, fabsf(v[i]));
     if (br > 32) {
       pmax[part][col] = fmaxf(m0, m1);
       __syncthreads();
@@ -373,8 +385,7 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok, int tiles_c,
       uint32_t w[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g)
-        w[g] = encode4<POW2>(tile[rbase + 4 * g][col], tile[rbase + 4 * g + 1][col], tile[rbase + 4 * g + 2][col],
-                       tile[rbase + 4 * g + 3][col], g < 4 ? sa : sb, p.code);
+        w[g] = encode4<POW2>(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3], g < 4 ? sa : sb, p.code);
       const int64_t e = (c0 + col) * p.ld_codes + r0 + rbase;
       const bool full32 = rbase + 32 <= nr;  // else only the first 16 rows exist
       if (p.code == BSMM_E2M1) {
@@ -391,7 +402,7 @@ __global__ void __launch_bounds__(256) quant_cols(QP p, int vec_ok, int tiles_c,
       // Row-major codes: lanes hold consecutive columns.
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const uint32_t cval = encode1<POW2>(tile[rbase + i][col], i < 16 ? sa : sb, p.code);
+        const uint32_t cval = encode1<POW2>(v[i], i < 16 ? sa : sb, p.code);
         const int64_t e = (r0 + rbase + i) * p.ld_codes + c0 + col;
         const bool ok = active && rbase + i < nr;
         if (p.code == BSMM_E2M1) {
@@ -577,7 +588,7 @@ cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
   } else if (p.bc == 1 && pow2_small_r && (!p.transpose || (codes16 && p.ld_codes % 32 == 0))) {
     const int tiles_c = static_cast<int>(ceil_div(p.cols, kColTileC));
     const int64_t n_tiles = static_cast<int64_t>(tiles_c) * ceil_div(p.rows, kColTileR);
-    const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 6);
+    const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 3);
     quant_cols<In, POW2><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, 0, s>>>(p, x_vec ? 1 : 0, tiles_c,
                                                                                       n_tiles);
   } else if (p.br == 128 && p.bc == 128 && !p.transpose && x_vec && codes16) {
