@@ -338,24 +338,55 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_commit_pair_mc(&tfull[0], 0x3);
           tph ^= 1u;
         }
-      } else {
+      } else if constexpr (MODE == kPairI8) {
+        // one TMEM buffer per chunk of p.chunk K blocks (exact FP32 integer
+        // sums), alternating between the two buffers
         int stage = 0, tb = 0;
         uint32_t phase = 0, tph = 0;
         bool ok = true;
-        // K blocks accumulated per TMEM buffer: one (kPairF32) or a chunk
-        // (kPairI8)
-        const int per_buf = MODE == kPairF32 ? 1 : p.chunk;
         for (int t = cid; ok && t < p.num_tiles; t += ncl) {
-          int kc = 0;  // K blocks already in the current buffer
-          for (int kt = 0; kt < p.k_tiles; ++kt) {
-            if (kc == 0) {
-              if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
+          for (int k0 = 0; ok && k0 < p.k_tiles; k0 += p.chunk) {
+            if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + static_cast<uint32_t>(tb * PN);
+            const int k1 = k0 + p.chunk < p.k_tiles ? k0 + p.chunk : p.k_tiles;
+            for (int kt = k0; kt < k1; ++kt) {
+              if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
+              const uint64_t a_d = smem_desc(smem_u32(sA + stage * A_BYTES), 16, 1024, 2);
+              const uint64_t b_d = smem_desc(smem_u32(sB + stage * B_BYTES), 16, 1024, 2);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_f16_pair(d, desc_add(a_d, 32 * k), desc_add(b_d, 32 * k), p.idesc, (kt > k0 || k > 0) ? 1u : 0u);
+              tc_commit_pair_mc(&empty[stage], 0x3);
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
             }
-            if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
+            if (!ok) break;
+            tc_commit_pair_mc(&tfull[tb], 0x3);
+            if (++tb == NACC) {
+              tb = 0;
+              tph ^= 1u;
+            }
+          }
+        }
+      } else {
+        // kPairF32: every K block's partial gets a TMEM buffer of its own
+        int stage = 0, tb = 0;
+        uint32_t phase = 0, tph = 0;
+        bool ok = true;
+        for (int t = cid; ok && t < p.num_tiles; t += ncl) {
+          for (int kt = 0; kt < p.k_tiles; ++kt) {
+            if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem) ||
+                !mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
               ok = false;
               break;
             }
@@ -363,29 +394,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t a_d = smem_desc(smem_u32(sA + stage * A_BYTES), 16, 1024, 2);
             const uint64_t b_d = smem_desc(smem_u32(sB + stage * B_BYTES), 16, 1024, 2);
             const uint32_t d = tmem + static_cast<uint32_t>(tb * PN);
-            if constexpr (MODE == kPairF32) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_f8f6f4_pair(d, desc_add(a_d, 32 * k), desc_add(b_d, 32 * k), p.idesc, k > 0 ? 1u : 0u);
-              tc_commit_pair_mc(&empty[stage], 0x3);
-            } else if constexpr (MODE == kPairI8) {
-              // bf16 codes: a 128-byte K block is 64 elements, four K = 16 MMAs
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_f16_pair(d, desc_add(a_d, 32 * k), desc_add(b_d, 32 * k), p.idesc, (kc > 0 || k > 0) ? 1u : 0u);
-              tc_commit_pair_mc(&empty[stage], 0x3);
-            }
+            for (int k = 0; k < 4; ++k)
+              mma_f8f6f4_pair(d, desc_add(a_d, 32 * k), desc_add(b_d, 32 * k), p.idesc, k > 0 ? 1u : 0u);
+            tc_commit_pair_mc(&empty[stage], 0x3);
+            tc_commit_pair_mc(&tfull[tb], 0x3);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
-            if (++kc == per_buf || kt + 1 == p.k_tiles) {  // the buffer is complete
-              tc_commit_pair_mc(&tfull[tb], 0x3);
-              kc = 0;
-              if (++tb == NACC) {
-                tb = 0;
-                tph ^= 1u;
-              }
+            if (++tb == NACC) {
+              tb = 0;
+              tph ^= 1u;
             }
           }
         }
