@@ -297,7 +297,8 @@ bsmm_status bsmm_gemm_grouped(int64_t M, int64_t N, int64_t K, const void* a, bs
 }
 
 size_t bsmm_int8_channel_workspace_size(int64_t B, int64_t D_in, int64_t D_out) {
-  if (B <= 0 || D_in <= 0 || D_out <= 0) return 0;
+  if (B < 0 || D_in <= 0 || D_out <= 0) return 0;
+  if (B == 0) return align_up(static_cast<size_t>(D_out) * 4, 256);  // w alone: its column maxima
   return int8_workspace_bytes(B, D_in, D_out);
 }
 
@@ -305,11 +306,20 @@ bsmm_status bsmm_int8_channel(const float* x, const float* w, int64_t B, int64_t
                               float* x_scales, int8_t* w_q, float* w_scales, float* y, int32_t* acc,
                               void* workspace, size_t workspace_bytes, bsmm_stream_t stream) {
   if (B < 0 || D_in < 0 || D_out < 0) return fail(BSMM_ERR_INVALID_ARG, "negative size");
-  if (B == 0 || D_out == 0) {
+  if (D_out == 0) {
     set_error("");
     return BSMM_OK;
   }
   if (D_in == 0) return fail(BSMM_ERR_UNSUPPORTED, "D_in == 0");
+  if (B == 0) {  // no rows of x: w_q and w_scales are still outputs
+    if (!w || !w_q || !w_scales) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
+    const size_t need = bsmm_int8_channel_workspace_size(0, D_in, D_out);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return fail(BSMM_ERR_WORKSPACE, "workspace must be 256-byte aligned and at least " + std::to_string(need) +
+                                          " bytes");
+    Int8Request r{x, w, 0, D_in, D_out, x_q, x_scales, w_q, w_scales, y, acc, workspace};
+    return launched(launch_int8_channel(r, reinterpret_cast<cudaStream_t>(stream)), "int8 launch");
+  }
   if (!x || !w || !x_q || !x_scales || !w_q || !w_scales || !y) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(y) || (acc && !aligned16(acc))) return fail(BSMM_ERR_ALIGNMENT, "y and acc must be 16-byte aligned");
   if (B > 65535LL * 128 || D_out > INT32_MAX / 2 || D_in > 1 << 24)

@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
   // transposed write: thread -> (row j of wqT, 16 consecutive i)
   const int jt = t >> 2, part = t & 3;
   const int64_t jrow = j0 + jt;
-  if (jrow < D_out) {
+  if (wqT != nullptr && jrow < D_out) {  // no matmul copy when x has no rows
     const int64_t ibase = i0 + part * 16;
     if (ibase < Kp) {
       if constexpr (sizeof(Pad) == 1) {
@@ -417,6 +417,14 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
 
   cudaError_t e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(r.D_out) * 4, s);
   if (e != cudaSuccess) return e;
+  if (r.B == 0) {  // w alone: column maxima, then codes and scales (no transposed copy)
+    const int rows_per_cta = 256;
+    dim3 g1(static_cast<unsigned>(ceil_div(r.D_out, 32)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
+    i8_colmax<<<g1, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
+    dim3 g2(static_cast<unsigned>(ceil_div(r.D_out, 64)), static_cast<unsigned>(Kp / 64));
+    i8_quant_cols<int8_t><<<g2, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales, nullptr);
+    return cudaGetLastError();
+  }
   const bool rows_vec = (r.D_in % 4) == 0 && (reinterpret_cast<uintptr_t>(r.x) & 15) == 0 &&
                         (reinterpret_cast<uintptr_t>(r.x_q) & 3) == 0 && r.D_in <= 8192;
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xpad);

@@ -255,7 +255,10 @@ bsmm_status bsmm_gemm_grouped(int64_t M, int64_t N, int64_t K, const void* a, bs
  *   workspace  at least bsmm_int8_channel_workspace_size() bytes (holds
  *            K-padded, K-major copies of both operands' codes for the
  *            matmul).
- *   D_in must be a multiple of 16.
+ *   Any D_in >= 1 (the matmul's copies are zero-padded to a multiple of
+ *   128).  With B == 0 only w is quantized (w_q,
+ *   w_scales); x, x_q, x_scales, y and acc are not touched, and the
+ *   workspace needs D_out * 4 bytes (the query returns it).
  * The integer sums are exact for any codes: the matmul runs on the bf16
  * tensor cores (codes and their products are exact there) and adds FP32
  * partials of at most 1024 products, each an exact integer below 2^24, in

@@ -280,3 +280,28 @@ def test_mxfp8_scales_at_unaligned_base(offset):
     y_ref = bsmm.gemm(t(ca), t(cb), t(sa), t(sb), "e4m3", "e4m3", "ue8m0")
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
+
+
+@pytest.mark.parametrize("m,n", [(0, 256), (128, 0)])
+def test_grouped_empty_output_is_a_no_op(m, n):
+    """An empty M or N gives an empty y and launches nothing (K stays 256)."""
+    bsmm = _bsmm()
+    a = torch.zeros((m, 256), dtype=torch.uint8, device="cuda")
+    b = torch.zeros((n, 256), dtype=torch.uint8, device="cuda")
+    sa = torch.ones((m, 2), dtype=torch.float32, device="cuda")
+    sb = torch.ones((max(1, (n + 127) // 128), 2), dtype=torch.float32, device="cuda")
+    y = bsmm.gemm_grouped(a, b, sa, sb)
+    torch.cuda.synchronize()
+    assert y.shape == (m, n) and bsmm.check_device_status()[0] == 0
+
+
+@pytest.mark.parametrize("Bn,M,N", [(0, 64, 64), (2, 0, 64), (2, 64, 0)])
+def test_batched_empty_output_is_a_no_op(Bn, M, N):
+    bsmm = _bsmm()
+    a = torch.zeros((Bn, M, 64), dtype=torch.uint8, device="cuda")
+    b = torch.zeros((Bn, N, 64), dtype=torch.uint8, device="cuda")
+    sa = torch.full((Bn, M, 2), 127, dtype=torch.uint8, device="cuda")
+    sb = torch.full((Bn, N, 2), 127, dtype=torch.uint8, device="cuda")
+    y = bsmm.gemm(a, b, sa, sb, "e4m3", "e4m3", "ue8m0")
+    torch.cuda.synchronize()
+    assert y.shape == (Bn, M, N) and bsmm.check_device_status()[0] == 0

@@ -172,3 +172,18 @@ def test_bounded_wait_gives_up_and_context_survives():
     s = torch.full((1, 1), 127, dtype=torch.uint8, device="cuda")
     y = bsmm.gemm(a, a, s, s, "e4m3", "e4m3", "ue8m0")
     assert y.cpu().item() == 0.0
+
+
+def test_int8_empty_batch_still_quantizes_w():
+    """B == 0: no rows of x, y is empty, and w_q / w_scales are still the
+    page's per-column codes and scales (bit-exact)."""
+    bsmm = _bsmm()
+    g = torch.Generator().manual_seed(9)
+    w = torch.randn((200, 24), generator=g).numpy()
+    w[:, 5] = 0
+    out = bsmm.int8_channel(torch.zeros((0, 200), device="cuda"), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    assert out["y"].shape == (0, 24) and bsmm.check_device_status()[0] == 0
+    ref = G.int8_channel(np.zeros((1, 200), np.float32), w)
+    np.testing.assert_array_equal(out["w_q"].cpu().numpy(), ref["w_q"])
+    np.testing.assert_array_equal(out["w_scales"].cpu().numpy().view(np.uint32), ref["w_scales"].view(np.uint32))
