@@ -71,7 +71,9 @@ def test_int8_extreme_sums_stay_exact():
 
 @pytest.mark.parametrize("kernel", ["tc", "mma"])
 @pytest.mark.parametrize("B,D_in,D_out", [(100, 300, 72), (6, 64, 8), (257, 1000, 132), (300, 4133, 264),
-                                          (520, 2048, 516), (1, 128, 4)])
+                                          (520, 2048, 516), (1, 128, 4),
+                                          # D_out % 16 == 0: the fused column-strip quantizer
+                                          (100, 300, 80), (257, 1000, 144), (300, 4133, 256), (1, 37, 16)])
 def test_int8_each_kernel(monkeypatch, kernel, B, D_in, D_out):
     """The bf16 tensor-core path (exact FP32 chunks of 1024 products added in
     int32) and the mma.sync fallback, each forced, on ragged B / D_in / D_out
