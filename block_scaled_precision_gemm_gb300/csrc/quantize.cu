@@ -417,6 +417,138 @@ __global__ void __launch_bounds__(256, 3) quant_cols(QP p, int vec_ok, int tiles
 }
 
 // ---------------------------------------------------------------------------
+// br x 1 blocks down the columns of a bf16 array, transposed output, tiles
+// streamed by TMA
+// ---------------------------------------------------------------------------
+// The same 128-row x 64-column tiles and per-tile arithmetic as quant_cols,
+// but the tiles reach shared memory through a ring of kColStages TMA loads
+// (16 KB each), so the bytes in flight no longer depend on registers, and the
+// output goes out through shared memory as whole 128-byte lines (one-byte
+// scale types: UE8M0, UE4M3).
+// Persistent CTAs take tiles b, b + gridDim.x, ...; thread 0 refills a stage
+// as soon as every thread has read it.  Waits are bounded: the CTA agrees on
+// a failure before any barrier, and waits for its own copies in flight
+// before it exits.
+constexpr int kColStages = 3;
+constexpr int kColTileBytes = kColTileR * kColTileC * 2;  // 16 KB of bf16
+constexpr int kSiteQuantTile = 21, kSiteQuantDrain = 22;
+
+template <bool POW2>
+__global__ void __launch_bounds__(256) quant_cols_tma(const __grid_constant__ CUtensorMap tm, QP p, int tiles_c,
+                                                      int64_t n_tiles, int* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t qsm_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kColStages * kColTileBytes);
+  __shared__ float pmax[4][kColTileC];
+  // the tile's output staged for whole-line stores: 64 transposed rows of
+  // 128 codes (16-byte chunks swizzled by row) and their 128/br scale bytes
+  __shared__ __align__(16) uint8_t ostg[kColTileC * kColTileR];
+  __shared__ __align__(16) uint8_t sstg[kColTileC][8];
+  __shared__ int abort_flag;
+  int never_abort_storage = 0;
+  volatile int* never_abort = &never_abort_storage;
+  const int t = threadIdx.x;
+  if (t == 0) {
+    for (int st = 0; st < kColStages; ++st) mbar_init(&full[st], 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int64_t my_n = (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  auto issue = [&](int64_t i) {  // this CTA's i-th tile into stage i % kColStages
+    const int64_t tt = blockIdx.x + i * gridDim.x;
+    const int st = static_cast<int>(i % kColStages);
+    mbar_arrive_expect_tx(&full[st], kColTileBytes);
+    tma_load_3d(ring + st * kColTileBytes, &tm, &full[st], static_cast<int>((tt % tiles_c) * kColTileC),
+                static_cast<int>((tt / tiles_c) * kColTileR), 0);
+  };
+  int64_t issued = 0;
+  if (t == 0)
+    for (; issued < my_n && issued < kColStages; ++issued) issue(issued);
+  const int col = t % kColTileC, part = t / kColTileC;
+  const int rbase = part * 32;
+  const int br = p.br;
+  int64_t i = 0;
+  for (; i < my_n; ++i) {
+    const int st = static_cast<int>(i % kColStages);
+    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>(i / kColStages) & 1u, timeout_ns, &abort_flag,
+                              status, kSiteQuantTile);
+    float v[32];  // this thread's column, rows rbase .. rbase + 31
+    if (ok) {
+      const __nv_bfloat16* tile = reinterpret_cast<const __nv_bfloat16*>(ring + st * kColTileBytes);
+#pragma unroll
+      for (int r = 0; r < 32; ++r) v[r] = __bfloat162float(tile[(rbase + r) * kColTileC + col]);
+    }
+    if (__syncthreads_or(!ok)) break;  // every thread has read stage st (or the CTA gives up together)
+    if (t == 0 && issued < my_n) issue(issued++);
+    const int64_t tt = blockIdx.x + i * gridDim.x;
+    const int64_t r0 = (tt / tiles_c) * kColTileR;
+    const int64_t c0 = (tt % tiles_c) * kColTileC;
+    const int nr = static_cast<int>(p.rows - r0 < kColTileR ? p.rows - r0 : kColTileR);
+    const int nc = static_cast<int>(p.cols - c0 < kColTileC ? p.cols - c0 : kColTileC);
+    float m0 = 0.f, m1 = 0.f;  // maxima of the two 16-row halves (rows past the array read as zero)
+#pragma unroll
+    for (int r = 0; r < 16; ++r) m0 = fmaxf(m0, fabsf(v[r]));
+#pragma unroll
+    for (int r = 16; r < 32; ++r) m1 = fmaxf(m1, fabsf(v[r]));
+    if (br > 32) {
+      pmax[part][col] = fmaxf(m0, m1);
+      __syncthreads();
+    }
+    float amax_a, amax_b;
+    if (br == 16) {
+      amax_a = m0;
+      amax_b = m1;
+    } else if (br == 32) {
+      amax_a = amax_b = fmaxf(m0, m1);
+    } else if (br == 64) {
+      const int pp = part & ~1;
+      amax_a = amax_b = fmaxf(pmax[pp][col], pmax[pp + 1][col]);
+    } else {
+      amax_a = amax_b = fmaxf(fmaxf(pmax[0][col], pmax[1][col]), fmaxf(pmax[2][col], pmax[3][col]));
+    }
+    if (br > 32) __syncthreads();  // pmax is rewritten by the next tile
+    const Scale sa = make_scale(amax_a, p.code, p.scale);
+    const Scale sb = (br == 16) ? make_scale(amax_b, p.code, p.scale) : sa;
+    {
+      uint32_t w[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        w[g] = encode4<POW2>(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3], g < 4 ? sa : sb, p.code);
+      // row `col` of the staged output, chunks 2*part and 2*part+1 (XOR-swizzled)
+      uint8_t* row = ostg + col * kColTileR;
+      *reinterpret_cast<uint4*>(row + (((2 * part) ^ (col & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(row + (((2 * part + 1) ^ (col & 7)) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+      if ((rbase % br) == 0) sstg[col][rbase / br] = static_cast<uint8_t>(sa.stored);
+      if (br == 16) sstg[col][rbase / 16 + 1] = static_cast<uint8_t>(sb.stored);
+    }
+    __syncthreads();
+    // whole-line stores: each instruction writes 4 output rows x 128 bytes
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int idx = t + 256 * k;
+      const int c = idx >> 3, ch = idx & 7;
+      if (c < nc && ch * 16 < nr)
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.codes) + (c0 + c) * p.ld_codes + r0 + ch * 16) =
+            *reinterpret_cast<const uint4*>(ostg + c * kColTileR + ((ch ^ (c & 7)) * 16));
+    }
+    if (t < nc) {  // this column's scale bytes for the tile's rows
+      const int nblk = (nr + br - 1) / br;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.scales) + (c0 + t) * p.ld_scales + r0 / br;
+      if (nblk == 4 && (reinterpret_cast<uintptr_t>(dst) & 3) == 0)
+        *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(&sstg[t][0]);
+      else
+        for (int k = 0; k < nblk; ++k) dst[k] = sstg[t][k];
+    }
+  }
+  // copies this CTA started and did not consume (only after giving up)
+  if (t == 0)
+    for (int64_t j = i; j < issued; ++j)
+      mbar_wait(&full[j % kColStages], static_cast<uint32_t>(j / kColStages) & 1u, timeout_ns, never_abort, status,
+                kSiteQuantDrain);
+}
+
+// ---------------------------------------------------------------------------
 // 128 x 128 blocks
 // ---------------------------------------------------------------------------
 template <typename In, bool POW2>
@@ -574,6 +706,22 @@ __global__ void __launch_bounds__(256) quant_any(QP p) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+template <bool POW2>
+cudaError_t launch_cols_tma(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
+  CUtensorMap tm;
+  if (!make_tmap_3d(&tm, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.cols, p.rows, 1, kColTileC, kColTileR, false))
+    return cudaErrorInvalidValue;
+  const int tiles_c = static_cast<int>(ceil_div(p.cols, kColTileC));
+  const int64_t n_tiles = static_cast<int64_t>(tiles_c) * ceil_div(p.rows, kColTileR);
+  const int smem = kColStages * kColTileBytes + 128 + kColStages * 8;
+  cudaError_t e = cudaFuncSetAttribute(quant_cols_tma<POW2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 3);
+  quant_cols_tma<POW2><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
+      tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns());
+  return cudaGetLastError();
+}
+
 template <typename In, bool POW2>
 cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
   const int esz = sizeof(In);
@@ -581,6 +729,11 @@ cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
   const bool codes16 = aligned(p.codes, 16) && p.ld_codes % 32 == 0;
   const bool pow2_small = (p.bc == 16 || p.bc == 32 || p.bc == 64 || p.bc == 128);
   const bool pow2_small_r = (p.br == 16 || p.br == 32 || p.br == 64 || p.br == 128);
+  // bf16 columns into transposed 8-bit codes (the backward's operands): TMA-fed tiles
+  const bool cols_tma = sizeof(In) == 2 && p.transpose && p.bc == 1 && pow2_small_r && p.code != BSMM_E2M1 &&
+                        p.scale != BSMM_SCALE_F32 && codes16 && p.ld_codes % 32 == 0 && p.ld_x == p.cols &&
+                        p.cols % 8 == 0 && aligned(p.x, 16);
+  if (cols_tma) return launch_cols_tma<POW2>(p, ctx, s);
   if (p.br == 1 && pow2_small && !p.transpose && x_vec && codes16) {
     int64_t blocks = ceil_div(p.rows * (p.cols / kSlice), 256 * 2);
     blocks = std::min<int64_t>(blocks, static_cast<int64_t>(ctx->num_sms) * 8);
