@@ -552,26 +552,38 @@ __global__ void __launch_bounds__(256) quant_cols_tma(const __grid_constant__ CU
 // 128 x 128 blocks
 // ---------------------------------------------------------------------------
 template <typename In, bool POW2>
+// Lane l of warp w owns columns 4l .. 4l+3 of rows w, w+8, ..., w+120: every
+// load instruction of a warp reads one whole tile row (512 bytes of FP32,
+// 256 of bf16) and every store writes that row's 128 codes.
 __global__ void __launch_bounds__(256) quant_tile(QP p) {
   __shared__ float wmax[8];
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
   const int t = threadIdx.x;
-  const int row = t >> 1, half = t & 1;  // 64 elements per thread
-  const In* x = reinterpret_cast<const In*>(p.x) + (r0 + row) * p.ld_x + c0 + half * 64;
-  float v[64];
-  constexpr int VEC = 16 / sizeof(In);
+  const int lane = t & 31, warp = t >> 5;
+  const In* x = reinterpret_cast<const In*>(p.x) + (r0 + warp) * p.ld_x + c0 + 4 * lane;
+  float v[64];  // v[4k + j]: row warp + 8k, column 4 lane + j
 #pragma unroll
-  for (int i = 0; i < 64 / VEC; ++i) {
-    float tmp[VEC];
-    load_vec<In>(x + i * VEC, tmp);
-#pragma unroll
-    for (int k = 0; k < VEC; ++k) v[i * VEC + k] = tmp[k];
+  for (int k = 0; k < 16; ++k) {
+    const In* src = x + static_cast<int64_t>(8 * k) * p.ld_x;
+    if constexpr (sizeof(In) == 4) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(src));
+      v[4 * k] = q.x;
+      v[4 * k + 1] = q.y;
+      v[4 * k + 2] = q.z;
+      v[4 * k + 3] = q.w;
+    } else {
+      const uint2 q = __ldg(reinterpret_cast<const uint2*>(src));
+      v[4 * k] = __uint_as_float(q.x << 16);
+      v[4 * k + 1] = __uint_as_float(q.x & 0xFFFF0000u);
+      v[4 * k + 2] = __uint_as_float(q.y << 16);
+      v[4 * k + 3] = __uint_as_float(q.y & 0xFFFF0000u);
+    }
   }
   float m = 0.f;
 #pragma unroll
   for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(v[i]));
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((t & 31) == 0) wmax[t >> 5] = m;
+  if (lane == 0) wmax[warp] = m;
   __syncthreads();
   m = wmax[0];
 #pragma unroll
@@ -579,20 +591,14 @@ __global__ void __launch_bounds__(256) quant_tile(QP p) {
   const Scale sc = make_scale(m, p.code, p.scale);
   if (t == 0) store_scale(p.scales, blockIdx.y * p.ld_scales + blockIdx.x, p.scale, sc.stored);
   uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
-  const int64_t e = (r0 + row) * p.ld_codes + c0 + half * 64;
-  uint32_t w[16];
 #pragma unroll
-  for (int g = 0; g < 16; ++g) w[g] = encode4<POW2>(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3], sc, p.code);
-  if (p.code == BSMM_E2M1) {
-#pragma unroll
-    for (int g = 0; g < 2; ++g)
-      *reinterpret_cast<uint4*>(out + e / 2 + 16 * g) =
-          make_uint4(w[8 * g] | (w[8 * g + 1] << 16), w[8 * g + 2] | (w[8 * g + 3] << 16),
-                     w[8 * g + 4] | (w[8 * g + 5] << 16), w[8 * g + 6] | (w[8 * g + 7] << 16));
-  } else {
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      *reinterpret_cast<uint4*>(out + e + 16 * g) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t w = encode4<POW2>(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], sc, p.code);
+    const int64_t e = (r0 + warp + 8 * k) * p.ld_codes + c0 + 4 * lane;
+    if (p.code == BSMM_E2M1)
+      *reinterpret_cast<uint16_t*>(out + e / 2) = static_cast<uint16_t>(w);
+    else
+      *reinterpret_cast<uint32_t*>(out + e) = w;
   }
 }
 
