@@ -185,8 +185,9 @@ bsmm_status bsmm_quantize(const void* x, bsmm_dtype x_type, int64_t rows, int64_
 
 size_t bsmm_gemm_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K, bsmm_dtype a_type) {
   if (B <= 0 || M <= 0 || N <= 0 || K <= 0) return 0;
-  const bool nv = a_type == BSMM_E2M1;
-  return align_up(sf_atoms_bytes(B, M, K, nv), 256) + align_up(sf_atoms_bytes(B, N, K, nv), 256);
+  // E2M1: room for NVFP4's atoms, which covers MXFP4's
+  const int fmt = a_type == BSMM_E2M1 ? kFmtNVF4 : kFmtMXF8;
+  return align_up(sf_atoms_bytes(B, M, K, fmt), 256) + align_up(sf_atoms_bytes(B, N, K, fmt), 256);
 }
 
 bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K, const void* a, bsmm_dtype a_type, const void* b,
@@ -209,9 +210,12 @@ bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K, const void* a,
                   scale_type == BSMM_SCALE_UE8M0 && bs_a == 32 && bs_b == 32;
   const bool nv = a_type == BSMM_E2M1 && b_type == BSMM_E2M1 && scale_type == BSMM_SCALE_UE4M3 && bs_a == 16 &&
                   bs_b == 16;
-  if (!mx && !nv)
+  const bool mf4 = a_type == BSMM_E2M1 && b_type == BSMM_E2M1 && scale_type == BSMM_SCALE_UE8M0 && bs_a == 32 &&
+                   bs_b == 32;
+  if (!mx && !nv && !mf4)
     return fail(BSMM_ERR_UNSUPPORTED,
-                "supported: E4M3/E5M2 with UE8M0 scales per 32, or E2M1 with UE4M3 scales per 16");
+                "supported: E4M3/E5M2 with UE8M0 scales per 32, E2M1 with UE4M3 scales per 16 (NVFP4), "
+                "or E2M1 with UE8M0 scales per 32 (MXFP4)");
   if (!a || !b || !a_scales || !b_scales || !y) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
   if (K % 32) return fail(BSMM_ERR_SHAPE, "K must be a multiple of 32");
   if (!aligned16(a) || !aligned16(b) || !aligned16(y)) return fail(BSMM_ERR_ALIGNMENT, "a, b, y must be 16-byte aligned");
@@ -222,7 +226,8 @@ bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K, const void* a,
     return fail(BSMM_ERR_WORKSPACE, "workspace must be 256-byte aligned and at least " + std::to_string(need) +
                                         " bytes");
   MxGemmRequest r{B, M, N, K, a, b, a_type, b_type, static_cast<const uint8_t*>(a_scales),
-                  static_cast<const uint8_t*>(b_scales), nv, y, y_type == BSMM_BF16, workspace};
+                  static_cast<const uint8_t*>(b_scales), nv ? kFmtNVF4 : (mf4 ? kFmtMXF4 : kFmtMXF8), y,
+                  y_type == BSMM_BF16, workspace};
   std::string why;
   const cudaError_t e = launch_mx_gemm(r, reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess && !why.empty()) return fail(BSMM_ERR_CUDA, why);
@@ -249,9 +254,12 @@ bsmm_status bsmm_gemm_noalloc(int64_t B, int64_t M, int64_t N, int64_t K, const 
                   scale_type == BSMM_SCALE_UE8M0 && bs_a == 32 && bs_b == 32;
   const bool nv = a_type == BSMM_E2M1 && b_type == BSMM_E2M1 && scale_type == BSMM_SCALE_UE4M3 && bs_a == 16 &&
                   bs_b == 16;
-  if (!mx && !nv)
+  const bool mf4 = a_type == BSMM_E2M1 && b_type == BSMM_E2M1 && scale_type == BSMM_SCALE_UE8M0 && bs_a == 32 &&
+                   bs_b == 32;
+  if (!mx && !nv && !mf4)
     return fail(BSMM_ERR_UNSUPPORTED,
-                "supported: E4M3/E5M2 with UE8M0 scales per 32, or E2M1 with UE4M3 scales per 16");
+                "supported: E4M3/E5M2 with UE8M0 scales per 32, E2M1 with UE4M3 scales per 16 (NVFP4), "
+                "or E2M1 with UE8M0 scales per 32 (MXFP4)");
   if (!a || !b || !a_scales || !b_scales || !y) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
   if (K % 32) return fail(BSMM_ERR_SHAPE, "K must be a multiple of 32");
   if (!aligned16(a) || !aligned16(b) || !aligned16(y)) return fail(BSMM_ERR_ALIGNMENT, "a, b, y must be 16-byte aligned");
@@ -264,7 +272,8 @@ bsmm_status bsmm_gemm_noalloc(int64_t B, int64_t M, int64_t N, int64_t K, const 
                                         std::to_string(BSMM_NOALLOC_SCRATCH_BYTES) +
                                         " (use bsmm_gemm with a workspace)");
   MxGemmRequest r{B, M, N, K, a, b, a_type, b_type, static_cast<const uint8_t*>(a_scales),
-                  static_cast<const uint8_t*>(b_scales), nv, y, y_type == BSMM_BF16, nullptr};
+                  static_cast<const uint8_t*>(b_scales), nv ? kFmtNVF4 : (mf4 ? kFmtMXF4 : kFmtMXF8), y,
+                  y_type == BSMM_BF16, nullptr};
   std::string why;
   const cudaError_t e = launch_mx_gemm_noalloc(r, reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess && !why.empty()) return fail(BSMM_ERR_CUDA, why);

@@ -52,7 +52,7 @@
 namespace bsmm {
 namespace {
 
-enum PairMode { kPairF32 = 0, kPairMXF8 = 1, kPairNVF4 = 2, kPairI8 = 3 };
+enum PairMode { kPairF32 = 0, kPairMXF8 = 1, kPairNVF4 = 2, kPairI8 = 3, kPairMXF4 = 4 };
 
 constexpr int PM = 256, PN = 256;          // pair tile
 constexpr int HALF = 128;                  // A rows and B rows per CTA
@@ -66,7 +66,9 @@ constexpr int A_BYTES = HALF * KB, B_BYTES = HALF * KB;
 
 template <int MODE>
 struct PCfg {
-  static constexpr int ATOMS = MODE == kPairMXF8 ? 1 : (MODE == kPairNVF4 ? 4 : 0);  // per K block per 128 rows
+  // scale-factor atoms per K block per 128 rows: MXF8 1 (128 K / 32), NVF4 4
+  // (256 K / 16), MXF4 2 (256 K / 32)
+  static constexpr int ATOMS = MODE == kPairMXF8 ? 1 : (MODE == kPairNVF4 ? 4 : (MODE == kPairMXF4 ? 2 : 0));
   static constexpr int STAGES = MODE == kPairF32 ? 3 : 4;
   // output staging per epilogue warp: 32 rows x 128 bytes per 32-column chunk
   // (kPairF32 stages both chunks of a tile; the TMA-store path reuses one)
@@ -321,10 +323,14 @@ __global__ void __launch_bounds__(THREADS, 1)
               const uint64_t ad = desc_add(a_d, 32 * k);
               const uint64_t bd = desc_add(b_d, 32 * k);
               const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
-              if constexpr (MODE == kPairMXF8) {
+              if constexpr (MODE == kPairMXF8) {  // one atom, byte k of each row's word
                 const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
                 mma_mxf8_pair(tmem, ad, bd, idesc, sfa_t, sfb_t, acc);
-              } else {
+              } else if constexpr (MODE == kPairMXF4) {  // atom k/2, bytes 2(k%2) .. 2(k%2)+1
+                const uint32_t id = static_cast<uint32_t>(2 * (k & 1));
+                mma_mxf4_pair(tmem, ad, bd, p.idesc | (id << 4) | (id << 29), sfa_t + 4 * (k >> 1),
+                              sfb_t + 8 * (k >> 1), acc);
+              } else {  // one atom per instruction
                 mma_nvf4_pair(tmem, ad, bd, p.idesc, sfa_t + 4 * k, sfb_t + 8 * k, acc);
               }
             }
@@ -674,7 +680,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-int g_pair_clusters[4][64] = {};  // max co-resident clusters per mode and device
+int g_pair_clusters[5][64] = {};  // max co-resident clusters per mode and device
 
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const CUtensorMap& tsa,
@@ -773,9 +779,9 @@ bool mx_pair_eligible(const MxGemmRequest& r, const DeviceCtx* ctx) {
 cudaError_t launch_mx_gemm_pair(const MxGemmRequest& r, const MxAtoms& at, cudaStream_t s, std::string* why) {
   const DeviceCtx* ctx = device_ctx();
   if (!ctx) return cudaErrorInitializationError;
-  const bool nv = r.nvf4;
-  const int atoms = nv ? 4 : 1;
-  const int64_t kbytes = nv ? r.K / 2 : r.K;
+  const bool nv = r.fmt == kFmtNVF4, mf4 = r.fmt == kFmtMXF4;
+  const int atoms = nv ? 4 : (mf4 ? 2 : 1);
+  const int64_t kbytes = (nv || mf4) ? r.K / 2 : r.K;
   const int64_t sfa_rows = r.B * static_cast<int64_t>(at.sfa_rt) * at.ks4 * 4;  // 128-byte rows
   const int64_t sfb_rows = r.B * static_cast<int64_t>(at.sfb_rt) * at.ks4 * 4;
   CUtensorMap ta, tb, ty, tsa, tsb;
@@ -809,6 +815,12 @@ cudaError_t launch_mx_gemm_pair(const MxGemmRequest& r, const MxAtoms& at, cudaS
     // kind::mxf4nvf4: E2M1 = 1 for A and B, UE4M3 scales (bit 23 = 0), N = 256, M = 256 (pair).
     p.idesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(PN >> 3) << 17) | (static_cast<uint32_t>(PM >> 4) << 24);
     return launch_pair<kPairNVF4>(ta, tb, ty, tsa, tsb, p, ctx, s, why);
+  }
+  if (mf4) {
+    // kind::mxf4nvf4 .block32: E2M1 = 1 for A and B, UE8M0 scales (bit 23 = 1), N = 256, M = 256 (pair).
+    p.idesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(PN >> 3) << 17) | (1u << 23) |
+              (static_cast<uint32_t>(PM >> 4) << 24);
+    return launch_pair<kPairMXF4>(ta, tb, ty, tsa, tsb, p, ctx, s, why);
   }
   // kind::mxf8f6f4: E4M3 = 0 / E5M2 = 1, UE8M0 scales (bit 23 = 1), N = 256, M = 256 (pair).
   p.idesc = (f8_code(r.a_fmt) << 7) | (f8_code(r.b_fmt) << 10) | (static_cast<uint32_t>(PN >> 3) << 17) | (1u << 23) |

@@ -550,9 +550,11 @@ bool make_output_map(CUtensorMap* ty, void* y, bool bf16, int64_t B, int64_t M, 
 
 }  // namespace
 
-size_t sf_atoms_bytes(int64_t B, int64_t R, int64_t K, bool nvf4) {
-  const int64_t k_tiles = ceil_div(K, nvf4 ? 256 : 128);
-  const int64_t ks4 = k_tiles * (nvf4 ? 4 : 1);
+size_t sf_atoms_bytes(int64_t B, int64_t R, int64_t K, int fmt) {
+  // K per 128-byte tile: 128 FP8 or 256 FP4 elements; atoms per tile: one per
+  // 4 scales (MXF8 1, NVF4 4, MXF4 2)
+  const int64_t k_tiles = ceil_div(K, fmt == kFmtMXF8 ? 128 : 256);
+  const int64_t ks4 = k_tiles * (fmt == kFmtNVF4 ? 4 : (fmt == kFmtMXF4 ? 2 : 1));
   return static_cast<size_t>(B) * rt_rows(R) * ks4 * 512;
 }
 
@@ -560,15 +562,15 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
   const DeviceCtx* ctx = device_ctx();
   if (!ctx) return cudaErrorInitializationError;
   constexpr int BN = 128;
-  const bool nv = r.nvf4;
-  const int64_t k_tiles = ceil_div(r.K, nv ? 256 : 128);
-  const int ks4 = static_cast<int>(k_tiles * (nv ? 4 : 1));
+  const bool nv = r.fmt == kFmtNVF4, mf4 = r.fmt == kFmtMXF4;
+  const int64_t k_tiles = ceil_div(r.K, (nv || mf4) ? 256 : 128);
+  const int ks4 = static_cast<int>(k_tiles * (nv ? 4 : (mf4 ? 2 : 1)));
   const int KS = static_cast<int>(r.K / (nv ? 16 : 32));
   uint8_t* ws = reinterpret_cast<uint8_t*>(r.workspace);
-  const size_t a_bytes = align_up(sf_atoms_bytes(r.B, r.M, r.K, nv), 256);
+  const size_t a_bytes = align_up(sf_atoms_bytes(r.B, r.M, r.K, r.fmt), 256);
   uint8_t* sfa = ws;
   uint8_t* sfb = ws + a_bytes;
-  const uint32_t pad = nv ? 0u : 127u;
+  const uint32_t pad = nv ? 0u : 127u;  // scale 1 for UE8M0 blocks past K (their codes are zero)
   {
     const int RT = rt_rows(r.M);
     const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
@@ -594,7 +596,11 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
   const bool want_single = force && std::strcmp(force, "single") == 0;
   const int esz = r.y_bf16 ? 2 : 4;
   const bool storable = (r.N * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(r.y) % 16 == 0;
-  if (!want_single && (want_pair ? storable : mx_pair_eligible(r, ctx))) {
+  if (mf4 && !storable) {  // MXFP4 has only the pair kernel
+    *why = "MXFP4 output rows must be 16-byte aligned (N * element size % 16 == 0)";
+    return cudaErrorInvalidValue;
+  }
+  if (mf4 || (!want_single && (want_pair ? storable : mx_pair_eligible(r, ctx)))) {
     const MxAtoms at{sfa, sfb, rt_rows(r.M), rt_rows(r.N), ks4, static_cast<int>(k_tiles)};
     return launch_mx_gemm_pair(r, at, s, why);
   }

@@ -49,8 +49,10 @@ struct QuantRequest {
 };
 cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s);
 
+// Block-scaled formats of bsmm_gemm.
+enum MxFormat { kFmtMXF8 = 0, kFmtNVF4 = 1, kFmtMXF4 = 2 };
 // Scale relayout into the tensor-core scale-factor atoms (see gemm_tc.cu).
-size_t sf_atoms_bytes(int64_t B, int64_t R, int64_t K, bool nvf4);
+size_t sf_atoms_bytes(int64_t B, int64_t R, int64_t K, int fmt);
 
 struct MxGemmRequest {
   int64_t B, M, N, K;
@@ -59,7 +61,7 @@ struct MxGemmRequest {
   int a_fmt, b_fmt;  // bsmm_dtype
   const uint8_t* a_scales;
   const uint8_t* b_scales;
-  bool nvf4;
+  int fmt;  // MxFormat
   void* y;
   bool y_bf16;
   void* workspace;

@@ -323,6 +323,18 @@ __device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc, u
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// MXFP4 on a CTA pair: packed E2M1 operands, UE8M0 scale per 32 K (two
+// scales per row per K = 64 instruction, selected by the descriptor's
+// scale-factor ids).
+__device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.block32 [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 // Scale-factor copy (32 rows x 128 bits, replicated to the four lane
 // quarters) issued by the leader of a CTA pair: each CTA's tensor memory
 // receives the atom at the same shared-memory offset of that CTA.

@@ -164,6 +164,8 @@ bsmm_status bsmm_quantize(const void* x, bsmm_dtype x_type, int64_t rows, int64_
  *   MXFP8: a_type, b_type in {E4M3, E5M2} (may differ), scale_type UE8M0,
  *          bs_a = bs_b = 32.
  *   NVFP4: a_type = b_type = E2M1, scale_type UE4M3, bs_a = bs_b = 16.
+ *   MXFP4: a_type = b_type = E2M1, scale_type UE8M0, bs_a = bs_b = 32 (the
+ *          OCP MX block; its kernel needs N * sizeof(y element) % 16 == 0).
  * Other combinations return BSMM_ERR_UNSUPPORTED.
  *
  *   a        [B, M, K] codes, contiguous (E2M1: K/2 bytes per row).

@@ -56,6 +56,11 @@ def test_validation_without_gpu(lib):
                        fake, 1 << 20, None)
     assert st == b.ERR_UNSUPPORTED
     assert b"UE8M0" in lib.bsmm_last_error()
+    # E2M1 takes UE4M3 per 16 (NVFP4) or UE8M0 per 32 (MXFP4), not the other pairings
+    for scale, K_s in ((b.SCALE_UE8M0, 16), (b.SCALE_UE4M3, 8)):
+        st = lib.bsmm_gemm(1, 128, 128, 256, fake, b.E2M1, fake, b.E2M1, fake, K_s, fake, K_s, scale, fake, b.F32,
+                           fake, 1 << 20, None)
+        assert st == b.ERR_UNSUPPORTED
     # grouped: n not a multiple of group_n; group other than 128
     assert lib.bsmm_gemm_grouped(64, 200, 256, fake, b.E4M3, fake, b.E4M3, fake, fake, 128, 128, fake,
                                  None) == b.ERR_SHAPE

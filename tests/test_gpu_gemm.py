@@ -305,3 +305,50 @@ def test_batched_empty_output_is_a_no_op(Bn, M, N):
     y = bsmm.gemm(a, b, sa, sb, "e4m3", "e4m3", "ue8m0")
     torch.cuda.synchronize()
     assert y.shape == (Bn, M, N) and bsmm.check_device_status()[0] == 0
+
+
+# ---------------------------------------------------------------------------
+# MXFP4: E2M1 codes with a UE8M0 scale per 32 elements (jax.nn.scaled_matmul's
+# definition with the OCP MX block of 32; CTA-pair kernel only)
+# ---------------------------------------------------------------------------
+
+def mxf4_inputs(Bn, M, N, K, seed, pattern="random"):
+    g = torch.Generator().manual_seed(seed)
+    a = torch.randint(0, 256, (Bn, M, K // 2), generator=g, dtype=torch.int32).numpy().astype(np.uint8)
+    b = torch.randint(0, 256, (Bn, N, K // 2), generator=g, dtype=torch.int32).numpy().astype(np.uint8)
+    ea = torch.randint(-6, 7, (Bn, M, K // 32), generator=g).numpy()
+    eb = torch.randint(-6, 7, (Bn, N, K // 32), generator=g).numpy()
+    ks = K // 32
+    if pattern == "one_hot_a":  # row m keeps only K block (5m+1) % ks
+        ea = np.full_like(ea, -127)
+        for r in range(M):
+            ea[:, r, (5 * r + 1) % ks] = (r % 5) - 2
+    elif pattern == "one_hot_b":
+        eb = np.full_like(eb, -127)
+        for r in range(N):
+            eb[:, r, (3 * r + 2) % ks] = (r % 3) - 1
+    return a, b, (ea + 127).astype(np.uint8), (eb + 127).astype(np.uint8)
+
+
+@pytest.mark.parametrize("Bn,M,N,K,out,pattern", [
+    (1, 256, 256, 256, torch.float32, "random"),
+    (2, 200, 136, 512, torch.float32, "random"),
+    (1, 512, 384, 1024, torch.float32, "random"),
+    (3, 300, 520, 768, torch.bfloat16, "random"),
+    (1, 1, 256, 96, torch.float32, "random"),
+    (1, 512, 512, 1024, torch.float32, "one_hot_a"),
+    (1, 512, 512, 1024, torch.float32, "one_hot_b"),
+])
+def test_mxfp4_parity(Bn, M, N, K, out, pattern):
+    bsmm = _bsmm()
+    a, b, sa, sb = mxf4_inputs(Bn, M, N, K, seed=M + N + K, pattern=pattern)
+    t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()  # noqa: E731
+    y = bsmm.gemm(t(a), t(b), t(sa), t(sb), "e2m1", "e2m1", "ue8m0", out_dtype=out)
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    da, db = F.decode(F.unpack_e2m1(a), "e2m1"), F.decode(F.unpack_e2m1(b), "e2m1")
+    dsa, dsb = F.decode(sa, "ue8m0"), F.decode(sb, "ue8m0")
+    y_ref = G.scaled_matmul(da, db, dsa, dsb)
+    bound = G.scaled_matmul_bound(da, db, dsa, dsb)
+    assert_within(y.float().cpu().numpy(), y_ref, bound, f"mxfp4 {Bn}x{M}x{N}x{K} {pattern}",
+                  G.BF16_HALF_ULP if out == torch.bfloat16 else 0.0)
