@@ -7,7 +7,8 @@ whole hot path for all eight problems on inputs already in HBM: quantize the
 float32 activations per 1x128 block, quantize the float32 weights per
 128x128 block, and the FP32-scale GEMM.  Metric: TFLOPS = sum(2mnk) / step
 time.  Other workloads (--workload) are the remaining configurations:
-small block_scaled_mm, int8 per-channel, mxfp8, nvfp4, mxfp8 backward.
+small block_scaled_mm, int8 per-channel, mxfp8, nvfp4, mxfp8 backward, and mxfp4 (the
+next format, at the nvfp4 size).
 
 Prints one JSON line (rank 0).  With --impl reference the CPU oracle runs a
 bounded sample of the same workload on the host cores instead.
@@ -327,6 +328,14 @@ class MxWork(Work):
             self.sb = (raw[3] + 127).to(torch.uint8)
             self.types = ("e4m3", "e4m3", "ue8m0")
             self.dominant = "MXFP8 block-scaled GEMM call (sf_relayout + tc_gemm_pair kPairMXF8)"
+        elif p.fmt == "mxfp4":
+            self.a, self.b = raw[0], raw[1]
+            self.sa = (raw[2] + 127).to(torch.uint8)
+            self.sb = (raw[3] + 127).to(torch.uint8)
+            self.types = ("e2m1", "e2m1", "ue8m0")
+            self.peak_kind = "fp4"
+            self.dtype = "e2m1 (f32 accumulate)"
+            self.dominant = "MXFP4 block-scaled GEMM call (sf_relayout + tc_gemm_pair kPairMXF4)"
         else:
             self.a, self.b = raw[0], raw[1]
             self.sa = raw[2].to(torch.float8_e4m3fn).view(torch.uint8)
@@ -582,6 +591,13 @@ def oracle_sample(workload: W.Workload, rows: int):
             sb = torch.randint(121, 134, (1, 128, p.K // 32), generator=g).numpy().astype(np.uint8)
             run = lambda: G.scaled_matmul(F.decode(a, "e4m3"), F.decode(b, "e4m3"), F.decode(sa, "ue8m0"),  # noqa
                                           F.decode(sb, "ue8m0"))
+        elif p.fmt == "mxfp4":
+            a = torch.randint(0, 256, (1, r, p.K // 2), generator=g).numpy().astype(np.uint8)
+            b = torch.randint(0, 256, (1, 128, p.K // 2), generator=g).numpy().astype(np.uint8)
+            sa = torch.randint(121, 134, (1, r, p.K // 32), generator=g).numpy().astype(np.uint8)
+            sb = torch.randint(121, 134, (1, 128, p.K // 32), generator=g).numpy().astype(np.uint8)
+            run = lambda: G.scaled_matmul(F.decode(F.unpack_e2m1(a), "e2m1"), F.decode(F.unpack_e2m1(b), "e2m1"),  # noqa
+                                          F.decode(sa, "ue8m0"), F.decode(sb, "ue8m0"))
         else:
             a = torch.randint(0, 256, (1, r, p.K // 2), generator=g).numpy().astype(np.uint8)
             b = torch.randint(0, 256, (1, 128, p.K // 2), generator=g).numpy().astype(np.uint8)
@@ -671,7 +687,8 @@ def selected_workload(args) -> W.Workload:
 
 
 WORKLOADS_BY_KEY = {"sweep": W.GROUPED_SWEEP, "small": W.GROUPED_SMALL, "int8": W.INT8_4096,
-                    "mxfp8": W.MXFP8_BATCHED, "nvfp4": W.NVFP4_SQUARE, "backward": W.BACKWARD}
+                    "mxfp8": W.MXFP8_BATCHED, "nvfp4": W.NVFP4_SQUARE, "mxfp4": W.MXFP4_SQUARE,
+                    "backward": W.BACKWARD}
 
 
 def main(argv=None):

@@ -111,9 +111,10 @@ def test_int8_per_channel_sampled(device):
     _free()
 
 
-@pytest.mark.parametrize("workload", [W.MXFP8_BATCHED, W.NVFP4_SQUARE], ids=["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("workload", [W.MXFP8_BATCHED, W.NVFP4_SQUARE, W.MXFP4_SQUARE],
+                         ids=["mxfp8", "nvfp4", "mxfp4"])
 def test_batched_scaled_matmul_sampled(device, workload):
-    """MXFP8 B=8 x 4096 x 4096 x 8192 and NVFP4 16384^3, one bench step."""
+    """MXFP8 B=8 x 4096 x 4096 x 8192, NVFP4 and MXFP4 16384^3, one bench step."""
     import block_scaled_precision_gemm_gb300 as bsmm
     wl = bench.MxWork(workload, device)
     wl.step()
@@ -130,6 +131,9 @@ def test_batched_scaled_matmul_sampled(device, workload):
     sa, sb = wl.sa[idx_a].cpu().numpy(), wl.sb[idx_b].cpu().numpy()
     if p.fmt == "mxfp8":
         da, db = F.decode(a, "e4m3"), F.decode(b, "e4m3")
+        dsa, dsb = F.decode(sa, "ue8m0"), F.decode(sb, "ue8m0")
+    elif p.fmt == "mxfp4":
+        da, db = F.decode(F.unpack_e2m1(a), "e2m1"), F.decode(F.unpack_e2m1(b), "e2m1")
         dsa, dsb = F.decode(sa, "ue8m0"), F.decode(sb, "ue8m0")
     else:
         da, db = F.decode(F.unpack_e2m1(a), "e2m1"), F.decode(F.unpack_e2m1(b), "e2m1")

@@ -86,10 +86,13 @@ GROUPED_SWEEP = Workload(
     + tuple(Grouped(m, 4096, 4096) for m in (237, 4096, 65536, 299520)))
 MXFP8_BATCHED = Workload("mxfp8 B=8 M=N=4096 K=8192", 3, (Batched(8, 4096, 4096, 8192, "mxfp8"),))
 NVFP4_SQUARE = Workload("nvfp4 B=1 M=N=K=16384", 3, (Batched(1, 16384, 16384, 16384, "nvfp4"),))
+# MXFP4 (E2M1 with UE8M0 per 32) at the NVFP4 problem's size; not one of the
+# pages' published configurations, measured as the next format.
+MXFP4_SQUARE = Workload("mxfp4 B=1 M=N=K=16384", 3, (Batched(1, 16384, 16384, 16384, "mxfp4"),))
 BACKWARD = Workload("mxfp8 linear backward M=16384 N=K=8192", 4, (Backward(16384, 8192, 8192),))
 
 WORKLOADS = {w.name: w for w in (GROUPED_SMALL, INT8_4096, GROUPED_SWEEP,
-                                 MXFP8_BATCHED, NVFP4_SQUARE, BACKWARD)}
+                                 MXFP8_BATCHED, NVFP4_SQUARE, MXFP4_SQUARE, BACKWARD)}
 
 
 # --------------------------------------------------------------------------- #
@@ -181,6 +184,12 @@ def batched_raw(p: Batched, seed: int, device="cpu"):
         sa = log_uniform((p.B, p.M, p.K // 16), -4, 4, seed, S_A_SCALE, device)
         sb = log_uniform((p.B, p.N, p.K // 16), -4, 4, seed, S_B_SCALE, device)
         return a, b, sa, sb
+    if p.fmt == "mxfp4":  # E2M1 code bytes as for nvfp4, exponents as for mxfp8
+        a = random_bytes((p.B, p.M, p.K // 2), seed, S_A, device)
+        b = random_bytes((p.B, p.N, p.K // 2), seed, S_B, device)
+        ea = uniform_int((p.B, p.M, p.K // 32), -6, 6, seed, S_A_SCALE, device)
+        eb = uniform_int((p.B, p.N, p.K // 32), -6, 6, seed, S_B_SCALE, device)
+        return a, b, ea, eb
     raise ValueError(p.fmt)
 
 
