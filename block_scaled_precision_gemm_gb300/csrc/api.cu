@@ -106,6 +106,28 @@ bsmm_status launched(cudaError_t e, const char* what) {
   return BSMM_OK;
 }
 
+// Which kernel a bsmm_gemm problem takes.  The tensor cores scale per 32
+// elements (UE8M0: MXFP8, MXFP4) or 16 (UE4M3 with E2M1: NVFP4); a block that
+// is a multiple of that repeats its scale there.  Any other block size, and
+// FP8 codes with UE4M3 scales, run on the CUDA-core kernel.
+struct GemmRoute {
+  bool ok, tensor;
+  int fmt;  // MxFormat, for the tensor path
+  const char* why;
+};
+GemmRoute route_gemm(int at, int bt, int st, int64_t K, int64_t K_a, int64_t K_b) {
+  const bool fp8 = (at == BSMM_E4M3 || at == BSMM_E5M2) && (bt == BSMM_E4M3 || bt == BSMM_E5M2);
+  const bool fp4 = at == BSMM_E2M1 && bt == BSMM_E2M1;
+  if (!(fp8 || fp4) || (st != BSMM_SCALE_UE8M0 && st != BSMM_SCALE_UE4M3))
+    return {false, false, 0, "codes E4M3/E5M2 (both operands) or E2M1 (both), scales UE8M0 or UE4M3"};
+  if (fp4 && K % 2) return {false, false, 0, "E2M1 codes need an even K"};
+  const int64_t bs_a = K / K_a, bs_b = K / K_b;
+  const int64_t hw = (fp4 && st == BSMM_SCALE_UE4M3) ? 16 : 32;
+  const bool tensor = (fp4 || st == BSMM_SCALE_UE8M0) && bs_a % hw == 0 && bs_b % hw == 0 && K % 32 == 0;
+  const int fmt = fp8 ? kFmtMXF8 : (st == BSMM_SCALE_UE4M3 ? kFmtNVF4 : kFmtMXF4);
+  return {true, tensor, fmt, ""};
+}
+
 }  // namespace
 
 extern "C" {
@@ -205,19 +227,17 @@ bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K, const void* a,
     return BSMM_OK;
   }
   if (K == 0) return fail(BSMM_ERR_UNSUPPORTED, "K == 0");
-  const int64_t bs_a = K / K_a, bs_b = K / K_b;
-  const bool mx = (a_type == BSMM_E4M3 || a_type == BSMM_E5M2) && (b_type == BSMM_E4M3 || b_type == BSMM_E5M2) &&
-                  scale_type == BSMM_SCALE_UE8M0 && bs_a == 32 && bs_b == 32;
-  const bool nv = a_type == BSMM_E2M1 && b_type == BSMM_E2M1 && scale_type == BSMM_SCALE_UE4M3 && bs_a == 16 &&
-                  bs_b == 16;
-  const bool mf4 = a_type == BSMM_E2M1 && b_type == BSMM_E2M1 && scale_type == BSMM_SCALE_UE8M0 && bs_a == 32 &&
-                   bs_b == 32;
-  if (!mx && !nv && !mf4)
-    return fail(BSMM_ERR_UNSUPPORTED,
-                "supported: E4M3/E5M2 with UE8M0 scales per 32, E2M1 with UE4M3 scales per 16 (NVFP4), "
-                "or E2M1 with UE8M0 scales per 32 (MXFP4)");
+  const GemmRoute route = route_gemm(a_type, b_type, scale_type, K, K_a, K_b);
+  if (!route.ok) return fail(BSMM_ERR_UNSUPPORTED, route.why);
   if (!a || !b || !a_scales || !b_scales || !y) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
-  if (K % 32) return fail(BSMM_ERR_SHAPE, "K must be a multiple of 32");
+  if (!route.tensor) {  // a block size the tensor cores do not scale by
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2 || B > 65535)
+      return fail(BSMM_ERR_SHAPE, "size beyond the supported range");
+    MxGemmRequest g{B, M, N, K, a, b, a_type, b_type, static_cast<const uint8_t*>(a_scales),
+                    static_cast<const uint8_t*>(b_scales), route.fmt, y, y_type == BSMM_BF16, nullptr, K_a, K_b};
+    return launched(launch_mx_gemm_generic(g, K_a, K_b, scale_type, reinterpret_cast<cudaStream_t>(stream)),
+                    "gemm (generic block) launch");
+  }
   if (!aligned16(a) || !aligned16(b) || !aligned16(y)) return fail(BSMM_ERR_ALIGNMENT, "a, b, y must be 16-byte aligned");
   if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2 || B > 65535)
     return fail(BSMM_ERR_SHAPE, "size beyond the supported range");
@@ -226,8 +246,7 @@ bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K, const void* a,
     return fail(BSMM_ERR_WORKSPACE, "workspace must be 256-byte aligned and at least " + std::to_string(need) +
                                         " bytes");
   MxGemmRequest r{B, M, N, K, a, b, a_type, b_type, static_cast<const uint8_t*>(a_scales),
-                  static_cast<const uint8_t*>(b_scales), nv ? kFmtNVF4 : (mf4 ? kFmtMXF4 : kFmtMXF8), y,
-                  y_type == BSMM_BF16, workspace};
+                  static_cast<const uint8_t*>(b_scales), route.fmt, y, y_type == BSMM_BF16, workspace, K_a, K_b};
   std::string why;
   const cudaError_t e = launch_mx_gemm(r, reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess && !why.empty()) return fail(BSMM_ERR_CUDA, why);
@@ -249,19 +268,17 @@ bsmm_status bsmm_gemm_noalloc(int64_t B, int64_t M, int64_t N, int64_t K, const 
     return BSMM_OK;
   }
   if (K == 0) return fail(BSMM_ERR_UNSUPPORTED, "K == 0");
-  const int64_t bs_a = K / K_a, bs_b = K / K_b;
-  const bool mx = (a_type == BSMM_E4M3 || a_type == BSMM_E5M2) && (b_type == BSMM_E4M3 || b_type == BSMM_E5M2) &&
-                  scale_type == BSMM_SCALE_UE8M0 && bs_a == 32 && bs_b == 32;
-  const bool nv = a_type == BSMM_E2M1 && b_type == BSMM_E2M1 && scale_type == BSMM_SCALE_UE4M3 && bs_a == 16 &&
-                  bs_b == 16;
-  const bool mf4 = a_type == BSMM_E2M1 && b_type == BSMM_E2M1 && scale_type == BSMM_SCALE_UE8M0 && bs_a == 32 &&
-                   bs_b == 32;
-  if (!mx && !nv && !mf4)
-    return fail(BSMM_ERR_UNSUPPORTED,
-                "supported: E4M3/E5M2 with UE8M0 scales per 32, E2M1 with UE4M3 scales per 16 (NVFP4), "
-                "or E2M1 with UE8M0 scales per 32 (MXFP4)");
+  const GemmRoute route = route_gemm(a_type, b_type, scale_type, K, K_a, K_b);
+  if (!route.ok) return fail(BSMM_ERR_UNSUPPORTED, route.why);
   if (!a || !b || !a_scales || !b_scales || !y) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
-  if (K % 32) return fail(BSMM_ERR_SHAPE, "K must be a multiple of 32");
+  if (!route.tensor) {  // a block size the tensor cores do not scale by
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2 || B > 65535)
+      return fail(BSMM_ERR_SHAPE, "size beyond the supported range");
+    MxGemmRequest g{B, M, N, K, a, b, a_type, b_type, static_cast<const uint8_t*>(a_scales),
+                    static_cast<const uint8_t*>(b_scales), route.fmt, y, y_type == BSMM_BF16, nullptr, K_a, K_b};
+    return launched(launch_mx_gemm_generic(g, K_a, K_b, scale_type, reinterpret_cast<cudaStream_t>(stream)),
+                    "gemm (generic block) launch");
+  }
   if (!aligned16(a) || !aligned16(b) || !aligned16(y)) return fail(BSMM_ERR_ALIGNMENT, "a, b, y must be 16-byte aligned");
   if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2 || B > 65535)
     return fail(BSMM_ERR_SHAPE, "size beyond the supported range");
@@ -272,8 +289,7 @@ bsmm_status bsmm_gemm_noalloc(int64_t B, int64_t M, int64_t N, int64_t K, const 
                                         std::to_string(BSMM_NOALLOC_SCRATCH_BYTES) +
                                         " (use bsmm_gemm with a workspace)");
   MxGemmRequest r{B, M, N, K, a, b, a_type, b_type, static_cast<const uint8_t*>(a_scales),
-                  static_cast<const uint8_t*>(b_scales), nv ? kFmtNVF4 : (mf4 ? kFmtMXF4 : kFmtMXF8), y,
-                  y_type == BSMM_BF16, nullptr};
+                  static_cast<const uint8_t*>(b_scales), route.fmt, y, y_type == BSMM_BF16, nullptr, K_a, K_b};
   std::string why;
   const cudaError_t e = launch_mx_gemm_noalloc(r, reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess && !why.empty()) return fail(BSMM_ERR_CUDA, why);
@@ -411,11 +427,11 @@ bsmm_status bsmm_linear_backward(const void* dY, const void* W, const void* X, i
   }
   std::string why;
   // dX [M, K] = dY [M, N] . (W^T [K, N])^T, contraction over N
-  MxGemmRequest g1{1, M, K, N, dy_n, wt, ft, ft, dy_n_s, wt_s, false, dX, true, gws};
+  MxGemmRequest g1{1, M, K, N, dy_n, wt, ft, ft, dy_n_s, wt_s, kFmtMXF8, dX, true, gws, N / 32, N / 32};
   cudaError_t e = launch_mx_gemm(g1, s, &why);
   if (e != cudaSuccess) return why.empty() ? cuda_fail(e, "dX gemm launch") : fail(BSMM_ERR_CUDA, why);
   // dW [N, K] = dY^T [N, M] . (X^T [K, M])^T, contraction over M
-  MxGemmRequest g2{1, N, K, M, dyt, xt, ft, ft, dyt_s, xt_s, false, dW, true, gws};
+  MxGemmRequest g2{1, N, K, M, dyt, xt, ft, ft, dyt_s, xt_s, kFmtMXF8, dW, true, gws, M / 32, M / 32};
   e = launch_mx_gemm(g2, s, &why);
   if (e != cudaSuccess) return why.empty() ? cuda_fail(e, "dW gemm launch") : fail(BSMM_ERR_CUDA, why);
   (void)gws_bytes;

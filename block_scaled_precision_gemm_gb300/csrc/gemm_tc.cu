@@ -454,10 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Scale bytes [batch][rows][KS] (row-major, one per K block) -> atoms of the
-// tensor-core scale-factor layout: atom (b, row tile rt, K atom j) is 512
-// bytes; byte (r%32)*16 + ((r%128)/32)*4 + (kb%4) holds the scale of row
-// rt*128 + r for K block 4j + kb%4.  Missing rows / blocks get `pad`.
+// Scale bytes [batch][rows][KSu] (row-major, one per user block of `rep`
+// hardware blocks) -> atoms of the tensor-core scale-factor layout: atom
+// (b, row tile rt, K atom j) is 512 bytes; byte (r%32)*16 + ((r%128)/32)*4 +
+// (kb%4) holds the scale of row rt*128 + r for hardware K block 4j + kb%4,
+// i.e. user scale (4j + kb%4) / rep.  Missing rows / blocks get `pad`.
 // A thread owns word w of eight consecutive atoms j0..j0+7 of one row tile:
 // it reads the 32 scale bytes of row rt*128 + (w>>2) + 32*(w&3) for K blocks
 // 4*j0 .. 4*j0+31 (two 16-byte loads when in range and aligned) and writes
@@ -465,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The 16-byte loads need KS % 16 == 0 and a 16-byte aligned base; otherwise
 // (and at the K tail) the bytes are read one by one.
 __global__ void __launch_bounds__(256) sf_relayout(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst,
-                                                   int nb, int R, int KS, int RT, int KS4, uint32_t pad) {
+                                                   int nb, int R, int KS, int RT, int KS4, uint32_t pad, int KSu,
+                                                   int rep) {
   const int groups = (KS4 + 7) / 8;  // groups of eight atoms per row tile
   const int64_t total = static_cast<int64_t>(nb) * RT * groups * 128;
   const uint32_t pad4 = pad * 0x01010101u;
@@ -484,8 +486,8 @@ __global__ void __launch_bounds__(256) sf_relayout(const uint8_t* __restrict__ s
 #pragma unroll
       for (int i = 0; i < 8; ++i) word[i] = pad4;
     } else {
-      const uint8_t* row = src + (b * R + r) * static_cast<int64_t>(KS);
-      if (kb0 + 32 <= KS && (KS & 15) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      const uint8_t* row = src + (b * R + r) * static_cast<int64_t>(KSu);
+      if (rep == 1 && kb0 + 32 <= KS && (KS & 15) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
         const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(row + kb0));
         const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(row + kb0 + 16));
         word[0] = v0.x; word[1] = v0.y; word[2] = v0.z; word[3] = v0.w;
@@ -497,7 +499,7 @@ __global__ void __launch_bounds__(256) sf_relayout(const uint8_t* __restrict__ s
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int kb = kb0 + 4 * i + k;
-            v |= static_cast<uint32_t>(kb < KS ? row[kb] : pad) << (8 * k);
+            v |= static_cast<uint32_t>(kb < KS ? row[kb / rep] : pad) << (8 * k);
           }
           word[i] = v;
         }
@@ -576,14 +578,16 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
     const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
     const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
     sf_relayout<<<blocks, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
-                                       static_cast<int>(r.M), KS, RT, ks4, pad);
+                                       static_cast<int>(r.M), KS, RT, ks4, pad, static_cast<int>(r.K_a),
+                                       static_cast<int>(KS / r.K_a));
   }
   {
     const int RT = rt_rows(r.N);
     const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
     const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
     sf_relayout<<<blocks, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
-                                       static_cast<int>(r.N), KS, RT, ks4, pad);
+                                       static_cast<int>(r.N), KS, RT, ks4, pad, static_cast<int>(r.K_b),
+                                       static_cast<int>(KS / r.K_b));
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

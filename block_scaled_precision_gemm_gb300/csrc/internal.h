@@ -65,7 +65,14 @@ struct MxGemmRequest {
   void* y;
   bool y_bf16;
   void* workspace;
+  // scales per row as given (K_a, K_b): a user block may span several
+  // hardware blocks (32 elements for UE8M0, 16 for UE4M3), which then repeat
+  // its scale
+  int64_t K_a, K_b;
 };
+// Any block size, CUDA cores (gemm_generic.cu); no workspace.
+cudaError_t launch_mx_gemm_generic(const MxGemmRequest& r, int64_t K_a, int64_t K_b, int scale_type,
+                                   cudaStream_t s);
 cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* why);
 // Same, with the scale-factor atoms in the library's static device array.
 cudaError_t launch_mx_gemm_noalloc(const MxGemmRequest& r, cudaStream_t s, std::string* why);

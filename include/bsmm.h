@@ -160,13 +160,18 @@ bsmm_status bsmm_quantize(const void* x, bsmm_dtype x_type, int64_t rows, int64_
  * with bs_a = K/K_a and bs_b = K/K_b inferred from the scale counts, FP32
  * accumulation ([JAX] "Mathematically" definition and Parameters).
  *
- * Supported formats ([JAX] Notes, cuDNN on Blackwell):
- *   MXFP8: a_type, b_type in {E4M3, E5M2} (may differ), scale_type UE8M0,
- *          bs_a = bs_b = 32.
- *   NVFP4: a_type = b_type = E2M1, scale_type UE4M3, bs_a = bs_b = 16.
- *   MXFP4: a_type = b_type = E2M1, scale_type UE8M0, bs_a = bs_b = 32 (the
- *          OCP MX block; its kernel needs N * sizeof(y element) % 16 == 0).
- * Other combinations return BSMM_ERR_UNSUPPORTED.
+ * Codes: a_type, b_type both in {E4M3, E5M2} (they may differ) or both
+ * E2M1; scales UE8M0 or UE4M3; any block sizes bs_a, bs_b.  The tensor cores
+ * take ([JAX] Notes, cuDNN on Blackwell):
+ *   MXFP8: FP8 codes, UE8M0 scales, blocks that are multiples of 32.
+ *   NVFP4: E2M1 codes, UE4M3 scales, blocks that are multiples of 16.
+ *   MXFP4: E2M1 codes, UE8M0 scales, blocks that are multiples of 32 (this
+ *          kernel needs N * sizeof(y element) % 16 == 0).
+ * (a block of several hardware blocks repeats its scale; K must be a
+ * multiple of 32).  Every other combination -- e.g. the jax cuDNN example's
+ * UE8M0 scales per 16 FP8 elements, or FP8 codes with UE4M3 scales -- runs
+ * on a CUDA-core kernel (decode, scale, FP32 FMA; no workspace needed).
+ * Other code or scale types return BSMM_ERR_UNSUPPORTED.
  *
  *   a        [B, M, K] codes, contiguous (E2M1: K/2 bytes per row).
  *   b        [B, N, K] codes, contiguous.
@@ -175,7 +180,7 @@ bsmm_status bsmm_quantize(const void* x, bsmm_dtype x_type, int64_t rows, int64_
  *            contiguous.
  *   workspace  device scratch of at least bsmm_gemm_workspace_size() bytes
  *            (holds the scales in the tensor-core scale-factor layout).
- *   K must be a multiple of 32; pointers 16-byte aligned.
+ *   Pointers 16-byte aligned; E2M1 needs an even K.
  */
 size_t bsmm_gemm_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K, bsmm_dtype a_type);
 

@@ -51,16 +51,14 @@ def test_validation_without_gpu(lib):
     st = lib.bsmm_gemm(1, 128, 128, 100, fake, b.E4M3, fake, b.E4M3, fake, 3, fake, 4, b.SCALE_UE8M0, fake, b.F32,
                        fake, 1 << 20, None)
     assert st == b.ERR_SHAPE
-    # block size 16 with UE8M0 scales: valid definition, no kernel (jax cuDNN example shapes)
-    st = lib.bsmm_gemm(3, 128, 128, 64, fake, b.E4M3, fake, b.E4M3, fake, 4, fake, 4, b.SCALE_UE8M0, fake, b.F32,
-                       fake, 1 << 20, None)
-    assert st == b.ERR_UNSUPPORTED
-    assert b"UE8M0" in lib.bsmm_last_error()
-    # E2M1 takes UE4M3 per 16 (NVFP4) or UE8M0 per 32 (MXFP4), not the other pairings
-    for scale, K_s in ((b.SCALE_UE8M0, 16), (b.SCALE_UE4M3, 8)):
-        st = lib.bsmm_gemm(1, 128, 128, 256, fake, b.E2M1, fake, b.E2M1, fake, K_s, fake, K_s, scale, fake, b.F32,
+    # the definition takes any block size; what has no kernel: FP8 codes with
+    # E2M1 codes, INT8 codes, FP32 scales
+    for at, bt, scale in ((b.E4M3, b.E2M1, b.SCALE_UE8M0), (b.INT8, b.INT8, b.SCALE_UE8M0),
+                          (b.E4M3, b.E4M3, b.SCALE_F32)):
+        st = lib.bsmm_gemm(1, 128, 128, 256, fake, at, fake, bt, fake, 8, fake, 8, scale, fake, b.F32,
                            fake, 1 << 20, None)
         assert st == b.ERR_UNSUPPORTED
+        assert b"E4M3/E5M2" in lib.bsmm_last_error()
     # grouped: n not a multiple of group_n; group other than 128
     assert lib.bsmm_gemm_grouped(64, 200, 256, fake, b.E4M3, fake, b.E4M3, fake, fake, 128, 128, fake,
                                  None) == b.ERR_SHAPE

@@ -251,15 +251,58 @@ def test_jax_basic_case_padded_to_a_hardware_block():
     assert y.cpu().item() == 8.0
 
 
-def test_unsupported_block_16_with_ue8m0_is_reported():
-    """The jax cuDNN example's shapes (3,128,64) with (3,128,4) E8M0 scales
-    imply a block of 16, which the hardware MXFP8 path does not take."""
+def test_jax_cudnn_example_shapes_block_16_ue8m0():
+    """The jax cuDNN example's shapes: a, b (3, 128, 64) FP8 with (3, 128, 4)
+    E8M0 scales, i.e. a block of 16, which the tensor cores do not scale by:
+    computed by the CUDA-core kernel, checked against the definition."""
+    run_blocks(3, 128, 128, 64, "e4m3", "e4m3", "ue8m0", 16, 16, seed=64)
+
+
+def run_blocks(Bn, M, N, K, at, bt, scale, bs_a, bs_b, seed, out=torch.float32):
+    """Any block sizes: codes from seeded draws through the oracle's codec,
+    scale bytes drawn over a range of the scale format."""
     bsmm = _bsmm()
-    a = torch.zeros((3, 128, 64), dtype=torch.uint8, device="cuda")
-    s = torch.full((3, 128, 4), 127, dtype=torch.uint8, device="cuda")
-    with pytest.raises(bsmm.BsmmError) as e:
-        bsmm.gemm(a, a, s, s, "e4m3", "e4m3", "ue8m0")
-    assert e.value.status == bsmm.ERR_UNSUPPORTED
+    g = torch.Generator().manual_seed(seed)
+
+    def codes(rows, fmt):
+        if fmt == "e2m1":
+            return torch.randint(0, 256, (Bn, rows, K // 2), generator=g, dtype=torch.int32).numpy().astype(np.uint8)
+        return F.encode(torch.randn(Bn, rows, K, generator=g).numpy(), fmt)
+
+    def scales(rows, bs):
+        if scale == "ue8m0":
+            return (torch.randint(-6, 7, (Bn, rows, K // bs), generator=g).numpy() + 127).astype(np.uint8)
+        return F.encode(np.exp2(torch.empty(Bn, rows, K // bs).uniform_(-4, 4, generator=g).numpy()), "ue4m3")
+
+    ca, cb, sa, sb = codes(M, at), codes(N, bt), scales(M, bs_a), scales(N, bs_b)
+    t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()  # noqa: E731
+    y = bsmm.gemm(t(ca), t(cb), t(sa), t(sb), at, bt, scale, out_dtype=out)
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    dec = lambda c, f: F.decode(F.unpack_e2m1(c), "e2m1") if f == "e2m1" else F.decode(c, f)  # noqa: E731
+    da, db = dec(ca, at), dec(cb, bt)
+    dsa, dsb = F.decode(sa, scale), F.decode(sb, scale)
+    y_ref = G.scaled_matmul(da, db, dsa, dsb)
+    bound = G.scaled_matmul_bound(da, db, dsa, dsb)
+    assert_within(y.float().cpu().numpy(), y_ref, bound, f"{at}x{bt} {scale} blocks {bs_a}/{bs_b} {Bn}x{M}x{N}x{K}",
+                  G.BF16_HALF_ULP if out == torch.bfloat16 else 0.0)
+
+
+@pytest.mark.parametrize("at,bt,scale,bs_a,bs_b,K", [
+    # multiples of the hardware block: tensor cores, each scale repeated
+    ("e4m3", "e4m3", "ue8m0", 64, 64, 512), ("e4m3", "e5m2", "ue8m0", 128, 32, 512),
+    ("e2m1", "e2m1", "ue4m3", 32, 64, 512), ("e2m1", "e2m1", "ue8m0", 64, 128, 1024),
+    # other blocks: CUDA-core kernel
+    ("e4m3", "e4m3", "ue8m0", 16, 16, 256), ("e5m2", "e4m3", "ue8m0", 48, 96, 96),
+    ("e4m3", "e4m3", "ue4m3", 32, 32, 256), ("e2m1", "e2m1", "ue8m0", 16, 16, 256),
+    ("e2m1", "e2m1", "ue4m3", 8, 8, 64), ("e4m3", "e4m3", "ue8m0", 200, 200, 200),
+])
+def test_any_block_size(at, bt, scale, bs_a, bs_b, K):
+    run_blocks(2, 200, 136, K, at, bt, scale, bs_a, bs_b, seed=bs_a * 7 + bs_b + K)
+
+
+def test_any_block_size_bf16_output():
+    run_blocks(1, 256, 256, 256, "e4m3", "e4m3", "ue8m0", 16, 16, seed=5, out=torch.bfloat16)
 
 
 @pytest.mark.parametrize("offset", [1, 4])
