@@ -69,12 +69,20 @@ struct PCfg {
   // scale-factor atoms per K block per 128 rows: MXF8 1 (128 K / 32), NVF4 4
   // (256 K / 16), MXF4 2 (256 K / 32)
   static constexpr int ATOMS = MODE == kPairMXF8 ? 1 : (MODE == kPairNVF4 ? 4 : (MODE == kPairMXF4 ? 2 : 0));
-  static constexpr int STAGES = MODE == kPairF32 ? 3 : 4;
+  static constexpr int STAGES = (MODE == kPairF32 || MODE == kPairNVF4) ? 3 : 4;
   // output staging per epilogue warp: 32 rows x 128 bytes per 32-column chunk
   // (kPairF32 stages both chunks of a tile; the TMA-store path reuses one)
   static constexpr int STG_PER_WARP = MODE == kPairF32 ? 8192 : 4096;
-  static constexpr int SFA_BYTES = ATOMS * 512;      // this CTA's 128 A rows
-  static constexpr int SFB_BYTES = 2 * ATOMS * 512;  // all 256 B rows
+  // Scale factors per stage, in 512-byte slots: this CTA's 128 A rows, ATOMS
+  // atoms skewed by lane quarter over ATOMS + 3 slots (a single atom in one
+  // slot); all 256 B rows, 2 ATOMS atoms, for NVFP4 each four times over
+  // (every lane quarter reads all of B's scales), which costs shared memory
+  // but halves B's copies.
+  static constexpr bool B_REPL = ATOMS > 0 && pair_b_replicated(ATOMS);
+  static constexpr int SFA_SLOTS = ATOMS == 0 ? 0 : pair_sfa_slots(ATOMS);
+  static constexpr int SFB_SLOTS = ATOMS == 0 ? 0 : pair_sfb_slots(ATOMS);
+  static constexpr int SFA_BYTES = SFA_SLOTS * 512;
+  static constexpr int SFB_BYTES = SFB_SLOTS * 512;
   static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + SF_BYTES;  // per CTA
   static constexpr int NACC = (MODE == kPairF32 || MODE == kPairI8) ? 2 : 1;
@@ -248,15 +256,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_3d_pair(sA + stage * A_BYTES, &tmA, full_leader, kt * KB, mb * PM + rank * HALF, b);
           tma_load_3d_pair(sB + stage * B_BYTES, &tmB, full_leader, kt * KB, nb * PN + rank * HALF, b);
           if constexpr (C::ATOMS > 0) {  // block-scaled modes: this stage's scale-factor atoms
-            // atoms as rows of 128 bytes: atom j of row tile rt of batch b
-            // starts at row 4 * ((b * rt_count + rt) * ks4 + j)
+            // one block of slots per operand, as rows of 128 bytes: A's for
+            // (batch, row tile, K tile), B's for (batch, row-tile pair, K tile)
             uint8_t* sf = sSF + stage * C::SF_BYTES;
-            const int a_row = 4 * ((b * p.sfa_rt + 2 * mb + static_cast<int>(rank)) * p.ks4 + kt * C::ATOMS);
+            const int a_row = 4 * C::SFA_SLOTS * ((b * p.sfa_rt + 2 * mb + static_cast<int>(rank)) * p.k_tiles + kt);
             tma_load_3d_pair(sf, &tmSFA, full_leader, 0, a_row, 0);
+            if constexpr (C::B_REPL) {
+              const int b_row = 4 * C::SFB_SLOTS * ((b * (p.sfb_rt / 2) + nb) * p.k_tiles + kt);
+              tma_load_3d_pair(sf + C::SFA_BYTES, &tmSFB, full_leader, 0, b_row, 0);
+            } else {  // atom j of row tile rt of batch b: rows 4 ((b rt_count + rt) ks4 + j) ..
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int b_row = 4 * ((b * p.sfb_rt + 2 * nb + r) * p.ks4 + kt * C::ATOMS);
-              tma_load_3d_pair(sf + C::SFA_BYTES + r * C::ATOMS * 512, &tmSFB, full_leader, 0, b_row, 0);
+              for (int r = 0; r < 2; ++r) {
+                const int b_row = 4 * ((b * p.sfb_rt + 2 * nb + r) * p.ks4 + kt * C::ATOMS);
+                tma_load_3d_pair(sf + C::SFA_BYTES + r * C::ATOMS * 512, &tmSFB, full_leader, 0, b_row, 0);
+              }
             }
           }
           if (!leader) mbar_arrive_cluster(full_leader);
@@ -306,18 +319,41 @@ __global__ void __launch_bounds__(THREADS, 1)
             // descriptors for the stage's first bytes, stepped by constants
             const uint64_t a_d = smem_desc(smem_u32(sA + stage * A_BYTES), 16, 1024, 2);
             const uint64_t b_d = smem_desc(smem_u32(sB + stage * B_BYTES), 16, 1024, 2);
-            const uint64_t sf_d = smem_desc(smem_u32(sSF + stage * C::SF_BYTES), 0, 128, 0);
+            const uint32_t sf_s = smem_u32(sSF + stage * C::SF_BYTES);
             const uint32_t sfa_t = tmem + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
             // A atom i (K sub-block i) -> columns sfa_t + 4i; B atom (row tile
-            // r, K sub-block i) -> columns sfb_t + 4*(2i + r).
+            // r, K sub-block i) -> columns sfb_t + 4*(2i + r).  In each atom's
+            // 4 columns, lane 32q + m0 column j holds row 32j + m0's scales.
+            // The MMA reads A's rows 32q.. from lane quarter q's column q
+            // only, but every quarter reads all 256 of B's rows.  A 128-lane
+            // copy of 8 columns (core matrices of 8 rows x 16 bytes, 128
+            // bytes apart; second 16 bytes LBO on) fills two atoms at once:
+            //  - A: row 32q + m0's words sit at slot a + q, so with LBO one
+            //    slot the copy's rows 32q.. read atoms 2c and 2c + 1 from
+            //    slots 2c + q and 2c + 1 + q;
+            //  - B (NVFP4): each atom is stored four times (slot 4a + q for
+            //    quarter q), so with LBO four slots quarter q reads its own.
+            // One copy per pair of atoms instead of one per atom.
+            if constexpr (C::ATOMS == 1) {  // a single A atom, replicated by the copy
+              tc_cp_sf_pair(sfa_t, smem_desc(sf_s, 0, 128, 0));
+            } else {
+              const uint64_t sfa_d = smem_desc(sf_s, 512, 128, 0);
 #pragma unroll
-            for (int i = 0; i < C::ATOMS; ++i) tc_cp_sf_pair(sfa_t + 4 * i, desc_add(sf_d, 512 * i));
+              for (int c = 0; c < C::ATOMS / 2; ++c) tc_cp_sf_pair_x2(sfa_t + 8 * c, desc_add(sfa_d, 1024 * c));
+            }
+            if constexpr (C::B_REPL) {
+              const uint64_t sfb_d = smem_desc(sf_s + C::SFA_BYTES, 2048, 128, 0);
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+              for (int i = 0; i < C::ATOMS; ++i) tc_cp_sf_pair_x2(sfb_t + 8 * i, desc_add(sfb_d, 4096 * i));
+            } else {  // one copy per atom, replicated to the four lane quarters by the copy
+              const uint64_t sfb_d = smem_desc(sf_s + C::SFA_BYTES, 0, 128, 0);
 #pragma unroll
-              for (int i = 0; i < C::ATOMS; ++i)
-                tc_cp_sf_pair(sfb_t + 4 * (2 * i + r), desc_add(sf_d, C::SFA_BYTES + 512 * (r * C::ATOMS + i)));
+              for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int i = 0; i < C::ATOMS; ++i)
+                  tc_cp_sf_pair(sfb_t + 4 * (2 * i + r), desc_add(sfb_d, 512 * (r * C::ATOMS + i)));
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint64_t ad = desc_add(a_d, 32 * k);
@@ -782,16 +818,21 @@ cudaError_t launch_mx_gemm_pair(const MxGemmRequest& r, const MxAtoms& at, cudaS
   const bool nv = r.fmt == kFmtNVF4, mf4 = r.fmt == kFmtMXF4;
   const int atoms = nv ? 4 : (mf4 ? 2 : 1);
   const int64_t kbytes = (nv || mf4) ? r.K / 2 : r.K;
-  const int64_t sfa_rows = r.B * static_cast<int64_t>(at.sfa_rt) * at.ks4 * 4;  // 128-byte rows
-  const int64_t sfb_rows = r.B * static_cast<int64_t>(at.sfb_rt) * at.ks4 * 4;
+  // scale blocks as 128-byte rows, one TMA box per block
+  const int sa_rows = 4 * pair_sfa_slots(atoms), sb_rows = 4 * pair_sfb_slots(atoms);
+  const int64_t sfa_rows = r.B * static_cast<int64_t>(at.sfa_rt) * at.k_tiles * sa_rows;
+  const bool brep = pair_b_replicated(atoms);
+  const int64_t sfb_rows = brep ? r.B * static_cast<int64_t>(at.sfb_rt / 2) * at.k_tiles * sb_rows
+                                : r.B * static_cast<int64_t>(at.sfb_rt) * at.ks4 * 4;
   CUtensorMap ta, tb, ty, tsa, tsb;
   const bool ok =
       make_tmap_3d(&ta, r.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, r.M, r.B, KB, HALF, true) &&
       make_tmap_3d(&tb, r.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, r.N, r.B, KB, HALF, true) &&
       make_tmap_3d(&ty, r.y, r.y_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                    r.y_bf16 ? 2 : 4, r.N, r.M, r.B, r.y_bf16 ? 64 : 32, 32, true) &&
-      make_tmap_3d(&tsa, at.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, sfa_rows, 1, 128, 4 * atoms, false) &&
-      make_tmap_3d(&tsb, at.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, sfb_rows, 1, 128, 4 * atoms, false);
+      make_tmap_3d(&tsa, at.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, sfa_rows, 1, 128, sa_rows, false) &&
+      make_tmap_3d(&tsb, at.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, sfb_rows, 1, 128, brep ? sb_rows : 4 * atoms,
+                   false);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;

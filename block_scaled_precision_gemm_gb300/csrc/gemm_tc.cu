@@ -512,6 +512,62 @@ __global__ void __launch_bounds__(256) sf_relayout(const uint8_t* __restrict__ s
   }
 }
 
+// Scale bytes [batch][rows][KSu] -> the CTA-pair kernel's blocks of 512-byte
+// slots, one block per (batch, T, K tile kt) holding the scales of K tile kt
+// for `tiles` row tiles of 128 (rows 128 * tiles * T ..).  Atom a = tiles * j
+// + r holds the scales of row tile tiles * T + r for hardware K blocks
+// 4 (kt * atoms + j) .. +3.  Its row 32q + m0 is word q of 16-byte line m0 of
+// slot a + q (`skew`), of slot a (neither), or of each of slots 4a .. 4a + 3
+// (`replicate`); one byte per hardware block, in K order.  Missing rows and
+// blocks past K get `pad`.  Slot positions that no atom fills are never read
+// by the GEMM and are left as they are.
+// A thread owns one row (q, m0) of one tile of one block: it reads the row's
+// 4 * atoms scale bytes of the K tile and writes its word of every atom.
+__global__ void __launch_bounds__(256) sf_relayout_pair(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst,
+                                                        int nb, int R, int KS, int NT, int k_tiles, int atoms,
+                                                        int tiles, int slots, int skew, int replicate,
+                                                        uint32_t pad, int KSu, int rep) {
+  const int64_t total = static_cast<int64_t>(nb) * NT * k_tiles * tiles * 128;
+  const uint32_t pad4 = pad * 0x01010101u;
+  const bool fast = rep == 1 && (KS & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 3) == 0;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int q = static_cast<int>(idx & 3);
+    const int m0 = static_cast<int>((idx >> 2) & 31);
+    int64_t t = idx >> 7;
+    const int r = static_cast<int>(t % tiles);
+    t /= tiles;
+    const int kt = static_cast<int>(t % k_tiles);
+    t /= k_tiles;
+    const int T = static_cast<int>(t % NT);
+    const int64_t b = t / NT;
+    const int row = (T * tiles + r) * 128 + 32 * q + m0;
+    uint32_t* block = dst + ((b * NT + T) * k_tiles + kt) * static_cast<int64_t>(slots) * 128;
+    const uint8_t* src_row = src + (b * R + (row < R ? row : 0)) * static_cast<int64_t>(KSu);
+    for (int j = 0; j < atoms; ++j) {
+      const int hb0 = 4 * (kt * atoms + j);
+      uint32_t v;
+      if (row >= R) {
+        v = pad4;
+      } else if (fast && hb0 + 4 <= KS) {
+        v = __ldg(reinterpret_cast<const uint32_t*>(src_row + hb0));
+      } else {
+        v = 0;
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb)
+          v |= static_cast<uint32_t>(hb0 + kb < KS ? src_row[(hb0 + kb) / rep] : pad) << (8 * kb);
+      }
+      const int a = tiles * j + r;
+      if (replicate) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) block[(4 * a + c) * 128 + m0 * 4 + q] = v;
+      } else {
+        block[(a + (skew ? q : 0)) * 128 + m0 * 4 + q] = v;
+      }
+    }
+  }
+}
+
 __global__ void selftest_wait_kernel(uint64_t timeout_ns, int* status) {
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
@@ -554,10 +610,14 @@ bool make_output_map(CUtensorMap* ty, void* y, bool bf16, int64_t B, int64_t M, 
 
 size_t sf_atoms_bytes(int64_t B, int64_t R, int64_t K, int fmt) {
   // K per 128-byte tile: 128 FP8 or 256 FP4 elements; atoms per tile: one per
-  // 4 scales (MXF8 1, NVF4 4, MXF4 2)
+  // 4 scales (MXF8 1, NVF4 4, MXF4 2).  The larger of the one-CTA kernel's
+  // atoms and the pair kernel's blocks, for either operand.
   const int64_t k_tiles = ceil_div(K, fmt == kFmtMXF8 ? 128 : 256);
-  const int64_t ks4 = k_tiles * (fmt == kFmtNVF4 ? 4 : (fmt == kFmtMXF4 ? 2 : 1));
-  return static_cast<size_t>(B) * rt_rows(R) * ks4 * 512;
+  const int atoms = fmt == kFmtNVF4 ? 4 : (fmt == kFmtMXF4 ? 2 : 1);
+  const int64_t rt = rt_rows(R);
+  const int64_t slots = std::max({rt * atoms, rt * pair_sfa_slots(atoms),
+                                  pair_b_replicated(atoms) ? rt / 2 * pair_sfb_slots(atoms) : 0});
+  return static_cast<size_t>(B) * k_tiles * slots * 512;
 }
 
 cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* why) {
@@ -573,6 +633,47 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
   uint8_t* sfa = ws;
   uint8_t* sfb = ws + a_bytes;
   const uint32_t pad = nv ? 0u : 127u;  // scale 1 for UE8M0 blocks past K (their codes are zero)
+
+  // Kernel choice: CTA-pair 256 x 256 tiles when there is a tile for every
+  // cluster, else one CTA per 128 x 128 tile.  BSMM_MX_KERNEL=pair|single
+  // overrides the choice (pair still needs TMA-storable output rows).
+  const char* force = std::getenv("BSMM_MX_KERNEL");
+  const bool want_pair = force && std::strcmp(force, "pair") == 0;
+  const bool want_single = force && std::strcmp(force, "single") == 0;
+  const int esz = r.y_bf16 ? 2 : 4;
+  const bool storable = (r.N * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(r.y) % 16 == 0;
+  if (mf4 && !storable) {  // MXFP4 has only the pair kernel
+    *why = "MXFP4 output rows must be 16-byte aligned (N * element size % 16 == 0)";
+    return cudaErrorInvalidValue;
+  }
+  if (mf4 || (!want_single && (want_pair ? storable : mx_pair_eligible(r, ctx)))) {
+    const int atoms = nv ? 4 : (mf4 ? 2 : 1);
+    const int RTa = rt_rows(r.M), RTb = rt_rows(r.N);
+    const int sa = pair_sfa_slots(atoms), sb = pair_sfb_slots(atoms);
+    const int64_t ta_threads = r.B * RTa * k_tiles * 128, tb_threads = r.B * (RTb / 2) * k_tiles * 2 * 128;
+    const int ga = static_cast<int>(std::min<int64_t>(ceil_div(ta_threads, 256), ctx->num_sms * 16));
+    const int gb = static_cast<int>(std::min<int64_t>(ceil_div(tb_threads, 256), ctx->num_sms * 16));
+    sf_relayout_pair<<<ga, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
+                                        static_cast<int>(r.M), KS, RTa, static_cast<int>(k_tiles), atoms, 1, sa,
+                                        atoms > 1 ? 1 : 0, 0, pad, static_cast<int>(r.K_a),
+                                        static_cast<int>(KS / r.K_a));
+    if (pair_b_replicated(atoms)) {
+      sf_relayout_pair<<<gb, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
+                                          static_cast<int>(r.N), KS, RTb / 2, static_cast<int>(k_tiles), atoms, 2, sb,
+                                          0, 1, pad, static_cast<int>(r.K_b), static_cast<int>(KS / r.K_b));
+    } else {  // the one-CTA kernel's atoms
+      const int64_t words = r.B * RTb * static_cast<int64_t>((ks4 + 7) / 8) * 128;
+      const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
+      sf_relayout<<<blocks, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
+                                         static_cast<int>(r.N), KS, RTb, ks4, pad, static_cast<int>(r.K_b),
+                                         static_cast<int>(KS / r.K_b));
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const MxAtoms at{sfa, sfb, RTa, RTb, ks4, static_cast<int>(k_tiles)};
+    return launch_mx_gemm_pair(r, at, s, why);
+  }
+
   {
     const int RT = rt_rows(r.M);
     const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
@@ -591,23 +692,6 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-
-  // Kernel choice: CTA-pair 256 x 256 tiles when there is a tile for every
-  // cluster, else one CTA per 128 x 128 tile.  BSMM_MX_KERNEL=pair|single
-  // overrides the choice (pair still needs TMA-storable output rows).
-  const char* force = std::getenv("BSMM_MX_KERNEL");
-  const bool want_pair = force && std::strcmp(force, "pair") == 0;
-  const bool want_single = force && std::strcmp(force, "single") == 0;
-  const int esz = r.y_bf16 ? 2 : 4;
-  const bool storable = (r.N * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(r.y) % 16 == 0;
-  if (mf4 && !storable) {  // MXFP4 has only the pair kernel
-    *why = "MXFP4 output rows must be 16-byte aligned (N * element size % 16 == 0)";
-    return cudaErrorInvalidValue;
-  }
-  if (mf4 || (!want_single && (want_pair ? storable : mx_pair_eligible(r, ctx)))) {
-    const MxAtoms at{sfa, sfb, rt_rows(r.M), rt_rows(r.N), ks4, static_cast<int>(k_tiles)};
-    return launch_mx_gemm_pair(r, at, s, why);
-  }
 
   const int64_t kbytes = nv ? r.K / 2 : r.K;
   CUtensorMap ta, tb, ty;

@@ -76,8 +76,15 @@ cudaError_t launch_mx_gemm_generic(const MxGemmRequest& r, int64_t K_a, int64_t 
 cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* why);
 // Same, with the scale-factor atoms in the library's static device array.
 cudaError_t launch_mx_gemm_noalloc(const MxGemmRequest& r, cudaStream_t s, std::string* why);
-// Scale-factor atoms already laid out by launch_mx_gemm: [batch][row tile of
-// 128 (sfa_rt / sfb_rt of them, an even count)][K atom (ks4)] x 512 bytes.
+// Scale factors already laid out by launch_mx_gemm for the CTA-pair kernel,
+// in 512-byte slots.  A: [batch][row tile of 128 (sfa_rt)][K tile] x
+// pair_sfa_slots, the atoms skewed by lane quarter (one atom: as is).  B, when
+// pair_b_replicated: [batch][pair of row tiles (sfb_rt / 2)][K tile] x
+// pair_sfb_slots, each atom four times over; otherwise the one-CTA kernel's
+// atoms [batch][row tile][K atom (ks4)].  See sf_relayout_pair (gemm_tc.cu).
+constexpr int pair_sfa_slots(int atoms) { return atoms == 1 ? 1 : atoms + 3; }
+constexpr bool pair_b_replicated(int atoms) { return atoms == 4; }
+constexpr int pair_sfb_slots(int atoms) { return pair_b_replicated(atoms) ? 8 * atoms : 2 * atoms; }
 struct MxAtoms {
   const uint8_t* sfa;
   const uint8_t* sfb;

@@ -341,6 +341,11 @@ __device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t adesc, u
 __device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
+// 128 rows x 32 bytes of shared memory -> 128 lanes x 8 columns of each
+// CTA's tensor memory (two 16-byte halves, LBO apart).
+__device__ __forceinline__ void tc_cp_sf_pair_x2(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));

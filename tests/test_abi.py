@@ -86,9 +86,13 @@ def test_validation_without_gpu(lib):
 
 def test_workspace_queries(lib):
     import block_scaled_precision_gemm_gb300 as b
-    # scale atoms: 512 B per (row tile of 128, rounded to pairs) per K atom
+    # scale slots of 512 B per operand and K tile: the most of the one-CTA
+    # layout (atoms per row tile of 128, rounded to pairs) and the pair
+    # kernel's blocks (A: atoms + 3 per row tile, one atom as is; NVFP4's B:
+    # 8 x atoms per pair of row tiles)
     assert lib.bsmm_gemm_workspace_size(1, 128, 128, 128, b.E4M3) == 2 * (2 * 512)
     assert lib.bsmm_gemm_workspace_size(8, 4096, 4096, 8192, b.E4M3) == 2 * 8 * 32 * 64 * 512
-    assert lib.bsmm_gemm_workspace_size(1, 16384, 16384, 16384, b.E2M1) == 2 * 128 * 256 * 512
+    # E2M1: NVFP4's B blocks, 32 slots per pair of row tiles (room also for MXFP4)
+    assert lib.bsmm_gemm_workspace_size(1, 16384, 16384, 16384, b.E2M1) == 2 * 64 * (64 * 32) * 512
     assert lib.bsmm_int8_channel_workspace_size(1, 3, 2) > 0
     assert lib.bsmm_linear_backward_workspace_size(64, 64, 64) > 4 * 64 * 64
