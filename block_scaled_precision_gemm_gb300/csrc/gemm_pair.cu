@@ -40,7 +40,8 @@
 // while the two otherwise idle control warps copy the staged results out with
 // coalesced global stores (through the TMA unit those stores delayed the
 // operand loads) and warm L2 with the next tile's A-scale rows.  The block-
-// scaled modes drain the accumulator once per tile and store through TMA.
+// scaled modes drain the accumulator once per tile and hand it to the same
+// copy warps in 128-byte column chunks.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -117,7 +118,7 @@ struct PairParams {
   // through 2-D tensor maps of 128-byte rows (an atom is 4 rows)
   int sfa_rt, sfb_rt, ks4;
   int y_bf16;
-  float* y;  // kPairF32 output [M][N], written by the copy warps
+  float* y;  // output [B][M][N] (F32, or bf16 when y_bf16), written by the copy warps
   // kPairI8: per-row and per-column scales, K blocks per exact FP32 chunk,
   // whether the int32 sums are stored (through tmSFA)
   const float* sx;
@@ -454,6 +455,50 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_commit_pair_mc(done, 0x1);
       mbar_wait(done, 0, p.timeout_ns, never_abort, p.status, kSiteDone);
+    } else if (C::ATOMS > 0 && warp >= 2) {
+      // ------------------------------------------------ output copy (both CTAs)
+      // Block-scaled modes: the epilogue stages each tile's result one
+      // 128-byte column chunk at a time (FP32: two rounds, bf16: one); warp 2
+      // copies epilogue warps 0-7, warp 3 warps 8-15, four whole 128-byte
+      // lines per instruction.  The copies trickle out during the next tile.
+      // (Tile-end TMA stores held up the operand loads queued behind them.)
+      const int cw = warp - 2;
+      const int rounds = p.y_bf16 ? 1 : 2;
+      uint32_t sph = 0;
+      bool ok = true;
+      for (int t = cid; ok && t < p.num_tiles; t += ncl) {
+        int b, mb, nb;
+        decode_pair_tile(p, t, b, mb, nb);
+        for (int c = 0; c < rounds; ++c) {
+          if (!mbar_wait(stg_full, sph, p.timeout_ns, abort_flag, p.status, kSiteStore)) {
+            ok = false;
+            break;
+          }
+          for (int i = 0; i < EPI_WARPS / 2; ++i) {
+            const int ew = cw * (EPI_WARPS / 2) + i;
+            const int row0 = mb * PM + static_cast<int>(rank) * HALF + (ew & 3) * 32;
+            const int col0 = nb * PN + (ew >> 2) * EPI_COLS + (p.y_bf16 ? 0 : 32 * c);
+            const uint8_t* src = stg + ew * C::STG_PER_WARP;
+            const int u = lane & 7;
+            const int col = col0 + (p.y_bf16 ? 8 : 4) * u;  // this lane's 16 bytes
+            if (row0 >= p.M || col >= p.N) continue;       // N * size % 16 == 0: all in or all out
+#pragma unroll 4
+            for (int j = 0; j < 8; ++j) {
+              const int r = 4 * j + (lane >> 3);
+              const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ((u ^ (r & 7)) * 16));
+              if (row0 + r < p.M) {
+                const size_t e = (static_cast<size_t>(b) * p.M + row0 + r) * p.N + col;
+                uint4* dst = p.y_bf16 ? reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.y) + e)
+                                      : reinterpret_cast<uint4*>(p.y + e);
+                *dst = v;
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(stg_empty);
+          sph ^= 1u;
+        }
+      }
     } else if (MODE == kPairF32 && warp >= 2) {
       // ------------------------------------------------ output copy (both CTAs)
       // Warp 2 copies the staging of epilogue warps 0-7, warp 3 that of 8-15:
@@ -645,6 +690,39 @@ __global__ void __launch_bounds__(THREADS, 1)
         sph ^= 1u;
         continue;
       }
+      if constexpr (C::ATOMS > 0) {
+        // stage the tile's result for the copy warps, one 128-byte column
+        // chunk (32 rows x 128 bytes, 16-byte units rotated by row) per round
+        const bool in_y = row0 < p.M && col_ok;
+        const int rounds = p.y_bf16 ? 1 : 2;
+        for (int c = 0; c < rounds; ++c) {
+          if (!mbar_wait(stg_empty, sph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteStaging)) {
+            ok = false;
+            break;
+          }
+          if (in_y) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint4 v;
+              if (p.y_bf16) {
+                const float2* a = &acc[4 * j];
+                v = make_uint4(pack_bf16x2_pair(a[0].x, a[0].y), pack_bf16x2_pair(a[1].x, a[1].y),
+                               pack_bf16x2_pair(a[2].x, a[2].y), pack_bf16x2_pair(a[3].x, a[3].y));
+              } else {
+                const float2 a0 = acc[16 * c + 2 * j], a1 = acc[16 * c + 2 * j + 1];
+                v = make_uint4(__float_as_uint(a0.x), __float_as_uint(a0.y), __float_as_uint(a1.x),
+                               __float_as_uint(a1.y));
+              }
+              *reinterpret_cast<uint4*>(my_stg + lane * 128 + ((j ^ (lane & 7)) * 16)) = v;
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(stg_full);
+          sph ^= 1u;
+        }
+        if (!ok) break;
+        continue;
+      }
       if (row0 >= p.M || !col_ok) continue;  // this warp's box lies outside y
       if constexpr (MODE == kPairI8) {
         if (p.store_acc) store_box_f32(&tmSFA, my_stg, acc, col0, row0, b, lane);  // int32 bits as they are
@@ -660,45 +738,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         store_box_f32(&tmY, my_stg, acc, col0, row0, b, lane);
         continue;
-      }
-      if (!p.y_bf16) {
-        // 64 FP32 columns of 32 rows leave as two 32 x 32 TMA stores
-#pragma unroll
-        for (int c = 0; c < COLS / 32; ++c) {
-          if (lane == 0) bulk_wait_read<0>();
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float2 v0 = acc[16 * c + 2 * j], v1 = acc[16 * c + 2 * j + 1];
-            const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
-            *reinterpret_cast<uint4*>(my_stg + off) =
-                make_uint4(__float_as_uint(v0.x), __float_as_uint(v0.y), __float_as_uint(v1.x), __float_as_uint(v1.y));
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tmY, my_stg, col0 + 32 * c, row0, b);
-            bulk_commit();
-          }
-        }
-      } else {
-        // 64 bf16 columns (128 bytes) of 32 rows: one TMA store
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float2* v = &acc[4 * j];
-          const uint32_t off = lane * 128 + ((j ^ (lane & 7)) * 16);
-          *reinterpret_cast<uint4*>(my_stg + off) =
-              make_uint4(pack_bf16x2_pair(v[0].x, v[0].y), pack_bf16x2_pair(v[1].x, v[1].y),
-                         pack_bf16x2_pair(v[2].x, v[2].y), pack_bf16x2_pair(v[3].x, v[3].y));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&tmY, my_stg, col0, row0, b);
-          bulk_commit();
-        }
       }
     }
     if (lane == 0) bulk_wait<0>();
@@ -848,6 +887,7 @@ cudaError_t launch_mx_gemm_pair(const MxGemmRequest& r, const MxAtoms& at, cudaS
   p.num_tiles = static_cast<int>(pair_tiles(r.B, r.M, r.N));
   p.sfa_rt = at.sfa_rt;
   p.sfb_rt = at.sfb_rt;
+  p.y = static_cast<float*>(r.y);
   p.ks4 = at.ks4;
   p.y_bf16 = r.y_bf16 ? 1 : 0;
   p.status = ctx->status;
