@@ -70,10 +70,14 @@ struct PCfg {
   // scale-factor atoms per K block per 128 rows: MXF8 1 (128 K / 32), NVF4 4
   // (256 K / 16), MXF4 2 (256 K / 32)
   static constexpr int ATOMS = MODE == kPairMXF8 ? 1 : (MODE == kPairNVF4 ? 4 : (MODE == kPairMXF4 ? 2 : 0));
-  static constexpr int STAGES = (MODE == kPairF32 || MODE == kPairNVF4) ? 3 : 4;
+  static constexpr int STAGES = MODE == kPairF32 ? 3 : 4;
   // output staging per epilogue warp: 32 rows x 128 bytes per 32-column chunk
-  // (kPairF32 stages both chunks of a tile; the TMA-store path reuses one)
-  static constexpr int STG_PER_WARP = MODE == kPairF32 ? 8192 : 4096;
+  // (kPairF32 stages both chunks of a tile; kPairI8's TMA stores reuse one;
+  // the block-scaled modes stage STG_ROWS rows of one chunk at a time)
+  // Rows per staging round in the block-scaled modes: NVFP4's scale blocks
+  // leave room for 8 (1 KB per warp), the others stage all 32 at once.
+  static constexpr int STG_ROWS = MODE == kPairNVF4 ? 8 : 32;
+  static constexpr int STG_PER_WARP = MODE == kPairF32 ? 8192 : (ATOMS > 0 ? STG_ROWS * 128 : 4096);
   // Scale factors per stage, in 512-byte slots: this CTA's 128 A rows, ATOMS
   // atoms skewed by lane quarter over ATOMS + 3 slots (a single atom in one
   // slot); all 256 B rows, 2 ATOMS atoms, for NVFP4 each four times over
@@ -457,13 +461,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(done, 0, p.timeout_ns, never_abort, p.status, kSiteDone);
     } else if (C::ATOMS > 0 && warp >= 2) {
       // ------------------------------------------------ output copy (both CTAs)
-      // Block-scaled modes: the epilogue stages each tile's result one
-      // 128-byte column chunk at a time (FP32: two rounds, bf16: one); warp 2
-      // copies epilogue warps 0-7, warp 3 warps 8-15, four whole 128-byte
-      // lines per instruction.  The copies trickle out during the next tile.
-      // (Tile-end TMA stores held up the operand loads queued behind them.)
+      // Block-scaled modes: the epilogue stages each tile's result STG_ROWS
+      // rows of one 128-byte column chunk at a time (FP32: 2 chunks, bf16: 1,
+      // times 32 / STG_ROWS row groups); warp 2 copies epilogue warps 0-7,
+      // warp 3 warps 8-15, four whole 128-byte lines per instruction.  The
+      // copies trickle out during the next tile.  (Tile-end TMA stores held
+      // up the operand loads queued behind them.)
+      constexpr int GROUPS = 32 / C::STG_ROWS;
       const int cw = warp - 2;
-      const int rounds = p.y_bf16 ? 1 : 2;
+      const int rounds = (p.y_bf16 ? 1 : 2) * GROUPS;
       uint32_t sph = 0;
       bool ok = true;
       for (int t = cid; ok && t < p.num_tiles; t += ncl) {
@@ -476,14 +482,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           for (int i = 0; i < EPI_WARPS / 2; ++i) {
             const int ew = cw * (EPI_WARPS / 2) + i;
-            const int row0 = mb * PM + static_cast<int>(rank) * HALF + (ew & 3) * 32;
-            const int col0 = nb * PN + (ew >> 2) * EPI_COLS + (p.y_bf16 ? 0 : 32 * c);
+            const int row0 = mb * PM + static_cast<int>(rank) * HALF + (ew & 3) * 32 + C::STG_ROWS * (c % GROUPS);
+            const int col0 = nb * PN + (ew >> 2) * EPI_COLS + 32 * (c / GROUPS);
             const uint8_t* src = stg + ew * C::STG_PER_WARP;
             const int u = lane & 7;
             const int col = col0 + (p.y_bf16 ? 8 : 4) * u;  // this lane's 16 bytes
             if (row0 >= p.M || col >= p.N) continue;       // N * size % 16 == 0: all in or all out
-#pragma unroll 4
-            for (int j = 0; j < 8; ++j) {
+#pragma unroll
+            for (int j = 0; j < C::STG_ROWS / 4; ++j) {
               const int r = 4 * j + (lane >> 3);
               const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ((u ^ (r & 7)) * 16));
               if (row0 + r < p.M) {
@@ -691,16 +697,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         continue;
       }
       if constexpr (C::ATOMS > 0) {
-        // stage the tile's result for the copy warps, one 128-byte column
-        // chunk (32 rows x 128 bytes, 16-byte units rotated by row) per round
+        // stage the tile's result for the copy warps: per round, the
+        // STG_ROWS rows of one row group of one 128-byte column chunk
+        // (128 bytes a row, 16-byte units rotated by row)
+        constexpr int GROUPS = 32 / C::STG_ROWS;
         const bool in_y = row0 < p.M && col_ok;
-        const int rounds = p.y_bf16 ? 1 : 2;
-        for (int c = 0; c < rounds; ++c) {
+        const int rounds = (p.y_bf16 ? 1 : 2) * GROUPS;
+        for (int rd = 0; rd < rounds; ++rd) {
+          const int c = rd / GROUPS, rg = rd % GROUPS;
           if (!mbar_wait(stg_empty, sph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteStaging)) {
             ok = false;
             break;
           }
-          if (in_y) {
+          if (in_y && lane / C::STG_ROWS == rg) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               uint4 v;
@@ -713,7 +722,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 v = make_uint4(__float_as_uint(a0.x), __float_as_uint(a0.y), __float_as_uint(a1.x),
                                __float_as_uint(a1.y));
               }
-              *reinterpret_cast<uint4*>(my_stg + lane * 128 + ((j ^ (lane & 7)) * 16)) = v;
+              *reinterpret_cast<uint4*>(my_stg + (lane % C::STG_ROWS) * 128 + ((j ^ (lane & 7)) * 16)) = v;
             }
           }
           __syncwarp();
