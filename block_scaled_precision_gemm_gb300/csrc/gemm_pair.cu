@@ -62,7 +62,7 @@ constexpr int THREADS = 640;               // 4 control warps + 16 epilogue warp
 constexpr int EPI_WARPS = 16;
 constexpr int EPI_COLS = 64;               // columns per epilogue thread
 constexpr int TMEM_COLS = 512;
-constexpr int GROUP_M = 16;
+constexpr int GROUP_M = 8;
 constexpr int A_BYTES = HALF * KB, B_BYTES = HALF * KB;
 
 template <int MODE>
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const size_t e = (static_cast<size_t>(b) * p.M + row0 + r) * p.N + col;
                 uint4* dst = p.y_bf16 ? reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.y) + e)
                                       : reinterpret_cast<uint4*>(p.y + e);
-                *dst = v;
+                __stcs(dst, v);  // streaming: y is not read again
               }
             }
           }
