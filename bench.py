@@ -493,6 +493,7 @@ def run_gpu(args):
     roofline = {"kernel": wl.dominant, "bound": "tensor", "achieved": round(achieved, 2),
                 "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                 "traffic": TRAFFIC_PER_LAUNCH.get(workload.name),
+                "traffic_unit": "bytes per launch (ncu DRAM read + write)",
                 "peak_source": f"{peak_src}: {peak_how}",
                 "share_of_step": round(dom_ms / elapsed_ms, 4)}
 
@@ -523,9 +524,19 @@ def run_gpu(args):
         torch.distributed.destroy_process_group()
 
 
-# DRAM bytes per GEMM launch from ncu (see profiles/); None until captured
-# for the kernel as it stands.
-TRAFFIC_PER_LAUNCH = {}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# the dominant kernel or call, from ncu captures of the same workloads
+# (profiles/traffic_by_workload.md); absent until captured for the kernels as
+# they stand.  sweep: the mean over the step's 8 GEMM launches.  mxfp8,
+# nvfp4, mxfp4: the GEMM launch (the scale relayouts add under 1%).  int8:
+# the whole call (4 launches).
+TRAFFIC_PER_LAUNCH = {
+    W.GROUPED_SWEEP.name: 1_968_950_000,
+    W.MXFP8_BATCHED.name: 1_314_209_280,
+    W.NVFP4_SQUARE.name: 4_356_233_000,
+    W.MXFP4_SQUARE.name: 2_462_586_000,
+    W.INT8_4096.name: 351_400_000,
+}
 
 
 # --------------------------------------------------------------------------- #

@@ -653,10 +653,17 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
     const int64_t ta_threads = r.B * RTa * k_tiles * 128, tb_threads = r.B * (RTb / 2) * k_tiles * 2 * 128;
     const int ga = static_cast<int>(std::min<int64_t>(ceil_div(ta_threads, 256), ctx->num_sms * 16));
     const int gb = static_cast<int>(std::min<int64_t>(ceil_div(tb_threads, 256), ctx->num_sms * 16));
-    sf_relayout_pair<<<ga, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
-                                        static_cast<int>(r.M), KS, RTa, static_cast<int>(k_tiles), atoms, 1, sa,
-                                        atoms > 1 ? 1 : 0, 0, pad, static_cast<int>(r.K_a),
-                                        static_cast<int>(KS / r.K_a));
+    if (atoms > 1) {
+      sf_relayout_pair<<<ga, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
+                                          static_cast<int>(r.M), KS, RTa, static_cast<int>(k_tiles), atoms, 1, sa, 1,
+                                          0, pad, static_cast<int>(r.K_a), static_cast<int>(KS / r.K_a));
+    } else {  // one atom per K tile: the pair layout is the one-CTA kernel's
+      const int64_t words = r.B * RTa * static_cast<int64_t>((ks4 + 7) / 8) * 128;
+      const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
+      sf_relayout<<<blocks, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
+                                         static_cast<int>(r.M), KS, RTa, ks4, pad, static_cast<int>(r.K_a),
+                                         static_cast<int>(KS / r.K_a));
+    }
     if (pair_b_replicated(atoms)) {
       sf_relayout_pair<<<gb, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
                                           static_cast<int>(r.N), KS, RTb / 2, static_cast<int>(k_tiles), atoms, 2, sb,
