@@ -12,10 +12,14 @@
 //   i8_quant_rows   one CTA per row of x: absmax, scale, codes into x_q and a
 //                   zero-padded K-major copy [B, Kp] the matmul reads (bf16,
 //                   or int8 for the fallback below).
-//   i8_colmax       column maxima of w, split over row chunks, combined with
-//                   an integer atomicMax on the (non-negative) float bits.
-//   i8_quant_cols   codes of w in the page's layout [D_in, D_out] and
-//                   transposed [D_out, Kp] through a shared-memory tile.
+//   i8_quant_w_strip  all of w in one launch: a cluster of four CTAs per
+//                   strip of 32 columns takes the column maxima (combined
+//                   through distributed shared memory), then the codes in the
+//                   page's layout [D_in, D_out] and transposed [D_out, Kp].
+//   i8_colmax, i8_quant_cols  the same in two launches (maxima by integer
+//                   atomicMax on the non-negative float bits; codes through
+//                   a shared-memory tile) where D_out % 4 != 0 or w is not
+//                   16-byte aligned.
 //   i8_gemm         fallback for outputs TMA cannot store (D_out % 4 != 0 or
 //                   unaligned y): the warp-level integer MMA (mma.sync
 //                   m16n8k32 s8.s8.s32, exact int32), 128x128 CTA tile,
@@ -258,6 +262,157 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
   }
 }
 
+// All of w's per-column quantization in one kernel.  A strip of 32 columns
+// goes to a cluster of four CTAs, CTA q taking rows q Kp/4 .. (q+1) Kp/4 - 1.
+// Thread (warp, lane) owns columns 4 (lane % 8) .. +3 of the strip and, in
+// each step of 256 rows, the 8 consecutive rows 8 (4 warp + lane / 8) .. +7.
+// Pass 1: column maxima of the CTA's rows (8 x 16-byte loads in flight per
+// thread); the four CTAs combine them through distributed shared memory.
+// Pass 2 reads the rows again -- from L2 when w fits there, as all strips
+// are in flight at once -- and writes the codes into w_q [D_in, D_out] (32
+// bytes a row per strip) and into wqT [D_out, Kp], where a thread's 8 codes
+// of one column are 8 consecutive elements of a row (zero codes for rows
+// >= D_in).  Needs D_out % 4 == 0, w 16-byte and w_q 4-byte aligned.
+constexpr int kStrip = 32, kStripSplit = 4;
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+template <typename Pad>
+__global__ void __launch_bounds__(256, 4) i8_quant_w_strip(const float* __restrict__ w, int64_t D_in, int64_t D_out,
+                                                        int64_t Kp, int8_t* __restrict__ wq, float* __restrict__ ws,
+                                                        Pad* __restrict__ wqT) {
+  __shared__ float red[8][kStrip];
+  __shared__ float part_max[kStrip];
+  __shared__ float sc[kStrip];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int cg = lane & 7;
+  const int rsub = (warp << 2) | (lane >> 3);  // 0..31
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kStrip;
+  const int64_t jc = j0 + 4 * cg;
+  const bool col_ok = jc < D_out;  // D_out % 4 == 0: all four in or all out
+  const int64_t n4 = D_out / 4;
+  const float4* base = reinterpret_cast<const float4*>(w) + (jc / 4);
+  const uint32_t q = cluster_ctarank();
+  const int64_t Kq = Kp / kStripSplit;  // a multiple of 32
+  const int64_t rbeg = q * Kq, rend = rbeg + Kq;
+  const int64_t dend = D_in < rend ? D_in : rend;
+  // pass 1: column maxima of this CTA's rows
+  float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col_ok) {
+    for (int64_t r0 = rbeg; r0 < dend; r0 += 256) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t r = r0 + 8 * rsub + u;
+        v[u] = r < dend ? __ldg(base + r * n4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        m.x = fmaxf(m.x, fabsf(v[u].x));
+        m.y = fmaxf(m.y, fabsf(v[u].y));
+        m.z = fmaxf(m.z, fabsf(v[u].z));
+        m.w = fmaxf(m.w, fabsf(v[u].w));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 8; o < 32; o <<= 1) {  // over the lanes holding the same columns
+    m.x = fmaxf(m.x, __shfl_xor_sync(0xffffffffu, m.x, o));
+    m.y = fmaxf(m.y, __shfl_xor_sync(0xffffffffu, m.y, o));
+    m.z = fmaxf(m.z, __shfl_xor_sync(0xffffffffu, m.z, o));
+    m.w = fmaxf(m.w, __shfl_xor_sync(0xffffffffu, m.w, o));
+  }
+  if (lane < 8) {
+    red[warp][4 * lane + 0] = m.x;
+    red[warp][4 * lane + 1] = m.y;
+    red[warp][4 * lane + 2] = m.z;
+    red[warp][4 * lane + 3] = m.w;
+  }
+  __syncthreads();
+  if (t < kStrip) {
+    float mm = red[0][t];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) mm = fmaxf(mm, red[i][t]);
+    part_max[t] = mm;
+  }
+  cluster_sync();  // the four CTAs' partial maxima are visible
+  if (t < kStrip) {
+    const uint32_t a = smem_u32(&part_max[t]);
+    float mm = 0.f;
+#pragma unroll
+    for (int c = 0; c < kStripSplit; ++c) mm = fmaxf(mm, ld_shared_cluster_f32(mapa_shared(a, c)));
+    const float sv = i8_scale(mm);
+    sc[t] = sv;
+    if (q == 0 && j0 + t < D_out) ws[j0 + t] = sv;
+  }
+  cluster_sync();  // peers have read part_max; sc is visible to the CTA
+  const float s0 = sc[4 * cg], s1 = sc[4 * cg + 1], s2 = sc[4 * cg + 2], s3 = sc[4 * cg + 3];
+  // pass 2: codes, 256 rows at a time (rend - i0 is a multiple of 32, so a
+  // thread's 8 rows are all below rend or all at or above it)
+  for (int64_t i0 = rbeg; i0 < rend; i0 += 256) {
+    const int64_t ir = i0 + 8 * rsub;
+    if (ir >= rend) break;
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = (col_ok && ir + u < dend) ? __ldg(base + (ir + u) * n4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    uint32_t code[8];  // row u: the four columns' codes, low byte first
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      code[u] = static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[u].x, s0))) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[u].y, s1))) << 8) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[u].z, s2))) << 16) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[u].w, s3))) << 24);
+      if (col_ok && ir + u < dend) *reinterpret_cast<uint32_t*>(wq + (ir + u) * D_out + jc) = code[u];
+    }
+    if (wqT != nullptr && col_ok) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // column jc + c: rows ir .. ir+7
+        Pad* dst = wqT + (jc + c) * Kp + ir;
+        if constexpr (sizeof(Pad) == 1) {
+          uint32_t lo = 0, hi = 0;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            lo |= ((code[u] >> (8 * c)) & 0xFFu) << (8 * u);
+            hi |= ((code[u + 4] >> (8 * c)) & 0xFFu) << (8 * u);
+          }
+          *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+        } else {
+          uint32_t word[4];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int8_t a = static_cast<int8_t>((code[2 * g] >> (8 * c)) & 0xFFu);
+            const int8_t b = static_cast<int8_t>((code[2 * g + 1] >> (8 * c)) & 0xFFu);
+            word[g] = static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(a))) |
+                      (static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(b))) << 16);
+          }
+          *reinterpret_cast<uint4*>(dst) = make_uint4(word[0], word[1], word[2], word[3]);
+        }
+      }
+    }
+  }
+}
+
+template <typename Pad>
+cudaError_t launch_w_strip(const Int8Request& r, int64_t Kp, Pad* wqT, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = kStripSplit;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(r.D_out, kStrip)), kStripSplit, 1);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, i8_quant_w_strip<Pad>, r.w, static_cast<int64_t>(r.D_in),
+                            static_cast<int64_t>(r.D_out), Kp, r.w_q, r.w_scales, wqT);
+}
+
 // ---------------------------------------------------------------- the matmul
 constexpr int GM = 128, GN = 128, GK = 128, GSTAGES = 4;
 constexpr int G_STAGE_BYTES = (GM + GN) * GK;
@@ -415,8 +570,17 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   const bool tc = !(force && std::strcmp(force, "mma") == 0) && (r.D_out * 4) % 16 == 0 &&
                   reinterpret_cast<uintptr_t>(r.y) % 16 == 0 && reinterpret_cast<uintptr_t>(r.acc) % 16 == 0;
 
-  cudaError_t e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(r.D_out) * 4, s);
-  if (e != cudaSuccess) return e;
+  // w's quantization in one pass over strips of columns (16-byte loads)
+  const bool w_strip = (r.D_out % 4) == 0 && (reinterpret_cast<uintptr_t>(r.w) & 15) == 0 &&
+                       (reinterpret_cast<uintptr_t>(r.w_q) & 3) == 0;
+  cudaError_t e = cudaSuccess;
+  if (!w_strip) {
+    e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(r.D_out) * 4, s);
+    if (e != cudaSuccess) return e;
+  }
+  if (r.B == 0 && w_strip) {  // w alone: codes and scales (no transposed copy)
+    return launch_w_strip<int8_t>(r, Kp, nullptr, s);
+  }
   if (r.B == 0) {  // w alone: column maxima, then codes and scales (no transposed copy)
     const int rows_per_cta = 256;
     dim3 g1(static_cast<unsigned>(ceil_div(r.D_out, 32)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
@@ -443,7 +607,11 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   else
     i8_quant_rows<int8_t><<<static_cast<unsigned>(r.B), 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales,
                                                                      reinterpret_cast<int8_t*>(xpad));
-  if ((r.D_out % 4) == 0 && (reinterpret_cast<uintptr_t>(r.w) & 15) == 0) {
+  if (w_strip) {
+    e = tc ? launch_w_strip<__nv_bfloat16>(r, Kp, reinterpret_cast<__nv_bfloat16*>(wpadT), s)
+           : launch_w_strip<int8_t>(r, Kp, reinterpret_cast<int8_t*>(wpadT), s);
+    if (e != cudaSuccess) return e;
+  } else if ((r.D_out % 4) == 0 && (reinterpret_cast<uintptr_t>(r.w) & 15) == 0) {
     const int rows_per_cta = 256;
     dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 128)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
     i8_colmax4<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
@@ -452,7 +620,7 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 32)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
     i8_colmax<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
   }
-  {
+  if (!w_strip) {
     dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 64)), static_cast<unsigned>(Kp / 64));
     if (tc)
       i8_quant_cols<__nv_bfloat16><<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales,
