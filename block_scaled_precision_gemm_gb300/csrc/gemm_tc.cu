@@ -49,7 +49,7 @@ constexpr int kGroupM = 16;
 constexpr int kStagingPerWarp = 2 * 4096;  // two 32-row x 128-byte buffers
 
 enum Site { kSiteProducer = 1, kSiteMmaTmem = 2, kSiteMmaFull = 3, kSiteEpilogue = 4, kSiteDrain = 5,
-            kSiteDone = 6, kSiteSelftest = 7 };
+            kSiteDone = 6, kSiteSelftest = 7, kSiteSplitK = 8 };
 
 constexpr int align1024(int v) { return (v + 1023) / 1024 * 1024; }
 
@@ -68,7 +68,9 @@ struct Cfg {
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_STG = align1024(OFF_SF + STAGES * SF_BYTES);
   static constexpr int OFF_BAR = OFF_STG + kEpiWarps * kStagingPerWarp;
-  static constexpr int N_BARS = 2 * STAGES + 2 * 4 + 1;
+  // full/empty per stage, tfull/tempty per accumulator, done, and (split K)
+  // red_full/red_empty per epilogue warp
+  static constexpr int N_BARS = 2 * STAGES + 2 * 4 + 1 + 2 * kEpiWarps;
   static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;  // + alignment slack
   // tensor-memory columns: NACC accumulators of BN columns, then scale factors
   static constexpr int NACC = MODE == kF32Scale ? kTmemCols / BN : 2;
@@ -93,6 +95,9 @@ struct Params {
   const float* a_scales;
   const float* b_scales;
   int kb;  // K / 128
+  // split K (FP32-scale path): clusters of `splits` CTAs share each tile,
+  // CTA rank r taking K tiles r * kpb .. min((r + 1) * kpb, k_tiles) - 1
+  int splits, kpb;
   // output
   void* y;
   int y_bf16;
@@ -135,7 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + C::NACC;
   uint64_t* done = tempty + C::NACC;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* red_full = done + 1;              // split K, in the leader: the peers' partials are staged
+  uint64_t* red_empty = red_full + kEpiWarps;  // split K, in each peer: the leader has read them
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_empty + kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int never_abort_storage = 0;  // drains ignore the CTA abort flag
   volatile int* never_abort = &never_abort_storage;
@@ -151,6 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[i], kEpiWarps);
     }
     mbar_init(done, 1);
+    for (int i = 0; i < kEpiWarps; ++i) {
+      mbar_init(&red_full[i], p.splits > 1 ? p.splits - 1 : 1);
+      mbar_init(&red_empty[i], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -161,8 +172,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.splits > 1) cluster_sync();  // every CTA's barriers are initialized before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // Split K: cluster `cid` of `ncl` works on tiles cid, cid + ncl, ..; this
+  // CTA (rank `krank`) on K tiles kbeg .. kend - 1 of each.
+  const int krank = p.splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cid = blockIdx.x / p.splits, ncl = gridDim.x / p.splits;
+  const int kbeg = krank * p.kpb;
+  const int kend = min(kbeg + p.kpb, p.k_tiles);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -170,10 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = cid; ok && t < p.num_tiles; t += ncl) {
         int b, mb, nb;
         decode_tile(p, t, b, mb, nb);
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = kbeg; kt < kend; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteProducer)) {
             ok = false;
             break;
@@ -212,12 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, tb = 0;
       uint32_t phase = 0, tph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = cid; ok && t < p.num_tiles; t += ncl) {
         if constexpr (MODE != kF32Scale) {
           if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) break;
           tc_fence_after();
         }
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = kbeg; kt < kend; ++kt) {
           if constexpr (MODE == kF32Scale) {
             if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
               ok = false;
@@ -262,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 4; ++k) {
               const uint64_t ad = smem_desc(a_base + 32 * k, 16, 1024, 2);
               const uint64_t bd = smem_desc(b_base + 32 * k, 16, 1024, 2);
-              const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
+              const uint32_t acc = (kt > kbeg || k > 0) ? 1u : 0u;
               if constexpr (MODE == kMXF8) {
                 // one byte of the 4-byte scale word per 32-K step
                 const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
@@ -300,8 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* my_stg = stg + ew * kStagingPerWarp;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int tb = 0, sbuf = 0;
-    uint32_t tph = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    uint32_t tph = 0, rph = 0;
+    for (int t = cid; t < p.num_tiles; t += ncl) {
       int b, mb, nb;
       decode_tile(p, t, b, mb, nb);
       const int row = mb * BM + q * 32 + lane;
@@ -314,11 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = row < p.M;
         const float* sa_row = p.a_scales + static_cast<size_t>(row_ok ? row : 0) * p.kb;
         const float* sb_row = p.b_scales + static_cast<size_t>(col0 / 128) * p.kb;
-        float sa_next = row_ok ? __ldg(sa_row) : 0.f;
-        float sb_next = __ldg(sb_row);
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        float sa_next = row_ok ? __ldg(sa_row + kbeg) : 0.f;
+        float sb_next = __ldg(sb_row + kbeg);
+        for (int kt = kbeg; kt < kend; ++kt) {
           const float s = sa_next * sb_next;
-          if (kt + 1 < p.k_tiles) {
+          if (kt + 1 < kend) {
             sa_next = row_ok ? __ldg(sa_row + kt + 1) : 0.f;
             sb_next = __ldg(sb_row + kt + 1);
           }
@@ -382,6 +400,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
+      if constexpr (MODE == kF32Scale) {
+        if (p.splits > 1) {
+          // Split K: each peer stages its partial sums (32 rows x 64 columns
+          // per warp, 16-byte units rotated by lane) and signals the leader,
+          // which adds them in rank order and stores the tile.
+          const uint32_t part = smem_u32(my_stg);
+          if (krank != 0) {
+            if (!mbar_wait_acq_cluster(&red_empty[ew], rph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteSplitK))
+              break;
+#pragma unroll
+            for (int j = 0; j < COLS / 4; ++j)
+              *reinterpret_cast<float4*>(my_stg + 16 * (lane * 16 + (j ^ (lane & 15)))) =
+                  make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_release_cluster(mapa_shared(smem_u32(&red_full[ew]), 0));
+            rph ^= 1u;
+            continue;
+          }
+          if (!mbar_wait_acq_cluster(&red_full[ew], rph, p.timeout_ns, abort_flag, p.status, kSiteSplitK)) break;
+          for (int r = 1; r < p.splits; ++r) {
+            const uint32_t peer = mapa_shared(part, static_cast<uint32_t>(r));
+#pragma unroll
+            for (int j = 0; j < COLS / 4; ++j) {
+              const float4 v = ld_shared_cluster_v4(peer + 16 * (lane * 16 + (j ^ (lane & 15))));
+              acc[4 * j] += v.x;
+              acc[4 * j + 1] += v.y;
+              acc[4 * j + 2] += v.z;
+              acc[4 * j + 3] += v.w;
+            }
+          }
+          __syncwarp();
+          if (lane == 0)
+            for (int r = 1; r < p.splits; ++r)
+              mbar_arrive_release_cluster(mapa_shared(smem_u32(&red_empty[ew]), static_cast<uint32_t>(r)));
+          rph ^= 1u;
+        }
+      }
       // ---- store the thread's row segment [col0, col0 + COLS)
       if (p.tma_store) {
         const int y0 = mb * BM + q * 32;
@@ -448,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (p.splits > 1) cluster_sync();  // no CTA exits while a peer may still touch its shared memory
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -586,15 +642,41 @@ __global__ void selftest_wait_kernel(uint64_t timeout_ns, int* status) {
 int rt_rows(int64_t R) { return static_cast<int>(ceil_div(R, 256) * 2); }  // row tiles, even for BN = 256
 
 template <int MODE, int BN, int STAGES>
-cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const Params& p,
+cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const Params& p_in,
                           const DeviceCtx* ctx, cudaStream_t s) {
   using C = Cfg<MODE, BN, STAGES>;
   auto kern = tc_gemm<MODE, BN, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const int grid = std::max(1, std::min(p.num_tiles, ctx->num_sms));
-  kern<<<grid, kThreads, C::SMEM, s>>>(ta, tb, ty, p);
-  return cudaGetLastError();
+  Params p = p_in;
+  if (p.splits <= 1) {
+    p.splits = 1;
+    p.kpb = p.k_tiles;
+    const int grid = std::max(1, std::min(p.num_tiles, ctx->num_sms));
+    kern<<<grid, kThreads, C::SMEM, s>>>(ta, tb, ty, p);
+    return cudaGetLastError();
+  }
+  // split K: clusters of `splits` CTAs, one tile per cluster at a time, as
+  // many clusters as fit at once (the GPCs' SM counts need not be multiples
+  // of the cluster size)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.splits * (ctx->num_sms / p.splits)));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int fit = 0;
+  e = cudaOccupancyMaxActiveClusters(&fit, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  const int ncl = std::max(1, std::min(p.num_tiles, fit));
+  cfg.gridDim = dim3(static_cast<unsigned>(ncl * p.splits));
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
 }
 
 uint32_t f8_fmt(int dtype) { return dtype == BSMM_E5M2 ? 1u : 0u; }
@@ -766,6 +848,18 @@ cudaError_t launch_grouped_gemm(const GroupedGemmRequest& r, cudaStream_t s, std
   p.a_scales = r.a_scales;
   p.b_scales = r.b_scales;
   p.kb = static_cast<int>(r.K / 128);
+  // Split K in two when the tiles leave half the SMs idle and each half keeps
+  // at least 16 K tiles.  Measured (one-CTA kernel, us for 1 / 2 splits):
+  // m=512 n=2048 k=8192 29.3 / 23.5, m=237 n=k=4096 17.9 / 17.7, m=349
+  // n=k=2048 13.2 / 15.7 (8 K tiles a split: the tile's fixed costs, pipeline
+  // fill, cross-CTA sum and store, outweigh the shorter K loop).  Eight
+  // splits of m=256 n=1024 k=16384 ran slower than one (66.4 / 52.3).
+  // BSMM_GROUPED_SPLITK=n forces n splits, up to 8 (at least one K tile each).
+  int splits = 1;
+  if (2 * p.num_tiles <= ctx->num_sms && p.k_tiles >= 32) splits = 2;
+  if (const char* fs = std::getenv("BSMM_GROUPED_SPLITK")) splits = std::max(1, std::min({8, std::atoi(fs), p.k_tiles}));
+  p.kpb = static_cast<int>(ceil_div(p.k_tiles, splits));
+  p.splits = static_cast<int>(ceil_div(p.k_tiles, p.kpb));  // no empty split
   p.y = r.y;
   p.y_bf16 = 0;
   p.tma_store = make_output_map(&ty, r.y, false, 1, r.M, r.N) ? 1 : 0;

@@ -184,10 +184,14 @@ def test_linear_backward_sampled(device):
     _free()
 
 
-def test_e2e_pipelined_chunks_match_the_plain_step(device):
+def test_e2e_pipelined_chunks_match_the_plain_step(device, monkeypatch):
     """bench.py's end-to-end step splits each problem into row chunks over
     three streams; every output row depends on its own row alone, so the
-    results must equal the plain step's bit for bit."""
+    results must equal the plain step's bit for bit.  (Split K, chosen by a
+    call's tile count, changes the order of the FP32 sums; it is held at one
+    split here because these chunks are far smaller than the Shapes-table
+    problems, whose 65536-row chunks all run on the CTA-pair kernel.)"""
+    monkeypatch.setenv("BSMM_GROUPED_SPLITK", "1")
     wl_spec = W.Workload("chunked e2e check", 5, (W.Grouped(1000, 256, 384), W.Grouped(3000, 512, 256)))
     wl = bench.GroupedWork(wl_spec, device)
     wl.E2E_ROWS = 256
@@ -206,6 +210,7 @@ def test_e2e_pipelined_chunks_match_the_plain_step(device):
     wl.step_e2e()
     torch.cuda.synchronize()
     for it, r in zip(wl.items, ref):
-        assert torch.equal(it["y"].view(torch.int32), r.view(torch.int32))
+        diff = (it["y"].view(torch.int32) != r.view(torch.int32)).sum().item()
+        assert diff == 0, f"m={it['p'].m} n={it['p'].n} k={it['p'].k}: {diff} entries differ"
     del wl
     _free()

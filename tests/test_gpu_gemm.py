@@ -75,6 +75,52 @@ def test_grouped_parity_each_kernel(monkeypatch, kernel, m, n, k):
     assert_within(y, y_ref, bound, f"grouped[{kernel}] m={m} n={n} k={k}")
 
 
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("m,n,k", [(349, 256, 2048), (237, 384, 1280), (64, 128, 640)])
+def test_grouped_split_k(monkeypatch, splits, m, n, k):
+    """Split K on the one-CTA FP32-scale kernel (a cluster of `splits` CTAs
+    per tile, partial sums added in rank order through distributed shared
+    memory), including splits that do not divide the K tiles evenly."""
+    monkeypatch.setenv("BSMM_GROUPED_KERNEL", "single")
+    monkeypatch.setenv("BSMM_GROUPED_SPLITK", str(splits))
+    y, y_ref, bound = run_grouped(*grouped_inputs(m, n, k, seed=m + 7 * splits))
+    assert_within(y, y_ref, bound, f"split-K {splits}: m={m} n={n} k={k}")
+
+
+def test_grouped_split_k_is_deterministic(monkeypatch):
+    """The split partials are added in a fixed order: repeated calls give
+    identical bits."""
+    monkeypatch.setenv("BSMM_GROUPED_KERNEL", "single")
+    monkeypatch.setenv("BSMM_GROUPED_SPLITK", "4")
+    ca, sa, cb, sb = grouped_inputs(300, 256, 2048, seed=5)
+    bsmm = _bsmm()
+    args = [torch.from_numpy(v).cuda() for v in (ca, cb, sa, sb)]
+    y1 = bsmm.gemm_grouped(*args, 128, 128)
+    y2 = bsmm.gemm_grouped(*args, 128, 128)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("m,n", [(349, 2048), (237, 4096)])
+def test_grouped_small_m_sweep_shapes(m, n):
+    """The Shapes-table problems with fewer 128 x 128 tiles than SMs take
+    split K by default; full size, checked against the oracle on sampled
+    rows."""
+    bsmm = _bsmm()
+    g = torch.Generator().manual_seed(m)
+    a_raw = torch.randn(m, n, generator=g).numpy()
+    b_raw = torch.randn(n, n, generator=g).numpy()
+    ca, sa = Q.quantize(a_raw, (1, 128), "e4m3", "f32")
+    cb, sb = Q.quantize(b_raw, (128, 128), "e4m3", "f32")
+    y = bsmm.gemm_grouped(torch.from_numpy(ca).cuda(), torch.from_numpy(cb).cuda(), torch.from_numpy(sa).cuda(),
+                          torch.from_numpy(sb).cuda(), 128, 128).cpu().numpy()
+    rows = np.array([0, 1, m // 2, m - 1])
+    da, db = F.decode(ca[rows], "e4m3"), F.decode(cb, "e4m3")
+    y_ref = G.grouped_matmul(da, db, sa[rows], sb, 128, 128)
+    a_s, b_s = G.grouped_operands(da, db, sa[rows], sb, 128, 128)
+    assert_within(y[rows], y_ref, np.abs(a_s) @ np.abs(b_s).T, f"small-m sweep shape m={m} n=k={n}")
+
+
 def test_grouped_e5m2_operands():
     ca, sa, _, _ = grouped_inputs(100, 256, 256, 5, "e5m2")
     _, _, cb, sb = grouped_inputs(100, 256, 256, 6, "e4m3")
