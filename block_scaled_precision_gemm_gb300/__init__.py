@@ -29,6 +29,7 @@ __all__ = [
     "BsmmError", "lib", "library_path", "quantize", "gemm", "gemm_noalloc", "gemm_grouped", "int8_channel",
     "linear_backward", "gemm_workspace_size", "int8_channel_workspace_size",
     "linear_backward_workspace_size", "check_device_status", "selftest_wait_timeout",
+    "scale_atoms_size", "quantize_atoms", "gemm_atoms", "linear_backward_quantized",
     "set_wait_timeout_ns", "version",
     "F32", "BF16", "E4M3", "E5M2", "E2M1", "INT8", "SCALE_F32", "SCALE_UE8M0", "SCALE_UE4M3",
 ]
@@ -76,6 +77,12 @@ _SIGS = {
     "bsmm_int8_channel": ([_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _INT),
     "bsmm_linear_backward_workspace_size": ([_I64, _I64, _I64], _SZ),
     "bsmm_linear_backward": ([_P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _SZ, _P], _INT),
+    "bsmm_scale_atoms_size": ([_I64, _I64, _I64, _INT, _INT], _SZ),
+    "bsmm_quantize_atoms": ([_P, _INT, _I64, _I64, _I64, _INT, _INT, _INT, _P, _P, _SZ, _P], _INT),
+    "bsmm_gemm_atoms": ([_I64, _I64, _I64, _I64, _P, _INT, _P, _INT, _P, _P, _INT, _P, _INT, _P, _SZ, _P], _INT),
+    "bsmm_linear_backward_quantized_workspace_size": ([_I64, _I64, _I64, _INT], _SZ),
+    "bsmm_linear_backward_quantized": ([_I64, _I64, _I64, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _INT, _P, _P, _P,
+                                        _SZ, _P], _INT),
 }
 
 
@@ -301,4 +308,87 @@ def linear_backward(dY, W, X, fp8="e5m2", dX=None, dW=None, workspace=None, stre
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _check(lib().bsmm_linear_backward(_ptr(dY), _ptr(W), _ptr(X), M, N, K, _code(fp8), _ptr(dX), _ptr(dW),
                                       _ptr(workspace), workspace.numel(), _stream(stream)), "bsmm_linear_backward")
+    return dX, dW
+
+
+# --------------------------------------------------------------------------- #
+# Scales in the tensor cores' atom layout                                     #
+# --------------------------------------------------------------------------- #
+
+def scale_atoms_size(B, rows, K, code="e4m3", scale="ue8m0") -> int:
+    return lib().bsmm_scale_atoms_size(B, rows, K, _code(code), _scale(scale))
+
+
+def quantize_atoms(x, code="e4m3", scale="ue8m0", batches=1, transpose=False, codes=None, atoms=None, stream=None):
+    """Quantize a GEMM operand with its scales written in the atom layout.
+
+    ``x`` is [batches * rows, K] (or [K, rows] with ``transpose``); returns
+    ``(codes, atoms)``: codes [batches * rows, K] (E2M1 packed: K/2 bytes a
+    row) and the atoms as a flat uint8 tensor."""
+    _dev(x, "x")
+    if x.dim() != 2 or x.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("x must be a 2-D float32 or bfloat16 tensor")
+    c, s = _code(code), _scale(scale)
+    if transpose:
+        K, rows = x.shape
+    else:
+        total, K = x.shape
+        rows = total // batches
+    if codes is None:
+        codes = torch.empty((batches * rows, K // 2 if c == E2M1 else K), dtype=torch.uint8, device=x.device)
+    need = scale_atoms_size(batches, rows, K, c, s)
+    if atoms is None:
+        atoms = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _check(lib().bsmm_quantize_atoms(_ptr(x), BF16 if x.dtype == torch.bfloat16 else F32, batches, rows, K,
+                                     1 if transpose else 0, c, s, _ptr(codes), _ptr(atoms), atoms.numel(),
+                                     _stream(stream)), "bsmm_quantize_atoms")
+    return codes, atoms
+
+
+def gemm_atoms(a, b, a_atoms, b_atoms, a_type="e4m3", b_type="e4m3", scale="ue8m0", out_dtype=torch.float32,
+               y=None, workspace=None, K=None, stream=None):
+    """:func:`gemm` with both operands' scales in the atom layout."""
+    for t, n in ((a, "a"), (b, "b"), (a_atoms, "a_atoms"), (b_atoms, "b_atoms")):
+        _dev(t, n)
+    at, bt = _code(a_type), _code(b_type)
+    if a.dim() == 2:
+        a, b = a[None], b[None]
+    Bn, M, ka = a.shape
+    N = b.shape[1]
+    if K is None:
+        K = ka * 2 if at == E2M1 else ka
+    if y is None:
+        y = torch.empty((Bn, M, N), dtype=out_dtype, device=a.device)
+    if workspace is None and at == E2M1:
+        workspace = torch.empty(max(gemm_workspace_size(Bn, M, N, K, at), 1), dtype=torch.uint8, device=a.device)
+    _check(lib().bsmm_gemm_atoms(Bn, M, N, K, _ptr(a), at, _ptr(b), bt, _ptr(a_atoms), _ptr(b_atoms),
+                                 _scale(scale), _ptr(y), BF16 if y.dtype == torch.bfloat16 else F32,
+                                 _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream)),
+           "bsmm_gemm_atoms")
+    return y
+
+
+def linear_backward_quantized(dy_n, dy_n_scales, w_t, w_t_scales, dy_t, dy_t_scales, x_t, x_t_scales,
+                              fp8="e5m2", scales_are_atoms=False, dX=None, dW=None, workspace=None, stream=None):
+    """The backward's two GEMMs from pre-quantized operands: dY along N
+    [M, N], W^T [K, N], dY^T [N, M], X^T [K, M] with their scales (row-major,
+    or atoms).  Returns ``(dX, dW)`` in bfloat16."""
+    for t, n in ((dy_n, "dy_n"), (w_t, "w_t"), (dy_t, "dy_t"), (x_t, "x_t"), (dy_n_scales, "dy_n_scales"),
+                 (w_t_scales, "w_t_scales"), (dy_t_scales, "dy_t_scales"), (x_t_scales, "x_t_scales")):
+        _dev(t, n)
+    M, N = dy_n.shape
+    K = w_t.shape[0]
+    dev = dy_n.device
+    if dX is None:
+        dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if dW is None:
+        dW = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    need = lib().bsmm_linear_backward_quantized_workspace_size(M, N, K, 1 if scales_are_atoms else 0)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(lib().bsmm_linear_backward_quantized(M, N, K, _code(fp8), _ptr(dy_n), _ptr(dy_n_scales), _ptr(w_t),
+                                                _ptr(w_t_scales), _ptr(dy_t), _ptr(dy_t_scales), _ptr(x_t),
+                                                _ptr(x_t_scales), 1 if scales_are_atoms else 0, _ptr(dX), _ptr(dW),
+                                                _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                                                _stream(stream)), "bsmm_linear_backward_quantized")
     return dX, dW

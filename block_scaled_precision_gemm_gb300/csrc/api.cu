@@ -128,6 +128,38 @@ GemmRoute route_gemm(int at, int bt, int st, int64_t K, int64_t K_a, int64_t K_b
   return {true, tensor, fmt, ""};
 }
 
+// The format of a GEMM operand quantized with hardware blocks: FP8 codes take
+// UE8M0 per 32 (MXFP8); E2M1 takes UE8M0 per 32 (MXFP4) or UE4M3 per 16
+// (NVFP4).  -1: no tensor-core format.
+int atom_format(int code, int scale) {
+  if ((code == BSMM_E4M3 || code == BSMM_E5M2) && scale == BSMM_SCALE_UE8M0) return kFmtMXF8;
+  if (code == BSMM_E2M1 && scale == BSMM_SCALE_UE8M0) return kFmtMXF4;
+  if (code == BSMM_E2M1 && scale == BSMM_SCALE_UE4M3) return kFmtNVF4;
+  return -1;
+}
+
+// Quantize a GEMM operand of B x rows x K (contraction K) with its scales
+// written straight into the plain atom layout; the atoms are first filled
+// with the neutral scale (UE8M0 127 = 1.0, UE4M3 0) so that padding rows and
+// blocks past K contribute nothing.  transpose_in: x is [K][rows] (B == 1).
+cudaError_t quantize_to_atoms(const void* x, bool bf16, int64_t B, int64_t rows, int64_t K, bool transpose_in,
+                              int code, int scale, void* codes, void* atoms, cudaStream_t s) {
+  const int fmt = atom_format(code, scale);
+  const int bs = fmt == kFmtNVF4 ? 16 : 32;
+  const int per_tile = fmt == kFmtNVF4 ? 4 : (fmt == kFmtMXF4 ? 2 : 1);
+  const int64_t k_tiles = ceil_div(K, fmt == kFmtMXF8 ? 128 : 256);
+  cudaError_t e = cudaMemsetAsync(atoms, scale == BSMM_SCALE_UE4M3 ? 0 : 127, sf_atoms_plain_bytes(B, rows, K, fmt), s);
+  if (e != cudaSuccess) return e;
+  QuantRequest q = transpose_in
+                       ? QuantRequest{x, bf16, K, rows, rows, bs, 1, code, scale, true, codes, K, atoms, 1}
+                       : QuantRequest{x, bf16, B * rows, K, K, 1, bs, code, scale, false, codes, K, atoms, 1};
+  q.sf_atoms = true;
+  q.sf_rows = rows;
+  q.sf_rt = ceil_div(rows, 256) * 2;
+  q.sf_ks4 = k_tiles * per_tile;
+  return launch_quantize(q, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -253,6 +285,72 @@ bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K, const void* a,
   return launched(e, "gemm launch");
 }
 
+size_t bsmm_scale_atoms_size(int64_t B, int64_t rows, int64_t K, bsmm_dtype code_type, bsmm_scale_type scale_type) {
+  const int fmt = atom_format(code_type, scale_type);
+  if (fmt < 0 || B <= 0 || rows <= 0 || K <= 0) return 0;
+  return sf_atoms_plain_bytes(B, rows, K, fmt);
+}
+
+bsmm_status bsmm_quantize_atoms(const void* x, bsmm_dtype x_type, int64_t B, int64_t rows, int64_t K,
+                                int transpose_in, bsmm_dtype code_type, bsmm_scale_type scale_type, void* codes,
+                                void* atoms, size_t atoms_bytes, bsmm_stream_t stream) {
+  if (x_type != BSMM_F32 && x_type != BSMM_BF16) return fail(BSMM_ERR_INVALID_ARG, "x_type must be F32 or BF16");
+  const int fmt = atom_format(code_type, scale_type);
+  if (fmt < 0)
+    return fail(BSMM_ERR_UNSUPPORTED, "atoms take E4M3/E5M2 or E2M1 codes with UE8M0, or E2M1 with UE4M3");
+  if (B < 0 || rows < 0 || K < 0) return fail(BSMM_ERR_INVALID_ARG, "negative size");
+  if (B == 0 || rows == 0 || K == 0) {
+    set_error("");
+    return BSMM_OK;
+  }
+  if (transpose_in && B != 1) return fail(BSMM_ERR_SHAPE, "a transposed input has one batch");
+  const int bs = fmt == kFmtNVF4 ? 16 : 32;
+  if (K % bs) return fail(BSMM_ERR_SHAPE, "K must be a multiple of the hardware block (32, or 16 for UE4M3)");
+  if (!x || !codes || !atoms) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
+  const size_t need = sf_atoms_plain_bytes(B, rows, K, fmt);
+  if (atoms_bytes < need) return fail(BSMM_ERR_WORKSPACE, "atoms need " + std::to_string(need) + " bytes");
+  if (reinterpret_cast<uintptr_t>(atoms) & 3u) return fail(BSMM_ERR_ALIGNMENT, "atoms must be 4-byte aligned");
+  return launched(quantize_to_atoms(x, x_type == BSMM_BF16, B, rows, K, transpose_in != 0, code_type, scale_type,
+                                    codes, atoms, reinterpret_cast<cudaStream_t>(stream)),
+                  "quantize (atoms) launch");
+}
+
+bsmm_status bsmm_gemm_atoms(int64_t B, int64_t M, int64_t N, int64_t K, const void* a, bsmm_dtype a_type,
+                            const void* b, bsmm_dtype b_type, const void* a_atoms, const void* b_atoms,
+                            bsmm_scale_type scale_type, void* y, bsmm_dtype y_type, void* workspace,
+                            size_t workspace_bytes, bsmm_stream_t stream) {
+  if (B < 0 || M < 0 || N < 0 || K < 0) return fail(BSMM_ERR_INVALID_ARG, "negative size");
+  if (y_type != BSMM_F32 && y_type != BSMM_BF16) return fail(BSMM_ERR_INVALID_ARG, "y_type must be F32 or BF16");
+  const int fa = atom_format(a_type, scale_type), fb = atom_format(b_type, scale_type);
+  if (fa < 0 || fb < 0 || fa != fb)
+    return fail(BSMM_ERR_UNSUPPORTED, "both operands MXFP8 (E4M3/E5M2, UE8M0), MXFP4 or NVFP4");
+  if (B == 0 || M == 0 || N == 0) {
+    set_error("");
+    return BSMM_OK;
+  }
+  if (K == 0 || K % (fa == kFmtNVF4 ? 16 : 32)) return fail(BSMM_ERR_SHAPE, "K must be a positive multiple of the block");
+  if (K % 32) return fail(BSMM_ERR_SHAPE, "K must be a multiple of 32");
+  if (!a || !b || !a_atoms || !b_atoms || !y) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(a) || !aligned16(b) || !aligned16(y) || !aligned16(a_atoms) || !aligned16(b_atoms))
+    return fail(BSMM_ERR_ALIGNMENT, "a, b, y and the atoms must be 16-byte aligned");
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2 || B > 65535)
+    return fail(BSMM_ERR_SHAPE, "size beyond the supported range");
+  if (fa != kFmtMXF8) {  // the pair kernel's skewed / replicated blocks are written from the atoms
+    const size_t need = bsmm_gemm_workspace_size(B, M, N, K, a_type);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return fail(BSMM_ERR_WORKSPACE, "workspace must be 256-byte aligned and at least " + std::to_string(need) +
+                                          " bytes");
+  }
+  const int64_t hw = fa == kFmtNVF4 ? 16 : 32;
+  MxGemmRequest r{B, M, N, K, a, b, a_type, b_type, static_cast<const uint8_t*>(a_atoms),
+                  static_cast<const uint8_t*>(b_atoms), fa, y, y_type == BSMM_BF16, workspace, K / hw, K / hw};
+  r.sf_atoms = true;
+  std::string why;
+  const cudaError_t e = launch_mx_gemm(r, reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess && !why.empty()) return fail(BSMM_ERR_CUDA, why);
+  return launched(e, "gemm (atoms) launch");
+}
+
 bsmm_status bsmm_gemm_noalloc(int64_t B, int64_t M, int64_t N, int64_t K, const void* a, bsmm_dtype a_type,
                               const void* b, bsmm_dtype b_type, const void* a_scales, int64_t K_a,
                               const void* b_scales, int64_t K_b, bsmm_scale_type scale_type, void* y,
@@ -359,17 +457,38 @@ bsmm_status bsmm_int8_channel(const float* x, const float* w, int64_t B, int64_t
 
 size_t bsmm_linear_backward_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  // codes: dY along N [M,N], W^T [K,N], dY^T [N,M], X^T [K,M]; UE8M0 scales of each
+  // codes: dY along N [M,N], W^T [K,N], dY^T [N,M], X^T [K,M]; the UE8M0
+  // scales of each in the tensor-core atom layout, read in place by the GEMMs
   size_t total = 0;
-  total += align_up(static_cast<size_t>(M * N), 256) + align_up(static_cast<size_t>(M * (N / 32)), 256);
-  total += align_up(static_cast<size_t>(K * N), 256) + align_up(static_cast<size_t>(K * (N / 32)), 256);
-  total += align_up(static_cast<size_t>(N * M), 256) + align_up(static_cast<size_t>(N * (M / 32)), 256);
-  total += align_up(static_cast<size_t>(K * M), 256) + align_up(static_cast<size_t>(K * (M / 32)), 256);
-  const size_t g1 = bsmm_gemm_workspace_size(1, M, K, N, BSMM_E4M3);
-  const size_t g2 = bsmm_gemm_workspace_size(1, N, K, M, BSMM_E4M3);
-  total += align_up(g1 > g2 ? g1 : g2, 256);
+  total += align_up(static_cast<size_t>(M * N), 256) + align_up(sf_atoms_plain_bytes(1, M, N, kFmtMXF8), 256);
+  total += align_up(static_cast<size_t>(K * N), 256) + align_up(sf_atoms_plain_bytes(1, K, N, kFmtMXF8), 256);
+  total += align_up(static_cast<size_t>(N * M), 256) + align_up(sf_atoms_plain_bytes(1, N, M, kFmtMXF8), 256);
+  total += align_up(static_cast<size_t>(K * M), 256) + align_up(sf_atoms_plain_bytes(1, K, M, kFmtMXF8), 256);
   return total;
 }
+
+namespace {
+// dX = dY . W and dW = dY^T . X from the four quantized operands.
+bsmm_status backward_gemms(int64_t M, int64_t N, int64_t K, int ft, const void* dy_n, const void* dy_n_s,
+                           const void* wt, const void* wt_s, const void* dyt, const void* dyt_s, const void* xt,
+                           const void* xt_s, bool atoms, void* dX, void* dW, void* gws, cudaStream_t s) {
+  std::string why;
+  // dX [M, K] = dY [M, N] . (W^T [K, N])^T, contraction over N
+  MxGemmRequest g1{1, M, K, N, dy_n, wt, ft, ft, static_cast<const uint8_t*>(dy_n_s),
+                   static_cast<const uint8_t*>(wt_s), kFmtMXF8, dX, true, gws, N / 32, N / 32};
+  g1.sf_atoms = atoms;
+  cudaError_t e = launch_mx_gemm(g1, s, &why);
+  if (e != cudaSuccess) return why.empty() ? cuda_fail(e, "dX gemm launch") : fail(BSMM_ERR_CUDA, why);
+  // dW [N, K] = dY^T [N, M] . (X^T [K, M])^T, contraction over M
+  MxGemmRequest g2{1, N, K, M, dyt, xt, ft, ft, static_cast<const uint8_t*>(dyt_s),
+                   static_cast<const uint8_t*>(xt_s), kFmtMXF8, dW, true, gws, M / 32, M / 32};
+  g2.sf_atoms = atoms;
+  e = launch_mx_gemm(g2, s, &why);
+  if (e != cudaSuccess) return why.empty() ? cuda_fail(e, "dW gemm launch") : fail(BSMM_ERR_CUDA, why);
+  set_error("");
+  return BSMM_OK;
+}
+}  // namespace
 
 bsmm_status bsmm_linear_backward(const void* dY, const void* W, const void* X, int64_t M, int64_t N, int64_t K,
                                  bsmm_dtype fp8_type, void* dX, void* dW, void* workspace, size_t workspace_bytes,
@@ -396,47 +515,67 @@ bsmm_status bsmm_linear_backward(const void* dY, const void* W, const void* X, i
     return r;
   };
   uint8_t* dy_n = take(M * N);
-  uint8_t* dy_n_s = take(M * (N / 32));
+  uint8_t* dy_n_s = take(sf_atoms_plain_bytes(1, M, N, kFmtMXF8));
   uint8_t* wt = take(K * N);
-  uint8_t* wt_s = take(K * (N / 32));
+  uint8_t* wt_s = take(sf_atoms_plain_bytes(1, K, N, kFmtMXF8));
   uint8_t* dyt = take(N * M);
-  uint8_t* dyt_s = take(N * (M / 32));
+  uint8_t* dyt_s = take(sf_atoms_plain_bytes(1, N, M, kFmtMXF8));
   uint8_t* xt = take(K * M);
-  uint8_t* xt_s = take(K * (M / 32));
-  uint8_t* gws = p;
-  const size_t gws_bytes = workspace_bytes - static_cast<size_t>(gws - static_cast<uint8_t*>(workspace));
+  uint8_t* xt_s = take(sf_atoms_plain_bytes(1, K, M, kFmtMXF8));
 
+  // Each operand quantized along its GEMM's contraction axis, scales straight
+  // into the tensor-core atom layout (no relayout before the GEMMs).
   const int ft = fp8_type;
   struct Q {
     const void* x;
-    int64_t rows, cols;
-    int br, bc, tr;
-    uint8_t *codes, *scales;
-    int64_t ldc, lds;
+    int64_t rows, K;  // the GEMM operand: rows x K
+    bool tr;          // x holds the operand transposed ([K][rows])
+    uint8_t *codes, *atoms;
   } qs[4] = {
-      {dY, M, N, 1, 32, 0, dy_n, dy_n_s, N, N / 32},  // dY along N          -> [M, N]
-      {W, N, K, 32, 1, 1, wt, wt_s, N, N / 32},       // W along N, transposed -> [K, N]
-      {dY, M, N, 32, 1, 1, dyt, dyt_s, M, M / 32},    // dY along M, transposed -> [N, M]
-      {X, M, K, 32, 1, 1, xt, xt_s, M, M / 32},       // X along M, transposed  -> [K, M]
+      {dY, M, N, false, dy_n, dy_n_s},  // dY along N           -> [M, N]
+      {W, K, N, true, wt, wt_s},        // W [N,K] along N       -> W^T [K, N]
+      {dY, N, M, true, dyt, dyt_s},     // dY [M,N] along M      -> dY^T [N, M]
+      {X, K, M, true, xt, xt_s},        // X [M,K] along M       -> X^T [K, M]
   };
   for (const Q& q : qs) {
-    QuantRequest r{q.x, true, q.rows, q.cols, q.cols, q.br, q.bc, ft, BSMM_SCALE_UE8M0, q.tr != 0,
-                   q.codes, q.ldc, q.scales, q.lds};
-    const cudaError_t e = launch_quantize(r, s);
+    const cudaError_t e = quantize_to_atoms(q.x, true, 1, q.rows, q.K, q.tr, ft, BSMM_SCALE_UE8M0, q.codes, q.atoms, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward quantize launch");
   }
-  std::string why;
-  // dX [M, K] = dY [M, N] . (W^T [K, N])^T, contraction over N
-  MxGemmRequest g1{1, M, K, N, dy_n, wt, ft, ft, dy_n_s, wt_s, kFmtMXF8, dX, true, gws, N / 32, N / 32};
-  cudaError_t e = launch_mx_gemm(g1, s, &why);
-  if (e != cudaSuccess) return why.empty() ? cuda_fail(e, "dX gemm launch") : fail(BSMM_ERR_CUDA, why);
-  // dW [N, K] = dY^T [N, M] . (X^T [K, M])^T, contraction over M
-  MxGemmRequest g2{1, N, K, M, dyt, xt, ft, ft, dyt_s, xt_s, kFmtMXF8, dW, true, gws, M / 32, M / 32};
-  e = launch_mx_gemm(g2, s, &why);
-  if (e != cudaSuccess) return why.empty() ? cuda_fail(e, "dW gemm launch") : fail(BSMM_ERR_CUDA, why);
-  (void)gws_bytes;
-  set_error("");
-  return BSMM_OK;
+  return backward_gemms(M, N, K, ft, dy_n, dy_n_s, wt, wt_s, dyt, dyt_s, xt, xt_s, true, dX, dW, nullptr, s);
+}
+
+size_t bsmm_linear_backward_quantized_workspace_size(int64_t M, int64_t N, int64_t K, int scales_are_atoms) {
+  if (M <= 0 || N <= 0 || K <= 0 || scales_are_atoms) return 0;
+  const size_t g1 = bsmm_gemm_workspace_size(1, M, K, N, BSMM_E4M3);
+  const size_t g2 = bsmm_gemm_workspace_size(1, N, K, M, BSMM_E4M3);
+  return g1 > g2 ? g1 : g2;
+}
+
+bsmm_status bsmm_linear_backward_quantized(int64_t M, int64_t N, int64_t K, bsmm_dtype fp8_type, const void* dy_n,
+                                           const void* dy_n_scales, const void* w_t, const void* w_t_scales,
+                                           const void* dy_t, const void* dy_t_scales, const void* x_t,
+                                           const void* x_t_scales, int scales_are_atoms, void* dX, void* dW,
+                                           void* workspace, size_t workspace_bytes, bsmm_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return fail(BSMM_ERR_INVALID_ARG, "negative size");
+  if (fp8_type != BSMM_E5M2 && fp8_type != BSMM_E4M3) return fail(BSMM_ERR_INVALID_ARG, "fp8_type must be E5M2 or E4M3");
+  if (M == 0 || N == 0 || K == 0) {
+    set_error("");
+    return BSMM_OK;
+  }
+  if (!dy_n || !dy_n_scales || !w_t || !w_t_scales || !dy_t || !dy_t_scales || !x_t || !x_t_scales || !dX || !dW)
+    return fail(BSMM_ERR_INVALID_ARG, "null pointer");
+  if (M % 32 || N % 32 || K % 32) return fail(BSMM_ERR_SHAPE, "M, N and K must be multiples of 32");
+  for (const void* q : {dy_n, w_t, dy_t, x_t, static_cast<const void*>(dX), static_cast<const void*>(dW)})
+    if (!aligned16(q)) return fail(BSMM_ERR_ALIGNMENT, "codes and outputs must be 16-byte aligned");
+  if (scales_are_atoms)
+    for (const void* q : {dy_n_scales, w_t_scales, dy_t_scales, x_t_scales})
+      if (!aligned16(q)) return fail(BSMM_ERR_ALIGNMENT, "atoms must be 16-byte aligned");
+  const size_t need = bsmm_linear_backward_quantized_workspace_size(M, N, K, scales_are_atoms);
+  if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return fail(BSMM_ERR_WORKSPACE, "workspace must be 256-byte aligned and at least " + std::to_string(need) +
+                                        " bytes");
+  return backward_gemms(M, N, K, fp8_type, dy_n, dy_n_scales, w_t, w_t_scales, dy_t, dy_t_scales, x_t, x_t_scales,
+                        scales_are_atoms != 0, dX, dW, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

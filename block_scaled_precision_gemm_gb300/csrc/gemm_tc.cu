@@ -576,16 +576,17 @@ __global__ void __launch_bounds__(256) sf_relayout(const uint8_t* __restrict__ s
 // slot a + q (`skew`), of slot a (neither), or of each of slots 4a .. 4a + 3
 // (`replicate`); one byte per hardware block, in K order.  Missing rows and
 // blocks past K get `pad`.  Slot positions that no atom fills are never read
-// by the GEMM and are left as they are.
+// by the GEMM and are left as they are.  With src_rt > 0 the source is the
+// plain atom layout instead ([batch][src_rt row tiles][src_ks4 atoms]).
 // A thread owns one row (q, m0) of one tile of one block: it reads the row's
 // 4 * atoms scale bytes of the K tile and writes its word of every atom.
 __global__ void __launch_bounds__(256) sf_relayout_pair(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst,
                                                         int nb, int R, int KS, int NT, int k_tiles, int atoms,
                                                         int tiles, int slots, int skew, int replicate,
-                                                        uint32_t pad, int KSu, int rep) {
+                                                        uint32_t pad, int KSu, int rep, int src_rt, int src_ks4) {
   const int64_t total = static_cast<int64_t>(nb) * NT * k_tiles * tiles * 128;
   const uint32_t pad4 = pad * 0x01010101u;
-  const bool fast = rep == 1 && (KS & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 3) == 0;
+  const bool fast = src_rt == 0 && rep == 1 && (KS & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 3) == 0;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int q = static_cast<int>(idx & 3);
@@ -599,12 +600,16 @@ __global__ void __launch_bounds__(256) sf_relayout_pair(const uint8_t* __restric
     const int64_t b = t / NT;
     const int row = (T * tiles + r) * 128 + 32 * q + m0;
     uint32_t* block = dst + ((b * NT + T) * k_tiles + kt) * static_cast<int64_t>(slots) * 128;
-    const uint8_t* src_row = src + (b * R + (row < R ? row : 0)) * static_cast<int64_t>(KSu);
+    const uint8_t* src_row = src + (src_rt > 0 ? 0 : (b * R + (row < R ? row : 0)) * static_cast<int64_t>(KSu));
     for (int j = 0; j < atoms; ++j) {
       const int hb0 = 4 * (kt * atoms + j);
       uint32_t v;
       if (row >= R) {
         v = pad4;
+      } else if (src_rt > 0) {  // word (row % 128) / 32 of line row % 32 of atom hb0 / 4
+        const uint32_t* at = reinterpret_cast<const uint32_t*>(src) +
+                             ((b * src_rt + (row >> 7)) * static_cast<int64_t>(src_ks4) + (hb0 >> 2)) * 128;
+        v = __ldg(at + (row & 31) * 4 + ((row >> 5) & 3));
       } else if (fast && hb0 + 4 <= KS) {
         v = __ldg(reinterpret_cast<const uint32_t*>(src_row + hb0));
       } else {
@@ -690,6 +695,12 @@ bool make_output_map(CUtensorMap* ty, void* y, bool bf16, int64_t B, int64_t M, 
 
 }  // namespace
 
+size_t sf_atoms_plain_bytes(int64_t B, int64_t R, int64_t K, int fmt) {
+  const int64_t k_tiles = ceil_div(K, fmt == kFmtMXF8 ? 128 : 256);
+  const int atoms = fmt == kFmtNVF4 ? 4 : (fmt == kFmtMXF4 ? 2 : 1);
+  return static_cast<size_t>(B) * rt_rows(R) * k_tiles * atoms * 512;
+}
+
 size_t sf_atoms_bytes(int64_t B, int64_t R, int64_t K, int fmt) {
   // K per 128-byte tile: 128 FP8 or 256 FP4 elements; atoms per tile: one per
   // 4 scales (MXF8 1, NVF4 4, MXF4 2).  The larger of the one-CTA kernel's
@@ -728,6 +739,18 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
     *why = "MXFP4 output rows must be 16-byte aligned (N * element size % 16 == 0)";
     return cudaErrorInvalidValue;
   }
+  // Scales given in the plain atom layout (r.sf_atoms) are read in place by
+  // every kernel that takes that layout; only the pair kernel's skewed and
+  // replicated blocks are rewritten from them.
+  // One operand's plain atoms [B][RT][ks4], from row-major scale bytes.
+  auto plain_atoms = [&](const uint8_t* src, uint8_t* dst, int64_t R, int64_t KU) {
+    const int RT = rt_rows(R);
+    const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
+    const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
+    sf_relayout<<<blocks, 256, 0, s>>>(src, reinterpret_cast<uint32_t*>(dst), static_cast<int>(r.B),
+                                       static_cast<int>(R), KS, RT, ks4, pad, static_cast<int>(KU),
+                                       static_cast<int>(KS / KU));
+  };
   if (mf4 || (!want_single && (want_pair ? storable : mx_pair_eligible(r, ctx)))) {
     const int atoms = nv ? 4 : (mf4 ? 2 : 1);
     const int RTa = rt_rows(r.M), RTb = rt_rows(r.N);
@@ -735,49 +758,43 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
     const int64_t ta_threads = r.B * RTa * k_tiles * 128, tb_threads = r.B * (RTb / 2) * k_tiles * 2 * 128;
     const int ga = static_cast<int>(std::min<int64_t>(ceil_div(ta_threads, 256), ctx->num_sms * 16));
     const int gb = static_cast<int>(std::min<int64_t>(ceil_div(tb_threads, 256), ctx->num_sms * 16));
+    const int src_rta = r.sf_atoms ? RTa : 0, src_rtb = r.sf_atoms ? RTb : 0;
+    const uint8_t* use_a = sfa;
+    const uint8_t* use_b = sfb;
     if (atoms > 1) {
       sf_relayout_pair<<<ga, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
                                           static_cast<int>(r.M), KS, RTa, static_cast<int>(k_tiles), atoms, 1, sa, 1,
-                                          0, pad, static_cast<int>(r.K_a), static_cast<int>(KS / r.K_a));
-    } else {  // one atom per K tile: the pair layout is the one-CTA kernel's
-      const int64_t words = r.B * RTa * static_cast<int64_t>((ks4 + 7) / 8) * 128;
-      const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
-      sf_relayout<<<blocks, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
-                                         static_cast<int>(r.M), KS, RTa, ks4, pad, static_cast<int>(r.K_a),
-                                         static_cast<int>(KS / r.K_a));
+                                          0, pad, static_cast<int>(r.K_a), r.sf_atoms ? 1 : static_cast<int>(KS / r.K_a),
+                                          src_rta, ks4);
+    } else if (r.sf_atoms) {  // one atom per K tile: the pair layout is the plain one
+      use_a = r.a_scales;
+    } else {
+      plain_atoms(r.a_scales, sfa, r.M, r.K_a);
     }
     if (pair_b_replicated(atoms)) {
       sf_relayout_pair<<<gb, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
                                           static_cast<int>(r.N), KS, RTb / 2, static_cast<int>(k_tiles), atoms, 2, sb,
-                                          0, 1, pad, static_cast<int>(r.K_b), static_cast<int>(KS / r.K_b));
-    } else {  // the one-CTA kernel's atoms
-      const int64_t words = r.B * RTb * static_cast<int64_t>((ks4 + 7) / 8) * 128;
-      const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
-      sf_relayout<<<blocks, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
-                                         static_cast<int>(r.N), KS, RTb, ks4, pad, static_cast<int>(r.K_b),
-                                         static_cast<int>(KS / r.K_b));
+                                          0, 1, pad, static_cast<int>(r.K_b), r.sf_atoms ? 1 : static_cast<int>(KS / r.K_b),
+                                          src_rtb, ks4);
+    } else if (r.sf_atoms) {
+      use_b = r.b_scales;
+    } else {
+      plain_atoms(r.b_scales, sfb, r.N, r.K_b);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const MxAtoms at{sfa, sfb, RTa, RTb, ks4, static_cast<int>(k_tiles)};
+    const MxAtoms at{use_a, use_b, RTa, RTb, ks4, static_cast<int>(k_tiles)};
     return launch_mx_gemm_pair(r, at, s, why);
   }
 
-  {
-    const int RT = rt_rows(r.M);
-    const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
-    const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
-    sf_relayout<<<blocks, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
-                                       static_cast<int>(r.M), KS, RT, ks4, pad, static_cast<int>(r.K_a),
-                                       static_cast<int>(KS / r.K_a));
-  }
-  {
-    const int RT = rt_rows(r.N);
-    const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
-    const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
-    sf_relayout<<<blocks, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
-                                       static_cast<int>(r.N), KS, RT, ks4, pad, static_cast<int>(r.K_b),
-                                       static_cast<int>(KS / r.K_b));
+  const uint8_t* use_a = sfa;
+  const uint8_t* use_b = sfb;
+  if (r.sf_atoms) {
+    use_a = r.a_scales;
+    use_b = r.b_scales;
+  } else {
+    plain_atoms(r.a_scales, sfa, r.M, r.K_a);
+    plain_atoms(r.b_scales, sfb, r.N, r.K_b);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -797,8 +814,8 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
   p.n_tiles = static_cast<int>(ceil_div(r.N, BN));
   p.k_tiles = static_cast<int>(k_tiles);
   p.num_tiles = static_cast<int>(r.B) * p.m_tiles * p.n_tiles;
-  p.sfa = sfa;
-  p.sfb = sfb;
+  p.sfa = use_a;
+  p.sfb = use_b;
   p.sfa_rt = rt_rows(r.M);
   p.sfb_rt = rt_rows(r.N);
   p.ks4 = ks4;

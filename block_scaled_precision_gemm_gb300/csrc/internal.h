@@ -46,6 +46,11 @@ struct QuantRequest {
   int64_t ld_codes;
   void* scales;
   int64_t ld_scales;
+  // Scales in the tensor-core atom layout instead of [rows][blocks]: output
+  // row r of batch r / sf_rows, row tile ((r % sf_rows) / 128) of sf_rt per
+  // batch, sf_ks4 atoms (4 blocks each) per row tile (gemm_tc.cu, sf_relayout).
+  bool sf_atoms = false;
+  int64_t sf_rows = 0, sf_rt = 0, sf_ks4 = 0;
 };
 cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s);
 
@@ -69,7 +74,13 @@ struct MxGemmRequest {
   // hardware blocks (32 elements for UE8M0, 16 for UE4M3), which then repeat
   // its scale
   int64_t K_a, K_b;
+  // a_scales / b_scales already in the tensor-core atom layout
+  // (sf_atoms_plain_bytes): one scale per hardware block, K_a / K_b unused
+  bool sf_atoms = false;
 };
+// Bytes of one operand's scales in the plain atom layout [B][row tiles of
+// 128, rounded to pairs][K atoms], 512 each (what bsmm_quantize_atoms writes).
+size_t sf_atoms_plain_bytes(int64_t B, int64_t R, int64_t K, int fmt);
 // Any block size, CUDA cores (gemm_generic.cu); no workspace.
 cudaError_t launch_mx_gemm_generic(const MxGemmRequest& r, int64_t K_a, int64_t K_b, int scale_type,
                                    cudaStream_t s);

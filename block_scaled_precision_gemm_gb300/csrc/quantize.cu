@@ -33,7 +33,19 @@ struct QP {
   int64_t ld_codes;
   void* scales;
   int64_t ld_scales;
+  int sf_atoms;
+  int64_t sf_rows, sf_rt, sf_ks4;
 };
+
+// Where the scale of output row r, block kb goes: [rows][ld_scales], or the
+// tensor-core atom layout (512-byte atoms of 128 rows x 4 blocks; row w of
+// the tile at byte (w % 32) * 16 + (w / 32) * 4 + kb % 4).
+__device__ __forceinline__ int64_t scale_index(const QP& p, int64_t r, int64_t kb) {
+  if (!p.sf_atoms) return r * p.ld_scales + kb;
+  const int64_t b = r / p.sf_rows, rr = r - b * p.sf_rows;
+  const int w = static_cast<int>(rr & 127);
+  return ((b * p.sf_rt + (rr >> 7)) * p.sf_ks4 + (kb >> 2)) * 512 + (w & 31) * 16 + (w >> 5) * 4 + (kb & 3);
+}
 
 __device__ __forceinline__ float qmax_of(int code) {
   return code == BSMM_E4M3 ? 448.f : code == BSMM_E5M2 ? 57344.f : code == BSMM_E2M1 ? 6.f : 127.f;
@@ -210,7 +222,7 @@ __global__ void __launch_bounds__(256) quant_rows(QP p) {
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const bool fp4 = p.code == BSMM_E2M1;
-  const bool dense = p.ld_x == p.cols && p.ld_codes == p.cols && p.ld_scales * p.bc == p.cols;
+  const bool dense = p.ld_x == p.cols && p.ld_codes == p.cols && p.ld_scales * p.bc == p.cols && !p.sf_atoms;
   const int g_shift = __ffs(G) - 1;
   const In* x = reinterpret_cast<const In*>(p.x);
   uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
@@ -245,7 +257,7 @@ __global__ void __launch_bounds__(256) quant_rows(QP p) {
       if (!dense) {
         const int64_t r = si[u] / spr, c = si[u] - r * spr;
         e = r * p.ld_codes + c * kSlice;
-        sidx = r * p.ld_scales + ((c * kSlice) / p.bc);
+        sidx = scale_index(p, r, (c * kSlice) / p.bc);
       }
       if ((lane & (G - 1)) == 0) store_scale(p.scales, sidx, p.scale, sc.stored);
       uint32_t w[4];
@@ -371,8 +383,8 @@ __global__ void __launch_bounds__(256, 3) quant_cols(QP p, int vec_ok, int tiles
       const int64_t blk0 = (r0 + rbase) / br;
       const bool writes_a = (rbase % br) == 0;
       if (p.transpose) {
-        if (writes_a) store_scale(p.scales, gc * p.ld_scales + blk0, p.scale, sa.stored);
-        if (br == 16) store_scale(p.scales, gc * p.ld_scales + blk0 + 1, p.scale, sb.stored);
+        if (writes_a) store_scale(p.scales, scale_index(p, gc, blk0), p.scale, sa.stored);
+        if (br == 16) store_scale(p.scales, scale_index(p, gc, blk0 + 1), p.scale, sb.stored);
       } else {
         if (writes_a) store_scale(p.scales, blk0 * p.ld_scales + gc, p.scale, sa.stored);
         if (br == 16) store_scale(p.scales, (blk0 + 1) * p.ld_scales + gc, p.scale, sb.stored);
@@ -534,7 +546,9 @@ __global__ void __launch_bounds__(256) quant_cols_tma(const __grid_constant__ CU
     }
     if (t < nc) {  // this column's scale bytes for the tile's rows
       const int nblk = (nr + br - 1) / br;
-      uint8_t* dst = reinterpret_cast<uint8_t*>(p.scales) + (c0 + t) * p.ld_scales + r0 / br;
+      // (atom layout: r0 / br is a multiple of 4, so the tile's blocks are the
+      // consecutive bytes of one word)
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.scales) + scale_index(p, c0 + t, r0 / br);
       if (nblk == 4 && (reinterpret_cast<uintptr_t>(dst) & 3) == 0)
         *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(&sstg[t][0]);
       else
@@ -620,7 +634,7 @@ __global__ void __launch_bounds__(256) quant_wrow(QP p) {
 #pragma unroll
   for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
   const Scale sc = make_scale(m, p.code, p.scale);
-  if (t == 0) store_scale(p.scales, r * p.ld_scales, p.scale, sc.stored);
+  if (t == 0) store_scale(p.scales, scale_index(p, r, 0), p.scale, sc.stored);
   uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
   if (p.code == BSMM_E2M1) {
     for (int64_t c = 2 * t; c < p.cols; c += 512) {
@@ -651,7 +665,7 @@ __global__ void __launch_bounds__(256) quant_wcol(QP p) {
 #pragma unroll
   for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i][lane]);
   const Scale sc = make_scale(m, p.code, p.scale);
-  if (warp == 0 && cok) store_scale(p.scales, c, p.scale, sc.stored);
+  if (warp == 0 && cok) store_scale(p.scales, p.transpose ? scale_index(p, c, 0) : c, p.scale, sc.stored);
   uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
   const bool fp4 = p.code == BSMM_E2M1;
   if (p.transpose) {
@@ -693,7 +707,7 @@ __global__ void __launch_bounds__(256) quant_any(QP p) {
   for (int i = 0; i < p.br; ++i)
     for (int j = 0; j < p.bc; ++j) m = fmaxf(m, fabsf(load1<In>(x, (bi * p.br + i) * p.ld_x + bj * p.bc + j)));
   const Scale sc = make_scale(m, p.code, p.scale);
-  store_scale(p.scales, p.transpose ? bj * p.ld_scales + bi : bi * p.ld_scales + bj, p.scale, sc.stored);
+  store_scale(p.scales, p.transpose ? scale_index(p, bj, bi) : scale_index(p, bi, bj), p.scale, sc.stored);
   uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
   for (int i = 0; i < p.br; ++i) {
     for (int j = 0; j < p.bc; ++j) {
@@ -770,7 +784,7 @@ cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s) {
   const DeviceCtx* ctx = device_ctx();
   if (!ctx) return cudaErrorInitializationError;
   QP p{q.x, q.rows, q.cols, q.ld_x, q.br, q.bc, q.code, q.scale, q.transpose ? 1 : 0,
-       q.codes, q.ld_codes, q.scales, q.ld_scales};
+       q.codes, q.ld_codes, q.scales, q.ld_scales, q.sf_atoms ? 1 : 0, q.sf_rows, q.sf_rt, q.sf_ks4};
   // UE8M0 scales are powers of two: the codes divide by multiplying with the
   // exact reciprocal.
   const bool pow2 = q.scale == BSMM_SCALE_UE8M0;

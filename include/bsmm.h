@@ -293,7 +293,7 @@ bsmm_status bsmm_int8_channel(const float* x, const float* w, int64_t B, int64_t
  *   dY [M, N], W [N, K], X [M, K] bfloat16, contiguous.
  *   dX [M, K], dW [N, K] bfloat16, contiguous.
  *   workspace  at least bsmm_linear_backward_workspace_size() bytes (the
- *            four quantized operands and their scales).
+ *            four quantized operands, their scales in the atom layout below).
  *   M, N and K must be multiples of 32.
  */
 size_t bsmm_linear_backward_workspace_size(int64_t M, int64_t N, int64_t K);
@@ -301,6 +301,81 @@ size_t bsmm_linear_backward_workspace_size(int64_t M, int64_t N, int64_t K);
 bsmm_status bsmm_linear_backward(const void* dY, const void* W, const void* X, int64_t M,
                                  int64_t N, int64_t K, bsmm_dtype fp8_type, void* dX, void* dW,
                                  void* workspace, size_t workspace_bytes, bsmm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Scales in the tensor cores' own layout                                    */
+/* ------------------------------------------------------------------------ */
+
+/* [NKI] Parameters: the backward takes optional pre-computed scales for its
+ * operands and flags saying that they are pre-swizzled.  Here the swizzled
+ * form is the layout in which the tcgen05 block-scaled MMAs take their scale
+ * factors, so that quantizers can write it and GEMMs read it in place, with
+ * no relayout between them.
+ *
+ * The atom layout of one GEMM operand of B x R rows x K (the contraction
+ * axis), hardware blocks of bs = 32 (UE8M0) or 16 (UE4M3) along K:
+ *   - 512-byte atoms [B][RT][KS4]: RT = ceil(R / 256) * 2 row tiles of 128
+ *     rows; KS4 = ceil(K / kt) * (kt / bs / 4) atoms per row tile, where
+ *     kt = 128 for FP8 codes and 256 for E2M1 (an atom holds 4 blocks).
+ *   - The scale of row 128 t + w (0 <= w < 128), block 4 j + i (0 <= i < 4) is
+ *     byte (w % 32) * 16 + (w / 32) * 4 + i of atom (b, t, j).
+ *   - Rows past R and blocks past K hold the neutral scale (UE8M0 127, which
+ *     is 1.0; UE4M3 0).
+ * Formats: MXFP8 (E4M3 / E5M2 codes, UE8M0), MXFP4 (E2M1, UE8M0), NVFP4
+ * (E2M1, UE4M3).  bsmm_scale_atoms_size returns the bytes (0 for other
+ * combinations or empty sizes).
+ */
+size_t bsmm_scale_atoms_size(int64_t B, int64_t rows, int64_t K, bsmm_dtype code_type,
+                             bsmm_scale_type scale_type);
+
+/* Quantize a GEMM operand with its scales written straight into the atom
+ * layout (same codes and scale values as bsmm_quantize with blocks of 1 x bs
+ * along K).
+ *   transpose_in = 0: x [B * rows, K] row-major, contiguous.
+ *   transpose_in = 1: x [K, rows] (the operand transposed; B must be 1).
+ *   codes [B * rows, K] (E2M1: K / 2 bytes a row, packed as in bsmm_quantize).
+ *   atoms  at least bsmm_scale_atoms_size() bytes, 4-byte aligned; the call
+ *          writes all of it (padding included).
+ * Errors: BSMM_ERR_UNSUPPORTED for other code / scale pairs, BSMM_ERR_SHAPE
+ * when K is not a multiple of bs, BSMM_ERR_WORKSPACE when atoms_bytes is too
+ * small.
+ */
+bsmm_status bsmm_quantize_atoms(const void* x, bsmm_dtype x_type, int64_t B, int64_t rows, int64_t K,
+                                int transpose_in, bsmm_dtype code_type, bsmm_scale_type scale_type,
+                                void* codes, void* atoms, size_t atoms_bytes, bsmm_stream_t stream);
+
+/* bsmm_gemm with both operands' scales in the atom layout (one scale per
+ * hardware block).  Same result as bsmm_gemm with the row-major scales they
+ * hold.  MXFP8 reads the atoms in place and takes no workspace (NULL, 0);
+ * MXFP4 and NVFP4 need bsmm_gemm_workspace_size() bytes, 256-byte aligned, in
+ * which the CTA-pair kernel's copy blocks are written from the atoms.
+ * Pointers 16-byte aligned; K a multiple of 32.
+ */
+bsmm_status bsmm_gemm_atoms(int64_t B, int64_t M, int64_t N, int64_t K, const void* a, bsmm_dtype a_type,
+                            const void* b, bsmm_dtype b_type, const void* a_atoms, const void* b_atoms,
+                            bsmm_scale_type scale_type, void* y, bsmm_dtype y_type, void* workspace,
+                            size_t workspace_bytes, bsmm_stream_t stream);
+
+/* [NKI] Parameters (pre-computed scales, pre-swizzled inputs): the backward's
+ * two GEMMs from operands already quantized along their contraction axes,
+ * MXFP8 with fp8_type codes:
+ *   dy_n [M, N] (dY along N),  w_t  [K, N] (W^T along N),
+ *   dy_t [N, M] (dY^T along M), x_t [K, M] (X^T along M),
+ * each with its UE8M0 scales: row-major [rows][contraction / 32]
+ * (scales_are_atoms = 0, as bsmm_quantize writes them) or in the atom layout
+ * (scales_are_atoms = 1, as bsmm_quantize_atoms writes them).
+ * dX [M, K] = dY W and dW [N, K] = dY^T X, bfloat16.  The workspace is
+ * bsmm_linear_backward_quantized_workspace_size() bytes (0 with atoms),
+ * 256-byte aligned.  M, N and K multiples of 32; pointers 16-byte aligned.
+ */
+size_t bsmm_linear_backward_quantized_workspace_size(int64_t M, int64_t N, int64_t K, int scales_are_atoms);
+
+bsmm_status bsmm_linear_backward_quantized(int64_t M, int64_t N, int64_t K, bsmm_dtype fp8_type,
+                                           const void* dy_n, const void* dy_n_scales, const void* w_t,
+                                           const void* w_t_scales, const void* dy_t, const void* dy_t_scales,
+                                           const void* x_t, const void* x_t_scales, int scales_are_atoms,
+                                           void* dX, void* dW, void* workspace, size_t workspace_bytes,
+                                           bsmm_stream_t stream);
 
 #ifdef __cplusplus
 }
