@@ -213,8 +213,9 @@ bsmm_status bsmm_gemm(int64_t B, int64_t M, int64_t N, int64_t K,
  * Errors: those of bsmm_gemm, and BSMM_ERR_WORKSPACE when the problem needs
  * more than BSMM_NOALLOC_SCRATCH_BYTES of scratch, i.e. when
  * bsmm_gemm_workspace_size(B, M, N, K, a_type) exceeds it (e.g. an MXFP8
- * batch of 8 x 4096 x 4096 x 8192 needs 16 MiB, an NVFP4 16384^3 problem
- * 32 MiB). */
+ * batch of 8 x 4096 x 4096 x 8192 needs 16 MiB and fits; E2M1 problems need
+ * room for NVFP4's replicated B blocks: 8192^3 takes 32 MiB, 16384^3
+ * 128 MiB and does not fit). */
 #define BSMM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 bsmm_status bsmm_gemm_noalloc(int64_t B, int64_t M, int64_t N, int64_t K,
