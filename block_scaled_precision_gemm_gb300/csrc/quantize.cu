@@ -42,7 +42,7 @@ struct QP {
 // the tile at byte (w % 32) * 16 + (w / 32) * 4 + kb % 4).
 __device__ __forceinline__ int64_t scale_index(const QP& p, int64_t r, int64_t kb) {
   if (!p.sf_atoms) return r * p.ld_scales + kb;
-  const int64_t b = r / p.sf_rows, rr = r - b * p.sf_rows;
+  const int64_t b = r < p.sf_rows ? 0 : r / p.sf_rows, rr = r - b * p.sf_rows;
   const int w = static_cast<int>(rr & 127);
   return ((b * p.sf_rt + (rr >> 7)) * p.sf_ks4 + (kb >> 2)) * 512 + (w & 31) * 16 + (w >> 5) * 4 + (kb & 3);
 }
@@ -222,8 +222,12 @@ __global__ void __launch_bounds__(256) quant_rows(QP p) {
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const bool fp4 = p.code == BSMM_E2M1;
-  const bool dense = p.ld_x == p.cols && p.ld_codes == p.cols && p.ld_scales * p.bc == p.cols && !p.sf_atoms;
+  // dense: x and codes contiguous; sdense: row-major scales without padding
+  const bool dense = p.ld_x == p.cols && p.ld_codes == p.cols;
+  const bool sdense = dense && !p.sf_atoms && p.ld_scales * p.bc == p.cols;
   const int g_shift = __ffs(G) - 1;
+  const bool spr_pow2 = (spr & (spr - 1)) == 0;
+  const int spr_shift = __ffsll(spr) - 1;
   const In* x = reinterpret_cast<const In*>(p.x);
   uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
   // b0 is warp-uniform, so every shuffle sees the whole warp
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(256) quant_rows(QP p) {
       if (si[u] < total) {
         int64_t off = si[u] * kSlice;
         if (!dense) {
-          const int64_t r = si[u] / spr;
+          const int64_t r = spr_pow2 ? si[u] >> spr_shift : si[u] / spr;
           off = r * p.ld_x + (si[u] - r * spr) * kSlice;
         }
         load_slice<In>(x + off, v[u]);
@@ -254,10 +258,11 @@ __global__ void __launch_bounds__(256) quant_rows(QP p) {
       if (si[u] >= total) continue;
       const Scale sc = make_scale(m, p.code, p.scale);
       int64_t e = si[u] * kSlice, sidx = si[u] >> g_shift;
-      if (!dense) {
-        const int64_t r = si[u] / spr, c = si[u] - r * spr;
-        e = r * p.ld_codes + c * kSlice;
-        sidx = scale_index(p, r, (c * kSlice) / p.bc);
+      if (!sdense) {
+        const int64_t r = spr_pow2 ? si[u] >> spr_shift : si[u] / spr;
+        const int64_t c = si[u] - r * spr;
+        if (!dense) e = r * p.ld_codes + c * kSlice;
+        sidx = scale_index(p, r, c >> g_shift);  // (c * kSlice) / bc
       }
       if ((lane & (G - 1)) == 0) store_scale(p.scales, sidx, p.scale, sc.stored);
       uint32_t w[4];
@@ -562,6 +567,114 @@ __global__ void __launch_bounds__(256) quant_cols_tma(const __grid_constant__ CU
                 kSiteQuantDrain);
 }
 
+// The same for 32-row blocks (MXFP8) with tiles of 128 x 128: a thread owns
+// two adjacent columns of one 32-row block, read as bf16 pairs (half the
+// shared-memory loads of one column per thread, which bound the kernel above).
+constexpr int kCol2C = 128;
+constexpr int kCol2TileBytes = kColTileR * kCol2C * 2;  // 32 KB of bf16
+
+template <bool POW2>
+__global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant__ CUtensorMap tm, QP p, int tiles_c,
+                                                          int64_t n_tiles, int* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t qsm_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kColStages * kCol2TileBytes);
+  // 128 transposed output rows of 128 codes (16-byte chunks swizzled by row)
+  // and their four scale bytes
+  __shared__ __align__(16) uint8_t ostg[kCol2C * kColTileR];
+  __shared__ __align__(16) uint8_t sstg[kCol2C][4];
+  __shared__ int abort_flag;
+  int never_abort_storage = 0;
+  volatile int* never_abort = &never_abort_storage;
+  const int t = threadIdx.x;
+  if (t == 0) {
+    for (int st = 0; st < kColStages; ++st) mbar_init(&full[st], 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int64_t my_n = (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  auto issue = [&](int64_t i) {  // this CTA's i-th tile into stage i % kColStages
+    const int64_t tt = blockIdx.x + i * gridDim.x;
+    const int st = static_cast<int>(i % kColStages);
+    mbar_arrive_expect_tx(&full[st], kCol2TileBytes);
+    tma_load_3d(ring + st * kCol2TileBytes, &tm, &full[st], static_cast<int>((tt % tiles_c) * kCol2C),
+                static_cast<int>((tt / tiles_c) * kColTileR), 0);
+  };
+  int64_t issued = 0;
+  if (t == 0)
+    for (; issued < my_n && issued < kColStages; ++issued) issue(issued);
+  const int cp = t & 63, part = t >> 6;  // columns 2cp, 2cp+1; rows 32 part .. +31 (one block)
+  int64_t i = 0;
+  for (; i < my_n; ++i) {
+    const int st = static_cast<int>(i % kColStages);
+    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>(i / kColStages) & 1u, timeout_ns, &abort_flag,
+                              status, kSiteQuantTile);
+    uint32_t w[32];  // bf16 pairs: rows 32 part + r, columns 2cp (low half) and 2cp+1 (high half)
+    if (ok) {
+      const uint32_t* tile = reinterpret_cast<const uint32_t*>(ring + st * kCol2TileBytes);
+#pragma unroll
+      for (int r = 0; r < 32; ++r) w[r] = tile[(32 * part + r) * (kCol2C / 2) + cp];
+    }
+    if (__syncthreads_or(!ok)) break;  // every thread has read stage st (or the CTA gives up together)
+    if (t == 0 && issued < my_n) issue(issued++);
+    const int64_t tt = blockIdx.x + i * gridDim.x;
+    const int64_t r0 = (tt / tiles_c) * kColTileR;
+    const int64_t c0 = (tt % tiles_c) * kCol2C;
+    const int nr = static_cast<int>(p.rows - r0 < kColTileR ? p.rows - r0 : kColTileR);
+    const int nc = static_cast<int>(p.cols - c0 < kCol2C ? p.cols - c0 : kCol2C);
+    float m0 = 0.f, m1 = 0.f;  // rows past the array read as zero
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      m0 = fmaxf(m0, fabsf(__uint_as_float(w[r] << 16)));
+      m1 = fmaxf(m1, fabsf(__uint_as_float(w[r] & 0xFFFF0000u)));
+    }
+    const Scale s0 = make_scale(m0, p.code, p.scale);
+    const Scale s1 = make_scale(m1, p.code, p.scale);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int col = 2 * cp + h;
+      uint32_t q[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        float f[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          f[j] = __uint_as_float(h ? (w[4 * g + j] & 0xFFFF0000u) : (w[4 * g + j] << 16));
+        q[g] = encode4<POW2>(f[0], f[1], f[2], f[3], h ? s1 : s0, p.code);
+      }
+      uint8_t* row = ostg + col * kColTileR;
+      *reinterpret_cast<uint4*>(row + (((2 * part) ^ (col & 7)) * 16)) = make_uint4(q[0], q[1], q[2], q[3]);
+      *reinterpret_cast<uint4*>(row + (((2 * part + 1) ^ (col & 7)) * 16)) = make_uint4(q[4], q[5], q[6], q[7]);
+      sstg[col][part] = static_cast<uint8_t>((h ? s1 : s0).stored);
+    }
+    __syncthreads();
+    // whole-line stores: each instruction writes 4 output rows x 128 bytes
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = t + 256 * k;
+      const int c = idx >> 3, ch = idx & 7;
+      if (c < nc && ch * 16 < nr)
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.codes) + (c0 + c) * p.ld_codes + r0 + ch * 16) =
+            *reinterpret_cast<const uint4*>(ostg + c * kColTileR + ((ch ^ (c & 7)) * 16));
+    }
+    if (t < nc) {  // this column's scale bytes for the tile's rows (atoms: one word)
+      const int nblk = (nr + 31) / 32;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.scales) + scale_index(p, c0 + t, r0 / 32);
+      if (nblk == 4 && (reinterpret_cast<uintptr_t>(dst) & 3) == 0)
+        *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(&sstg[t][0]);
+      else
+        for (int k = 0; k < nblk; ++k) dst[k] = sstg[t][k];
+    }
+    __syncthreads();  // ostg and sstg are rewritten by the next tile
+  }
+  // copies this CTA started and did not consume (only after giving up)
+  if (t == 0)
+    for (int64_t j = i; j < issued; ++j)
+      mbar_wait(&full[j % kColStages], static_cast<uint32_t>(j / kColStages) & 1u, timeout_ns, never_abort, status,
+                kSiteQuantDrain);
+}
+
 // ---------------------------------------------------------------------------
 // 128 x 128 blocks
 // ---------------------------------------------------------------------------
@@ -727,6 +840,22 @@ __global__ void __launch_bounds__(256) quant_any(QP p) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 template <bool POW2>
+cudaError_t launch_cols_tma2(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
+  CUtensorMap tm;
+  if (!make_tmap_3d(&tm, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.cols, p.rows, 1, kCol2C, kColTileR, false))
+    return cudaErrorInvalidValue;
+  const int tiles_c = static_cast<int>(ceil_div(p.cols, kCol2C));
+  const int64_t n_tiles = static_cast<int64_t>(tiles_c) * ceil_div(p.rows, kColTileR);
+  const int smem = kColStages * kCol2TileBytes + 128 + kColStages * 8;
+  cudaError_t e = cudaFuncSetAttribute(quant_cols_tma2<POW2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 2);
+  quant_cols_tma2<POW2><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
+      tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns());
+  return cudaGetLastError();
+}
+
+template <bool POW2>
 cudaError_t launch_cols_tma(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
   CUtensorMap tm;
   if (!make_tmap_3d(&tm, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.cols, p.rows, 1, kColTileC, kColTileR, false))
@@ -753,7 +882,7 @@ cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
   const bool cols_tma = sizeof(In) == 2 && p.transpose && p.bc == 1 && pow2_small_r && p.code != BSMM_E2M1 &&
                         p.scale != BSMM_SCALE_F32 && codes16 && p.ld_codes % 32 == 0 && p.ld_x == p.cols &&
                         p.cols % 8 == 0 && aligned(p.x, 16);
-  if (cols_tma) return launch_cols_tma<POW2>(p, ctx, s);
+  if (cols_tma) return p.br == 32 ? launch_cols_tma2<POW2>(p, ctx, s) : launch_cols_tma<POW2>(p, ctx, s);
   if (p.br == 1 && pow2_small && !p.transpose && x_vec && codes16) {
     int64_t blocks = ceil_div(p.rows * (p.cols / kSlice), 256 * 2);
     blocks = std::min<int64_t>(blocks, static_cast<int64_t>(ctx->num_sms) * 8);
