@@ -138,26 +138,33 @@ int atom_format(int code, int scale) {
   return -1;
 }
 
-// Quantize a GEMM operand of B x rows x K (contraction K) with its scales
-// written straight into the plain atom layout; the atoms are first filled
-// with the neutral scale (UE8M0 127 = 1.0, UE4M3 0) so that padding rows and
-// blocks past K contribute nothing.  transpose_in: x is [K][rows] (B == 1).
-cudaError_t quantize_to_atoms(const void* x, bool bf16, int64_t B, int64_t rows, int64_t K, bool transpose_in,
-                              int code, int scale, void* codes, void* atoms, cudaStream_t s) {
+// The request that quantizes a GEMM operand of B x rows x K (contraction K)
+// with its scales written straight into the plain atom layout, after filling
+// the atoms with the neutral scale (UE8M0 127 = 1.0, UE4M3 0) so that padding
+// rows and blocks past K contribute nothing.  transpose_in: x is [K][rows]
+// (B == 1).
+cudaError_t atoms_request(const void* x, bool bf16, int64_t B, int64_t rows, int64_t K, bool transpose_in, int code,
+                          int scale, void* codes, void* atoms, cudaStream_t s, QuantRequest* q) {
   const int fmt = atom_format(code, scale);
   const int bs = fmt == kFmtNVF4 ? 16 : 32;
   const int per_tile = fmt == kFmtNVF4 ? 4 : (fmt == kFmtMXF4 ? 2 : 1);
   const int64_t k_tiles = ceil_div(K, fmt == kFmtMXF8 ? 128 : 256);
   cudaError_t e = cudaMemsetAsync(atoms, scale == BSMM_SCALE_UE4M3 ? 0 : 127, sf_atoms_plain_bytes(B, rows, K, fmt), s);
   if (e != cudaSuccess) return e;
-  QuantRequest q = transpose_in
-                       ? QuantRequest{x, bf16, K, rows, rows, bs, 1, code, scale, true, codes, K, atoms, 1}
-                       : QuantRequest{x, bf16, B * rows, K, K, 1, bs, code, scale, false, codes, K, atoms, 1};
-  q.sf_atoms = true;
-  q.sf_rows = rows;
-  q.sf_rt = ceil_div(rows, 256) * 2;
-  q.sf_ks4 = k_tiles * per_tile;
-  return launch_quantize(q, s);
+  *q = transpose_in ? QuantRequest{x, bf16, K, rows, rows, bs, 1, code, scale, true, codes, K, atoms, 1}
+                    : QuantRequest{x, bf16, B * rows, K, K, 1, bs, code, scale, false, codes, K, atoms, 1};
+  q->sf_atoms = true;
+  q->sf_rows = rows;
+  q->sf_rt = ceil_div(rows, 256) * 2;
+  q->sf_ks4 = k_tiles * per_tile;
+  return cudaSuccess;
+}
+
+cudaError_t quantize_to_atoms(const void* x, bool bf16, int64_t B, int64_t rows, int64_t K, bool transpose_in,
+                              int code, int scale, void* codes, void* atoms, cudaStream_t s) {
+  QuantRequest q;
+  const cudaError_t e = atoms_request(x, bf16, B, rows, K, transpose_in, code, scale, codes, atoms, s, &q);
+  return e != cudaSuccess ? e : launch_quantize(q, s);
 }
 
 }  // namespace
@@ -524,23 +531,19 @@ bsmm_status bsmm_linear_backward(const void* dY, const void* W, const void* X, i
   uint8_t* xt_s = take(sf_atoms_plain_bytes(1, K, M, kFmtMXF8));
 
   // Each operand quantized along its GEMM's contraction axis, scales straight
-  // into the tensor-core atom layout (no relayout before the GEMMs).
+  // into the tensor-core atom layout (no relayout before the GEMMs); dY's two
+  // quantizations in one pass over it.
   const int ft = fp8_type;
-  struct Q {
-    const void* x;
-    int64_t rows, K;  // the GEMM operand: rows x K
-    bool tr;          // x holds the operand transposed ([K][rows])
-    uint8_t *codes, *atoms;
-  } qs[4] = {
-      {dY, M, N, false, dy_n, dy_n_s},  // dY along N           -> [M, N]
-      {W, K, N, true, wt, wt_s},        // W [N,K] along N       -> W^T [K, N]
-      {dY, N, M, true, dyt, dyt_s},     // dY [M,N] along M      -> dY^T [N, M]
-      {X, K, M, true, xt, xt_s},        // X [M,K] along M       -> X^T [K, M]
-  };
-  for (const Q& q : qs) {
-    const cudaError_t e = quantize_to_atoms(q.x, true, 1, q.rows, q.K, q.tr, ft, BSMM_SCALE_UE8M0, q.codes, q.atoms, s);
-    if (e != cudaSuccess) return cuda_fail(e, "backward quantize launch");
-  }
+  QuantRequest q_dyn, q_dyt;
+  cudaError_t e = atoms_request(dY, true, 1, M, N, false, ft, BSMM_SCALE_UE8M0, dy_n, dy_n_s, s, &q_dyn);  // [M, N]
+  if (e == cudaSuccess)
+    e = atoms_request(dY, true, 1, N, M, true, ft, BSMM_SCALE_UE8M0, dyt, dyt_s, s, &q_dyt);  // dY^T [N, M]
+  if (e == cudaSuccess) e = launch_quantize_dual(q_dyt, q_dyn, s);
+  if (e == cudaSuccess)  // W [N,K] along N -> W^T [K, N]
+    e = quantize_to_atoms(W, true, 1, K, N, true, ft, BSMM_SCALE_UE8M0, wt, wt_s, s);
+  if (e == cudaSuccess)  // X [M,K] along M -> X^T [K, M]
+    e = quantize_to_atoms(X, true, 1, K, M, true, ft, BSMM_SCALE_UE8M0, xt, xt_s, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward quantize launch");
   return backward_gemms(M, N, K, ft, dy_n, dy_n_s, wt, wt_s, dyt, dyt_s, xt, xt_s, true, dX, dW, nullptr, s);
 }
 

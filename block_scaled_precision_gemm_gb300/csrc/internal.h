@@ -53,6 +53,10 @@ struct QuantRequest {
   int64_t sf_rows = 0, sf_rt = 0, sf_ks4 = 0;
 };
 cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s);
+// Two quantizations of one bf16 array (qc: 32 x 1 blocks, transposed; qr:
+// 1 x 32 blocks) in a single pass over it where the formats allow, else the
+// two launches.
+cudaError_t launch_quantize_dual(const QuantRequest& qc, const QuantRequest& qr, cudaStream_t s);
 
 // Block-scaled formats of bsmm_gemm.
 enum MxFormat { kFmtMXF8 = 0, kFmtNVF4 = 1, kFmtMXF4 = 2 };

@@ -573,9 +573,13 @@ __global__ void __launch_bounds__(256) quant_cols_tma(const __grid_constant__ CU
 constexpr int kCol2C = 128;
 constexpr int kCol2TileBytes = kColTileR * kCol2C * 2;  // 32 KB of bf16
 
-template <bool POW2>
+// DUAL: the same tiles are also quantized along their rows (1 x 32 blocks,
+// untransposed output described by p2: codes, scales and their layout), so
+// an array both GEMMs of the backward read along different axes (dY) is
+// read from HBM once.
+template <bool POW2, bool DUAL>
 __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant__ CUtensorMap tm, QP p, int tiles_c,
-                                                          int64_t n_tiles, int* status, uint64_t timeout_ns) {
+                                                          int64_t n_tiles, int* status, uint64_t timeout_ns, QP p2) {
   extern __shared__ uint8_t qsm_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 127) & ~uintptr_t(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + kColStages * kCol2TileBytes);
@@ -611,18 +615,67 @@ __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant_
     const bool ok = mbar_wait(&full[st], static_cast<uint32_t>(i / kColStages) & 1u, timeout_ns, &abort_flag,
                               status, kSiteQuantTile);
     uint32_t w[32];  // bf16 pairs: rows 32 part + r, columns 2cp (low half) and 2cp+1 (high half)
-    if (ok) {
-      const uint32_t* tile = reinterpret_cast<const uint32_t*>(ring + st * kCol2TileBytes);
-#pragma unroll
-      for (int r = 0; r < 32; ++r) w[r] = tile[(32 * part + r) * (kCol2C / 2) + cp];
-    }
-    if (__syncthreads_or(!ok)) break;  // every thread has read stage st (or the CTA gives up together)
-    if (t == 0 && issued < my_n) issue(issued++);
     const int64_t tt = blockIdx.x + i * gridDim.x;
     const int64_t r0 = (tt / tiles_c) * kColTileR;
     const int64_t c0 = (tt % tiles_c) * kCol2C;
     const int nr = static_cast<int>(p.rows - r0 < kColTileR ? p.rows - r0 : kColTileR);
     const int nc = static_cast<int>(p.cols - c0 < kCol2C ? p.cols - c0 : kCol2C);
+    if (ok) {
+      const uint32_t* tile = reinterpret_cast<const uint32_t*>(ring + st * kCol2TileBytes);
+#pragma unroll
+      for (int r = 0; r < 32; ++r) w[r] = tile[(32 * part + r) * (kCol2C / 2) + cp];
+      if constexpr (DUAL) {
+        // along the rows: thread t takes tile row t / 2, columns 64 (t % 2)
+        // .. +63 (two blocks of 32).  Register k holds the row's 16-byte chunk
+        // (k + row) % 8, so that the eight threads of a load phase (four
+        // rows) hit different banks.
+        const int rr = t >> 1, hh = t & 1;
+        const int rot = rr & 7;
+        const uint4* src = reinterpret_cast<const uint4*>(tile + rr * (kCol2C / 2) + hh * 32);
+        uint4 q[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = src[(k + rot) & 7];
+        float mb[2] = {0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t u[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+          float m = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[j] << 16)), fabsf(__uint_as_float(u[j] & 0xFFFF0000u))));
+          const bool hi_blk = ((k + rot) & 7) >= 4;
+          mb[0] = hi_blk ? mb[0] : fmaxf(mb[0], m);
+          mb[1] = hi_blk ? fmaxf(mb[1], m) : mb[1];
+        }
+        const Scale sc0 = make_scale(mb[0], p2.code, p2.scale);
+        const Scale sc1 = make_scale(mb[1], p2.code, p2.scale);
+        const int64_t grow = r0 + rr;
+        const int64_t gcol = c0 + 64 * hh;
+        if (grow < p.rows) {
+          uint8_t* drow = reinterpret_cast<uint8_t*>(p2.codes) + grow * p2.ld_codes + gcol;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int lc = (k + rot) & 7;  // the chunk's 8 columns: gcol + 8 lc ..
+            const Scale& sc = lc >= 4 ? sc1 : sc0;
+            const uint32_t lo = encode4<POW2>(__uint_as_float(q[k].x << 16), __uint_as_float(q[k].x & 0xFFFF0000u),
+                                              __uint_as_float(q[k].y << 16), __uint_as_float(q[k].y & 0xFFFF0000u),
+                                              sc, p2.code);
+            const uint32_t hi = encode4<POW2>(__uint_as_float(q[k].z << 16), __uint_as_float(q[k].z & 0xFFFF0000u),
+                                              __uint_as_float(q[k].w << 16), __uint_as_float(q[k].w & 0xFFFF0000u),
+                                              sc, p2.code);
+            if (gcol + 8 * lc < p.cols) *reinterpret_cast<uint2*>(drow + 8 * lc) = make_uint2(lo, hi);
+          }
+          // the row's scales for blocks gcol / 32 and gcol / 32 + 1 (cols % 32 == 0)
+          const int64_t kb = gcol / 32;
+          if (gcol < p.cols)
+            reinterpret_cast<uint8_t*>(p2.scales)[scale_index(p2, grow, kb)] = static_cast<uint8_t>(sc0.stored);
+          if (gcol + 32 < p.cols)
+            reinterpret_cast<uint8_t*>(p2.scales)[scale_index(p2, grow, kb + 1)] = static_cast<uint8_t>(sc1.stored);
+        }
+      }
+    }
+    if (__syncthreads_or(!ok)) break;  // every thread has read stage st (or the CTA gives up together)
+    if (t == 0 && issued < my_n) issue(issued++);
     float m0 = 0.f, m1 = 0.f;  // rows past the array read as zero
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
@@ -839,19 +892,20 @@ __global__ void __launch_bounds__(256) quant_any(QP p) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-template <bool POW2>
-cudaError_t launch_cols_tma2(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
+template <bool POW2, bool DUAL = false>
+cudaError_t launch_cols_tma2(const QP& p, const DeviceCtx* ctx, cudaStream_t s, const QP& p2 = QP{}) {
   CUtensorMap tm;
   if (!make_tmap_3d(&tm, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.cols, p.rows, 1, kCol2C, kColTileR, false))
     return cudaErrorInvalidValue;
   const int tiles_c = static_cast<int>(ceil_div(p.cols, kCol2C));
   const int64_t n_tiles = static_cast<int64_t>(tiles_c) * ceil_div(p.rows, kColTileR);
   const int smem = kColStages * kCol2TileBytes + 128 + kColStages * 8;
-  cudaError_t e = cudaFuncSetAttribute(quant_cols_tma2<POW2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(quant_cols_tma2<POW2, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 2);
-  quant_cols_tma2<POW2><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
-      tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns());
+  quant_cols_tma2<POW2, DUAL><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
+      tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns(), p2);
   return cudaGetLastError();
 }
 
@@ -909,11 +963,37 @@ cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
 
 }  // namespace
 
+namespace {
+QP to_qp(const QuantRequest& q) {
+  return QP{q.x, q.rows, q.cols, q.ld_x, q.br, q.bc, q.code, q.scale, q.transpose ? 1 : 0,
+            q.codes, q.ld_codes, q.scales, q.ld_scales, q.sf_atoms ? 1 : 0, q.sf_rows, q.sf_rt, q.sf_ks4};
+}
+}  // namespace
+
+cudaError_t launch_quantize_dual(const QuantRequest& qc, const QuantRequest& qr, cudaStream_t s) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  // One pass over x when both are 8-bit MX quantizations of the same bf16
+  // array: qc transposed in 32 x 1 blocks, qr untransposed in 1 x 32.
+  const bool one_byte = qc.scale != BSMM_SCALE_F32 && qc.scale == qr.scale;
+  const bool eligible = qc.x == qr.x && qc.x_bf16 && qr.x_bf16 && qc.rows == qr.rows && qc.cols == qr.cols &&
+                        qc.transpose && qc.br == 32 && qc.bc == 1 && !qr.transpose && qr.br == 1 && qr.bc == 32 &&
+                        qc.code == qr.code && qc.code != BSMM_E2M1 && qc.code != BSMM_INT8 && one_byte &&
+                        qc.ld_x == qc.cols && qr.ld_x == qr.cols && qc.cols % 32 == 0 && aligned(qc.x, 16) &&
+                        aligned(qc.codes, 16) && qc.ld_codes % 32 == 0 && aligned(qr.codes, 8) && qr.ld_codes % 8 == 0;
+  if (!eligible) {
+    cudaError_t e = launch_quantize(qc, s);
+    return e != cudaSuccess ? e : launch_quantize(qr, s);
+  }
+  const QP pc = to_qp(qc), pr = to_qp(qr);
+  return qc.scale == BSMM_SCALE_UE8M0 ? launch_cols_tma2<true, true>(pc, ctx, s, pr)
+                                      : launch_cols_tma2<false, true>(pc, ctx, s, pr);
+}
+
 cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s) {
   const DeviceCtx* ctx = device_ctx();
   if (!ctx) return cudaErrorInitializationError;
-  QP p{q.x, q.rows, q.cols, q.ld_x, q.br, q.bc, q.code, q.scale, q.transpose ? 1 : 0,
-       q.codes, q.ld_codes, q.scales, q.ld_scales, q.sf_atoms ? 1 : 0, q.sf_rows, q.sf_rt, q.sf_ks4};
+  QP p = to_qp(q);
   // UE8M0 scales are powers of two: the codes divide by multiplying with the
   // exact reciprocal.
   const bool pow2 = q.scale == BSMM_SCALE_UE8M0;
