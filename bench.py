@@ -528,14 +528,15 @@ def run_gpu(args):
 # the dominant kernel or call, from ncu captures of the same workloads
 # (profiles/traffic_by_workload.md); absent until captured for the kernels as
 # they stand.  sweep: the mean over the step's 8 GEMM launches.  mxfp8,
-# nvfp4, mxfp4: the GEMM launch (the scale relayouts add under 1%).  int8:
-# the whole call (4 launches).
+# nvfp4, mxfp4: the GEMM launch (the scale relayouts add under 1%).
+# backward (5 launches) and int8 (3): the whole call.
 TRAFFIC_PER_LAUNCH = {
-    W.GROUPED_SWEEP.name: 1_968_950_000,
-    W.MXFP8_BATCHED.name: 1_314_209_280,
-    W.NVFP4_SQUARE.name: 4_356_233_000,
-    W.MXFP4_SQUARE.name: 2_462_586_000,
-    W.INT8_4096.name: 351_400_000,
+    W.GROUPED_SWEEP.name: 1_971_545_000,
+    W.MXFP8_BATCHED.name: 1_325_603_584,
+    W.NVFP4_SQUARE.name: 4_285_872_000,
+    W.MXFP4_SQUARE.name: 2_458_361_000,
+    W.BACKWARD.name: 3_179_986_000,
+    W.INT8_4096.name: 288_361_472,
 }
 
 
