@@ -96,3 +96,43 @@ def test_workspace_queries(lib):
     assert lib.bsmm_gemm_workspace_size(1, 16384, 16384, 16384, b.E2M1) == 2 * 64 * (64 * 32) * 512
     assert lib.bsmm_int8_channel_workspace_size(1, 3, 2) > 0
     assert lib.bsmm_linear_backward_workspace_size(64, 64, 64) > 4 * 64 * 64
+
+
+def test_atom_layout_queries_and_validation_without_gpu(lib):
+    """The tensor-core scale layout entry points: sizes from the documented
+    geometry, and argument errors reported before any CUDA call."""
+    import block_scaled_precision_gemm_gb300 as b
+    P = ctypes.c_void_p
+    fake = P(4096)
+    # 512-byte atoms [B][ceil(R/256)*2 row tiles][ceil(K/kt) * kt/bs/4 atoms]
+    assert lib.bsmm_scale_atoms_size(1, 300, 384, b.E4M3, b.SCALE_UE8M0) == 1 * 4 * 3 * 512
+    assert lib.bsmm_scale_atoms_size(2, 256, 1024, b.E5M2, b.SCALE_UE8M0) == 2 * 2 * 8 * 512
+    assert lib.bsmm_scale_atoms_size(1, 100, 512, b.E2M1, b.SCALE_UE8M0) == 1 * 2 * (2 * 2) * 512   # MXFP4
+    assert lib.bsmm_scale_atoms_size(1, 100, 512, b.E2M1, b.SCALE_UE4M3) == 1 * 2 * (2 * 4) * 512   # NVFP4
+    assert lib.bsmm_scale_atoms_size(1, 64, 64, b.E4M3, b.SCALE_UE4M3) == 0  # no tensor-core format
+    assert lib.bsmm_scale_atoms_size(1, 64, 64, b.INT8, b.SCALE_F32) == 0
+    # quantize to atoms
+    q = lib.bsmm_quantize_atoms
+    assert q(fake, b.BF16, 1, 64, 64, 0, b.E4M3, b.SCALE_UE4M3, fake, fake, 1 << 20, None) == b.ERR_UNSUPPORTED
+    assert q(fake, b.BF16, 1, 64, 48, 0, b.E4M3, b.SCALE_UE8M0, fake, fake, 1 << 20, None) == b.ERR_SHAPE
+    assert q(fake, b.BF16, 2, 64, 64, 1, b.E4M3, b.SCALE_UE8M0, fake, fake, 1 << 20, None) == b.ERR_SHAPE
+    assert q(fake, b.BF16, 1, 64, 64, 0, b.E4M3, b.SCALE_UE8M0, fake, fake, 100, None) == b.ERR_WORKSPACE
+    assert q(fake, b.BF16, 1, 64, 64, 0, b.E4M3, b.SCALE_UE8M0, fake, P(4097), 1 << 20, None) == b.ERR_ALIGNMENT
+    assert q(None, b.BF16, 0, 64, 64, 0, b.E4M3, b.SCALE_UE8M0, None, None, 0, None) == b.OK
+    # GEMM from atoms: both operands one format; FP4 needs the workspace
+    g = lib.bsmm_gemm_atoms
+    assert g(1, 128, 128, 256, fake, b.E4M3, fake, b.E2M1, fake, fake, b.SCALE_UE8M0, fake, b.F32, None, 0,
+             None) == b.ERR_UNSUPPORTED
+    assert g(1, 128, 128, 80, fake, b.E4M3, fake, b.E4M3, fake, fake, b.SCALE_UE8M0, fake, b.F32, None, 0,
+             None) == b.ERR_SHAPE
+    assert g(1, 128, 128, 256, fake, b.E2M1, fake, b.E2M1, fake, fake, b.SCALE_UE4M3, fake, b.F32, None, 0,
+             None) == b.ERR_WORKSPACE
+    # pre-quantized backward: multiples of 32; workspace only with row-major scales
+    bq = lib.bsmm_linear_backward_quantized
+    assert bq(33, 64, 64, b.E5M2, fake, fake, fake, fake, fake, fake, fake, fake, 1, fake, fake, None, 0,
+              None) == b.ERR_SHAPE
+    assert lib.bsmm_linear_backward_quantized_workspace_size(256, 512, 384, 1) == 0
+    assert lib.bsmm_linear_backward_quantized_workspace_size(256, 512, 384, 0) == max(
+        lib.bsmm_gemm_workspace_size(1, 256, 384, 512, b.E4M3), lib.bsmm_gemm_workspace_size(1, 512, 384, 256, b.E4M3))
+    assert bq(256, 512, 384, b.E5M2, fake, fake, fake, fake, fake, fake, fake, fake, 0, fake, fake, None, 0,
+              None) == b.ERR_WORKSPACE
