@@ -101,6 +101,17 @@ def test_int8_extreme_sums_tensor_core_path(D_in):
     assert got["acc"][0, 0] == D_in * 127 * 127 and got["acc"][1, 0] == -D_in * 127 * 127
 
 
+@pytest.mark.parametrize("B,D_in,D_out", [(2304, 1100, 2304), (2400, 2100, 2080)])
+def test_int8_more_tiles_than_clusters(B, D_in, D_out):
+    """More 256 x 256 tiles (81, 90) than clusters (76 on GB300), a partial
+    last wave, and K over two exact 16-block chunks: sums, codes and y stay
+    exact."""
+    g = np.random.default_rng(B + D_out)
+    x = g.standard_normal((B, D_in)).astype(np.float32)
+    w = g.standard_normal((D_in, D_out)).astype(np.float32)
+    run_int8(x, w)
+
+
 def _bf16(a):
     return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
 
