@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 
 #include <cstdlib>
+#include <mutex>
 #include <cstring>
 
 #include "internal.h"
@@ -395,6 +396,40 @@ __global__ void __launch_bounds__(256, 4) i8_quant_w_strip(const float* __restri
   }
 }
 
+// A second stream per device, on which w's quantization runs beside x's: it
+// forks from the caller's stream after its earlier work and joins back before
+// the matmul.  The record / wait pairs are made under a lock, so that calls
+// from several host threads never wait on each other's event records.
+std::mutex g_side_mutex;
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[64];
+
+cudaError_t side_fork(int dev, cudaStream_t main, cudaStream_t* side) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_side_mutex);
+  SideStream& ss = g_side[dev];
+  if (!ss.s) {
+    cudaError_t e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaEventRecord(ss.fork, main);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss.s, ss.fork, 0);
+  *side = ss.s;
+  return e;
+}
+
+cudaError_t side_join(int dev, cudaStream_t main) {
+  std::lock_guard<std::mutex> lock(g_side_mutex);
+  SideStream& ss = g_side[dev];
+  cudaError_t e = cudaEventRecord(ss.join, ss.s);
+  return e == cudaSuccess ? cudaStreamWaitEvent(main, ss.join, 0) : e;
+}
+
 template <typename Pad>
 cudaError_t launch_w_strip(const Int8Request& r, int64_t Kp, Pad* wqT, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -589,6 +624,14 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
     i8_quant_cols<int8_t><<<g2, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales, nullptr);
     return cudaGetLastError();
   }
+  // w's quantization beside x's on the side stream (tensor-core path)
+  const bool side = tc && w_strip;
+  if (side) {
+    cudaStream_t ss;
+    e = side_fork(ctx->device, s, &ss);
+    if (e == cudaSuccess) e = launch_w_strip<__nv_bfloat16>(r, Kp, reinterpret_cast<__nv_bfloat16*>(wpadT), ss);
+    if (e != cudaSuccess) return e;
+  }
   const bool rows_vec = (r.D_in % 4) == 0 && (reinterpret_cast<uintptr_t>(r.x) & 15) == 0 &&
                         (reinterpret_cast<uintptr_t>(r.x_q) & 3) == 0 && r.D_in <= 8192;
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xpad);
@@ -607,9 +650,11 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   else
     i8_quant_rows<int8_t><<<static_cast<unsigned>(r.B), 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales,
                                                                      reinterpret_cast<int8_t*>(xpad));
-  if (w_strip) {
-    e = tc ? launch_w_strip<__nv_bfloat16>(r, Kp, reinterpret_cast<__nv_bfloat16*>(wpadT), s)
-           : launch_w_strip<int8_t>(r, Kp, reinterpret_cast<int8_t*>(wpadT), s);
+  if (side) {
+    e = side_join(ctx->device, s);
+    if (e != cudaSuccess) return e;
+  } else if (w_strip) {
+    e = launch_w_strip<int8_t>(r, Kp, reinterpret_cast<int8_t*>(wpadT), s);
     if (e != cudaSuccess) return e;
   } else if ((r.D_out % 4) == 0 && (reinterpret_cast<uintptr_t>(r.w) & 15) == 0) {
     const int rows_per_cta = 256;
