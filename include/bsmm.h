@@ -272,6 +272,11 @@ bsmm_status bsmm_gemm_grouped(int64_t M, int64_t N, int64_t K, const void* a, bs
  * partials of at most 1024 products, each an exact integer below 2^24, in
  * int32.  Where y or acc cannot be stored through TMA (D_out % 4 != 0, or a
  * base not 16-byte aligned) the warp-level integer MMA computes the sums.
+ * On the tensor-core path w's quantization runs beside x's on a stream the
+ * library keeps per device: it starts after the work already on `stream`
+ * (an event recorded there) and `stream` waits for it before the matmul, so
+ * the call stays ordered on `stream` as a whole (CUDA graph capture
+ * included).
  */
 size_t bsmm_int8_channel_workspace_size(int64_t B, int64_t D_in, int64_t D_out);
 
