@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "internal.h"
@@ -764,7 +765,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-int g_pair_clusters[5][64] = {};  // max co-resident clusters per mode and device
+// max co-resident clusters per mode and device, found on first use (calls
+// from several host threads may race to fill it in; they find the same value)
+std::atomic<int> g_pair_clusters[5][64] = {};
 
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const CUtensorMap& tsa,
@@ -789,7 +792,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     *why = "device ordinal beyond the library's table";
     return cudaErrorInvalidDevice;
   }
-  int& max_clusters = g_pair_clusters[MODE][ctx->device];
+  int max_clusters = g_pair_clusters[MODE][ctx->device].load(std::memory_order_relaxed);
   if (max_clusters == 0) {
     cfg.gridDim = dim3(2 * (ctx->num_sms / 2));
     int n = 0;
@@ -800,6 +803,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
       return cudaErrorInvalidConfiguration;
     }
     max_clusters = n;
+    g_pair_clusters[MODE][ctx->device].store(n, std::memory_order_relaxed);
   }
   const int clusters = std::max(1, std::min(p.num_tiles, max_clusters));
   cfg.gridDim = dim3(2 * clusters);
