@@ -294,7 +294,7 @@ class Int8Work(Work):
         self.ws = torch.empty(bsmm.int8_channel_workspace_size(p.B, p.D_in, p.D_out), dtype=torch.uint8,
                               device=device)
         self.flops = 2.0 * p.B * p.D_in * p.D_out
-        self.launches_per_step = 5
+        self.launches_per_step = 3  # x quantizer, w strip quantizer (side stream), the matmul
         self.inputs, self.outputs = [self.x, self.wt], [self.out["y"]]
 
     def step(self, events=None):
@@ -383,7 +383,7 @@ class BackwardWork(Work):
         self.ws = torch.empty(bsmm.linear_backward_workspace_size(p.M, p.N, p.K), dtype=torch.uint8,
                               device=device)
         self.flops = 2 * 2.0 * p.M * p.N * p.K
-        self.launches_per_step = 8
+        self.launches_per_step = 5  # dual quantizer on dY, W^T and X^T quantizers, two GEMMs
         self.inputs, self.outputs = [self.dY, self.W, self.X], [self.dX, self.dW]
 
     def step(self, events=None):
