@@ -370,7 +370,7 @@ class BackwardWork(Work):
     """NKI MXFP8 linear backward, M=16384, N=K=8192: a step quantizes dY (along
     N and along M), W (along N) and X (along M) to E5M2 and runs dX = dY.W and
     dW = dY^T.X with bf16 outputs."""
-    dominant = "MXFP8 backward call (4 quantizers + 2 x (sf_relayout + tc_gemm_pair kPairMXF8))"
+    dominant = "MXFP8 backward call (dual dY quantizer + W^T, X^T quantizers into scale atoms + 2 x tc_gemm_pair kPairMXF8)"
     dtype = "e5m2 (f32 accumulate, bf16 out)"
 
     def __init__(self, workload, device):
