@@ -64,3 +64,28 @@ def test_reference_arm_non_zero_rank_does_no_work(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
     assert capsys.readouterr().out == ""
+
+
+@pytest.mark.parametrize("workload", ["small", "int8"])
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys, workload):
+    """--impl reference on rank 0 runs the oracle on the host cores (no GPU)
+    and prints one JSON line with the base contract's keys, the reference
+    arm's e2e and cpu_baseline objects."""
+    import json
+
+    import bench
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    bench.main(["--impl", "reference", "--workload", workload, "--steps", "1", "--warmup", "0",
+                "--reference-rows", "4"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"]
