@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -92,8 +93,12 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed
-    region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons.
+
+    A reader thread stamps each sample with the host clock when it arrives, so
+    that the summary can keep the samples of one window (the timed region).
+    Entering waits for the first sample, so the sampler is live before the
+    window opens."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -102,6 +107,16 @@ class ClockSampler:
         self.gpu = gpu_index
         self.period = period_ms
         self.proc = None
+        self.thread = None
+        self.rows = []  # (host time of arrival, csv fields)
+        self.window = (float("-inf"), float("inf"))
+        self.note = "timed region"
+
+    def _read(self):
+        for line in self.proc.stdout:
+            fields = next(csv.reader([line]), [])
+            if len(fields) >= 9:
+                self.rows.append((time.perf_counter(), fields))
 
     def __enter__(self):
         try:
@@ -110,22 +125,37 @@ class ClockSampler:
                  f"-lms={self.period}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.perf_counter()
+        while not self.rows and self.proc.poll() is None and time.perf_counter() - t0 < 5.0:
+            time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                self.proc.wait()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def count(self, t0, t1):
+        return sum(1 for t, _ in self.rows if t0 <= t <= t1)
+
+    def set_window(self, t0, t1, note):
+        self.window, self.note = (t0, t1), note
 
     def summary(self):
-        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        t0, t1 = self.window
+        rows = [r for t, r in self.rows if t0 <= t <= t1]
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0,
+                    "window": self.note}
         def num(x):
             try:
                 return float(x.strip())
@@ -136,7 +166,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip().lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows),
+                "reasons": reasons, "samples": len(rows), "window": self.note,
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
@@ -449,12 +479,26 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
+        t_open = time.perf_counter()
         e_start, e_end = _ev(), _ev()
         e_start.record()
         for _ in range(args.steps):
             wl.step(events)
         e_end.record()
         torch.cuda.synchronize()
+        t_close = time.perf_counter()
+        clk.set_window(t_open, t_close, "timed region")
+        if clk.count(t_open, t_close) < 3:
+            # a timed region shorter than a few sampling periods: the clocks
+            # are those of further, untimed steps of the same workload run
+            # straight after it (at most two seconds of them)
+            while clk.count(t_open, time.perf_counter()) < 3 and time.perf_counter() - t_close < 2.0:
+                for _ in range(args.steps):
+                    wl.step()
+                torch.cuda.synchronize()
+            clk.set_window(t_open, time.perf_counter(),
+                           f"timed region ({1e3 * (t_close - t_open):.0f} ms) and the untimed steps of the same "
+                           "workload run right after it")
         barrier(world)
     elapsed_ms = e_start.elapsed_time(e_end)
     st, site = bsmm.check_device_status()
