@@ -580,7 +580,7 @@ TRAFFIC_PER_LAUNCH = {
     W.NVFP4_SQUARE.name: 4_285_872_000,
     W.MXFP4_SQUARE.name: 2_458_361_000,
     W.BACKWARD.name: 3_179_986_000,
-    W.INT8_4096.name: 288_361_472,
+    W.INT8_4096.name: 290_881_472,
 }
 
 
