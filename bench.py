@@ -440,16 +440,26 @@ def make_work(workload: W.Workload, device) -> Work:
     return BackwardWork(workload, device)
 
 
-def peak_tflops(peaks, kind):
-    """Dense peak for the path's own dtype: measured bf16 (sustained) times the
-    nominal dense ratio on GB300 (FP8 4.5/2.25 = 2x, FP4 13.5/2.25 = 6x).  INT8 has no measured or usable nominal
-    figure on this part: its exact matmul runs on the bf16 tensor cores, so the
-    bf16 rate is its peak."""
-    base = peaks["bf16_tflops_sustained"]
+def peak_tflops(peaks, kind, sustained):
+    """Dense peak for the path's own dtype: measured bf16 times the nominal
+    dense ratio on GB300 (FP8 4.5/2.25 = 2x, FP4 13.5/2.25 = 6x).  INT8 has no
+    measured or usable nominal figure on this part: its exact matmul runs on
+    the bf16 tensor cores, so the bf16 rate is its peak.
+
+    ``sustained`` picks the bf16 figure measured back to back under the power
+    cap, for a timed region that ran under it; otherwise the burst figure."""
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    base = peaks[key]
     return {"fp8": 2.0 * base, "fp4": 6.0 * base, "int8": base}[kind], {
-        "fp8": "2 x bf16_tflops_sustained (FP8/BF16 nominal dense ratio 4.5/2.25)",
-        "fp4": "6 x bf16_tflops_sustained (FP4/BF16 nominal dense ratio 13.5/2.25)",
-        "int8": "bf16_tflops_sustained (the INT8 matmul runs exactly on the bf16 tensor cores)"}[kind]
+        "fp8": f"2 x {key} (FP8/BF16 nominal dense ratio 4.5/2.25)",
+        "fp4": f"6 x {key} (FP4/BF16 nominal dense ratio 13.5/2.25)",
+        "int8": f"{key} (the INT8 matmul runs exactly on the bf16 tensor cores)"}[kind]
+
+
+def power_capped(clocks):
+    """The timed region ran under the power cap: the sampler saw
+    sw_power_cap active."""
+    return "sw_power_cap" in clocks.get("reasons", [])
 
 
 def run_gpu(args):
@@ -531,8 +541,12 @@ def run_gpu(args):
         e2e = {"value": round(e2e_val, 3), "unit": "TFLOPS", "h2d_bytes_per_step": wl.h2d,
                "d2h_bytes_per_step": wl.d2h, "steps": e2e_steps}
 
+    clocks = clk.summary()
     peaks, peak_src = load_peaks()
-    peak, peak_how = peak_tflops(peaks, wl.peak_kind)
+    capped = power_capped(clocks)
+    peak, peak_how = peak_tflops(peaks, wl.peak_kind, capped)
+    peak_how += ("; sw_power_cap was active in the timed region" if capped
+                 else "; no power cap seen in the timed region")
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     roofline = {"kernel": wl.dominant, "bound": "tensor", "achieved": round(achieved, 2),
                 "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -561,7 +575,7 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": wl.launches_per_step * args.steps,
-            "clocks": clk.summary(),
+            "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

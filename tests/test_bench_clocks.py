@@ -60,3 +60,19 @@ def test_sampler_without_nvidia_smi(tmp_path, monkeypatch):
         pass
     s = clk.summary()
     assert s["reasons"] == ["unavailable"] and s["samples"] == 0
+
+
+def test_peak_follows_the_power_cap_seen():
+    """The roofline denominator: the burst bf16 figure for a region that ran
+    below the power cap, the sustained one for a region that ran under it;
+    FP8 and FP4 scale it by the nominal dense ratios 2 and 6."""
+    import bench
+    peaks = {"bf16_tflops": 1971.4, "bf16_tflops_sustained": 1745.6}
+    assert bench.peak_tflops(peaks, "fp8", False)[0] == 2 * 1971.4
+    assert bench.peak_tflops(peaks, "fp8", True)[0] == 2 * 1745.6
+    assert bench.peak_tflops(peaks, "fp4", False)[0] == 6 * 1971.4
+    assert bench.peak_tflops(peaks, "int8", True)[0] == 1745.6
+    assert "bf16_tflops_sustained" in bench.peak_tflops(peaks, "fp8", True)[1]
+    assert bench.power_capped({"reasons": ["sw_power_cap"]})
+    assert not bench.power_capped({"reasons": []})
+    assert not bench.power_capped({"reasons": ["unavailable"]})
