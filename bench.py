@@ -150,8 +150,8 @@ class ClockSampler:
     def set_window(self, t0, t1, note):
         self.window, self.note = (t0, t1), note
 
-    def summary(self):
-        t0, t1 = self.window
+    def summary(self, window=None):
+        t0, t1 = window or self.window
         rows = [r for t, r in self.rows if t0 <= t <= t1]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0,
@@ -498,6 +498,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         t_close = time.perf_counter()
         clk.set_window(t_open, t_close, "timed region")
+        region = (t_open, t_close)
         if clk.count(t_open, t_close) < 3:
             # a timed region shorter than a few sampling periods: the clocks
             # are those of further, untimed steps of the same workload run
@@ -542,11 +543,16 @@ def run_gpu(args):
                "d2h_bytes_per_step": wl.d2h, "steps": e2e_steps}
 
     clocks = clk.summary()
+    # the peak follows the samples inside the timed region alone: a region too
+    # short to be sampled has not reached the sustained regime
+    in_region = clk.summary(region)
+    capped = power_capped(in_region)
     peaks, peak_src = load_peaks()
-    capped = power_capped(clocks)
     peak, peak_how = peak_tflops(peaks, wl.peak_kind, capped)
-    peak_how += ("; sw_power_cap was active in the timed region" if capped
-                 else "; no power cap seen in the timed region")
+    peak_how += ("; sw_power_cap was active in the timed region" if capped else
+                 f"; no power cap among the {in_region['samples']} samples inside the timed region")
+    clocks["timed_region_samples"] = in_region["samples"]
+    clocks["timed_region_reasons"] = in_region["reasons"]
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     roofline = {"kernel": wl.dominant, "bound": "tensor", "achieved": round(achieved, 2),
                 "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),

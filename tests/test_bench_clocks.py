@@ -76,3 +76,19 @@ def test_peak_follows_the_power_cap_seen():
     assert bench.power_capped({"reasons": ["sw_power_cap"]})
     assert not bench.power_capped({"reasons": []})
     assert not bench.power_capped({"reasons": ["unavailable"]})
+
+
+def test_summary_of_a_sub_window(fake_smi):
+    """summary(window) keeps the samples of that window only (the peak choice
+    reads the timed region alone, not the untimed steps after it)."""
+    import bench
+    with bench.ClockSampler(0, period_ms=20) as clk:
+        t0 = time.perf_counter()
+        time.sleep(0.25)
+        t1 = time.perf_counter()
+        time.sleep(0.25)
+        t2 = time.perf_counter()
+        clk.set_window(t0, t2, "timed region and the untimed steps after it")
+    whole, part = clk.summary(), clk.summary((t0, t1))
+    assert 0 < part["samples"] < whole["samples"]
+    assert clk.summary((t2 + 10, t2 + 20))["samples"] == 0
