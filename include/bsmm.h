@@ -123,6 +123,9 @@ bsmm_status bsmm_selftest_wait_timeout(uint64_t timeout_ns, bsmm_stream_t stream
  * code format's largest value: E4M3 448, E5M2 57344, E2M1 6, INT8 127.
  * All arithmetic is binary32 with IEEE division (x/scale, never x*(1/scale));
  * rounding is to nearest, ties to even; floating codes saturate.
+ * Inputs are taken to be finite: the pages give no rule for NaN or
+ * infinity, the library does not look for them, and a block holding one gets
+ * unspecified codes and scale.
  *
  *   x        [rows, cols] input, element (r, c) at x[r*ld_x + c]; F32 or BF16.
  *   block_rows x block_cols
