@@ -136,3 +136,23 @@ def test_atom_layout_queries_and_validation_without_gpu(lib):
         lib.bsmm_gemm_workspace_size(1, 256, 384, 512, b.E4M3), lib.bsmm_gemm_workspace_size(1, 512, 384, 256, b.E4M3))
     assert bq(256, 512, 384, b.E5M2, fake, fake, fake, fake, fake, fake, fake, fake, 0, fake, fake, None, 0,
               None) == b.ERR_WORKSPACE
+
+
+def test_atom_sizes_follow_the_documented_geometry(lib):
+    """bsmm_scale_atoms_size over many shapes: 512-byte atoms, [B][ceil(R/256)
+    * 2 row tiles][ceil(K/kt) * kt/bs/4 atoms], kt the K of one 128-byte code
+    tile (128 for FP8, 256 for E2M1), bs the hardware block (32, or 16 for
+    UE4M3); zero for shapes the tensor cores take no scales for."""
+    import math
+    import random
+    import block_scaled_precision_gemm_gb300 as b
+    fmts = [(b.E4M3, b.SCALE_UE8M0, 128, 32), (b.E5M2, b.SCALE_UE8M0, 128, 32),
+            (b.E2M1, b.SCALE_UE8M0, 256, 32), (b.E2M1, b.SCALE_UE4M3, 256, 16)]
+    rnd = random.Random(7)
+    for _ in range(300):
+        code, scale, kt, bs = rnd.choice(fmts)
+        B, R, K = rnd.randint(1, 4), rnd.randint(1, 3000), bs * rnd.randint(1, 200)
+        want = B * math.ceil(R / 256) * 2 * math.ceil(K / kt) * (kt // bs // 4) * 512
+        assert lib.bsmm_scale_atoms_size(B, R, K, code, scale) == want, (B, R, K, code, scale)
+    assert lib.bsmm_scale_atoms_size(0, 64, 64, b.E4M3, b.SCALE_UE8M0) == 0
+    assert lib.bsmm_scale_atoms_size(1, 0, 64, b.E4M3, b.SCALE_UE8M0) == 0
