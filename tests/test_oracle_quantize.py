@@ -259,3 +259,41 @@ def test_fp_ties_round_half_even_through_quantizer():
     c, s = Q.quantize(x, (1, 4), "e4m3", "f32")
     assert s[0, 0] == 1.0
     assert F.decode(c, "e4m3").tolist() == [[448.0, 1.0, 1.25, -1.0]]
+
+
+def test_ceil_log2_meets_its_definition():
+    """ceil(log2 r) is the integer c with 2^(c-1) < r <= 2^c, checked in exact
+    arithmetic on powers of two, their float32 neighbours, subnormals and
+    random values over the whole binary32 range."""
+    rng = np.random.default_rng(3)
+    powers = np.array([2.0 ** e for e in range(-149, 128)], np.float32)
+    r = np.concatenate([powers, np.nextafter(powers, np.float32(np.inf)), np.nextafter(powers, np.float32(0)),
+                        rng.uniform(1e-3, 1e3, 2000).astype(np.float32),
+                        (2.0 ** rng.uniform(-140, 127, 2000)).astype(np.float32)])
+    r = r[(r > 0) & np.isfinite(r)]
+    c = Q.ceil_log2(r)
+    for v, ci in zip(r.tolist(), c.tolist()):
+        assert math.ldexp(1.0, ci - 1) < v <= math.ldexp(1.0, ci), (v, ci)
+
+
+def test_int8_per_column_is_per_row_of_the_transpose():
+    """A per-column scale of w is the per-row scale of w^T: codes and scales
+    agree element for element (TensorTonic, problem statement)."""
+    rng = np.random.default_rng(4)
+    w = rng.standard_normal((37, 23)).astype(np.float32)
+    w[:, 5] = 0
+    qc, sc = Q.int8_per_col(w)
+    qr, sr = Q.int8_per_row(w.T.copy())
+    np.testing.assert_array_equal(qc, qr.T)
+    np.testing.assert_array_equal(sc, sr)
+    assert sc[5] == 1.0 and not qc[:, 5].any()
+
+
+def test_code_values_ties_and_saturation():
+    """Quotients on a tie go to the even integer (INT8) and past the format's
+    largest value saturate to it (INT8 127, E4M3 448, E5M2 57344, E2M1 6)."""
+    q = np.array([2.5, -2.5, 3.5, 0.5, -0.5, 127.6, -300.0], np.float32)
+    np.testing.assert_array_equal(Q.code_values(q, "int8"), [2, -2, 4, 0, 0, 127, -127])
+    for code, top in (("e4m3", 448.0), ("e5m2", 57344.0), ("e2m1", 6.0)):
+        v = F.decode(Q.code_values(np.array([top * 4, -top * 4, top], np.float32), code), code)
+        np.testing.assert_array_equal(v, [top, -top, top])
