@@ -156,3 +156,17 @@ def test_atom_sizes_follow_the_documented_geometry(lib):
         assert lib.bsmm_scale_atoms_size(B, R, K, code, scale) == want, (B, R, K, code, scale)
     assert lib.bsmm_scale_atoms_size(0, 64, 64, b.E4M3, b.SCALE_UE8M0) == 0
     assert lib.bsmm_scale_atoms_size(1, 0, 64, b.E4M3, b.SCALE_UE8M0) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """Without the compiled library every entry point raises: there is no CPU
+    or other fallback path."""
+    import block_scaled_precision_gemm_gb300 as b
+    monkeypatch.setattr(b, "_LIB", None)
+    monkeypatch.setattr(b, "library_path", str(tmp_path / "libbsmm.so"))
+    with pytest.raises(RuntimeError, match="is missing"):
+        b.lib()
+    with pytest.raises(RuntimeError, match="is missing"):
+        b.gemm_workspace_size(1, 128, 128, 128, "e4m3")
+    with pytest.raises(RuntimeError, match="is missing"):
+        b.version()
