@@ -301,8 +301,13 @@ bsmm_status bsmm_int8_channel(const float* x, const float* w, int64_t B, int64_t
  *
  *   dY [M, N], W [N, K], X [M, K] bfloat16, contiguous.
  *   dX [M, K], dW [N, K] bfloat16, contiguous.
- *   workspace  at least bsmm_linear_backward_workspace_size() bytes (the
- *            four quantized operands, their scales in the atom layout below).
+ *   workspace  at least bsmm_linear_backward_workspace_size() bytes,
+ *            256-byte aligned.  The call leaves the four quantized operands
+ *            there, in this order, each part starting on a 256-byte boundary:
+ *            the codes of dY along N [M, N], then their scales in the atom
+ *            layout below (bsmm_scale_atoms_size(1, M, N, fp8_type, UE8M0)
+ *            bytes); W^T along N [K, N] and its atoms; dY^T along M [N, M]
+ *            and its atoms; X^T along M [K, M] and its atoms.
  *   M, N and K must be multiples of 32.
  */
 size_t bsmm_linear_backward_workspace_size(int64_t M, int64_t N, int64_t K);

@@ -2,9 +2,12 @@
 tensor cores' own layout"; NKI backward page, Parameters: pre-computed scales
 and pre-swizzled inputs).
 
-The atom quantizer must give the same codes and scale values as the
-row-major quantizer, placed by the layout the header documents; GEMMs and the
-backward fed atoms must give the same bits as when fed row-major scales."""
+Against the oracle: the atom quantizer's codes are bit-exact with the
+oracle's quantizer, and its atoms, read back through the layout the header
+documents, hold the oracle's scale bytes (neutral scale in the padding);
+GEMMs and the backward fed atoms built from the oracle's scales match the
+oracle's float64 products within the parity bound.  Against the row-major
+path: the same scales placed by the layout, and the same output bits."""
 import math
 
 import numpy as np
@@ -128,3 +131,117 @@ def test_atoms_reject_other_formats():
         bsmm.quantize_atoms(x, "e4m3", "ue4m3")
     with pytest.raises(bsmm.BsmmError):
         bsmm.quantize_atoms(x[:, :48].contiguous(), "e4m3", "ue8m0")  # K not a multiple of 32
+
+
+# ---------------------------------------------------------------------------
+# against the oracle
+# ---------------------------------------------------------------------------
+
+from oracle import formats as F  # noqa: E402
+from oracle import gemm as G  # noqa: E402
+from oracle import quantize as Q  # noqa: E402
+
+
+def _layout(B, R, K, fmt):
+    _, scale, bs, kt = FORMATS[fmt]
+    KS = K // bs
+    ks4 = math.ceil(K / kt) * (kt // bs // 4)
+    RT = math.ceil(R / 256) * 2
+    return KS, ks4, RT, (0 if scale == "ue4m3" else 127)
+
+
+def decode_atoms(atoms, B, R, K, fmt):
+    """The header's atom layout read back: scale bytes [B, R, K / bs]; asserts
+    that every padding byte holds the neutral scale."""
+    KS, ks4, RT, neutral = _layout(B, R, K, fmt)
+    a = np.asarray(atoms).reshape(B, RT, ks4, 512)
+    r = np.arange(RT * 128)
+    kb = np.arange(ks4 * 4)
+    byte = ((r % 128) % 32 * 16 + (r % 128) // 32 * 4)[:, None] + (kb % 4)[None, :]
+    full = a[:, (r // 128)[:, None], (kb // 4)[None, :], byte]  # [B, RT*128, ks4*4]
+    assert (full[:, R:, :] == neutral).all() and (full[:, :, KS:] == neutral).all(), "padding not neutral"
+    return full[:, :R, :KS]
+
+
+def encode_atoms(sc, B, R, K, fmt):
+    """Scale bytes [B, R, K / bs] written into the header's atom layout."""
+    return atoms_from_row_major(np.asarray(sc, np.uint8), B, R, K, fmt)
+
+
+@pytest.mark.parametrize("fmt", sorted(FORMATS))
+@pytest.mark.parametrize("B,R,K,transpose", [(1, 300, 384, False), (2, 130, 256, False), (1, 200, 288, True),
+                                             (1, 256, 1024, True)])
+def test_quantize_atoms_matches_oracle(fmt, B, R, K, transpose):
+    bsmm = _bsmm()
+    code, scale, bs, _ = FORMATS[fmt]
+    if K % bs:
+        pytest.skip("K must be a multiple of the block")
+    g = torch.Generator().manual_seed(7 * B * R + K)
+    x = (torch.randn(B * R, K, generator=g) * 3).to(torch.bfloat16)
+    xin = x.t().contiguous() if transpose else x
+    codes, atoms = bsmm.quantize_atoms(xin.cuda(), code, scale, batches=B, transpose=transpose)
+    torch.cuda.synchronize()
+    oc, osc = Q.quantize(x.float().numpy(), (1, bs), code, scale)
+    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
+    got = decode_atoms(atoms.cpu().numpy(), B, R, K, fmt)
+    np.testing.assert_array_equal(got, osc.reshape(B, R, -1))
+
+
+def _oracle_operand(fmt, Bn, R, K, g):
+    """Codes and scales by the oracle's quantizer from seeded draws, and the
+    scaled float64 operand."""
+    code, scale, bs, _ = FORMATS[fmt]
+    x = torch.randn(Bn * R, K, generator=g).numpy() * 2
+    c, s = Q.quantize(x, (1, bs), code, scale)
+    v = F.decode(F.unpack_e2m1(c), "e2m1") if code == "e2m1" else F.decode(c, code)
+    return c.reshape(Bn, R, -1), s.reshape(Bn, R, -1), G.scaled_operand(v, F.decode(s, scale)).reshape(Bn, R, K)
+
+
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+@pytest.mark.parametrize("fmt", sorted(FORMATS))
+@pytest.mark.parametrize("Bn,M,N,K", [(1, 512, 512, 512), (2, 300, 384, 768), (3, 600, 520, 256)])
+def test_gemm_atoms_matches_oracle(monkeypatch, kernel, fmt, Bn, M, N, K):
+    if fmt == "mxfp4" and kernel == "single":
+        pytest.skip("MXFP4 has only the pair kernel")
+    monkeypatch.setenv("BSMM_MX_KERNEL", kernel)
+    bsmm = _bsmm()
+    code, scale, _, _ = FORMATS[fmt]
+    g = torch.Generator().manual_seed(11 * Bn + M + 3 * N + K)
+    ca, sa, a_s = _oracle_operand(fmt, Bn, M, K, g)
+    cb, sb, b_s = _oracle_operand(fmt, Bn, N, K, g)
+    t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()  # noqa: E731
+    y = bsmm.gemm_atoms(t(ca), t(cb), t(encode_atoms(sa, Bn, M, K, fmt)), t(encode_atoms(sb, Bn, N, K, fmt)),
+                        code, code, scale, K=K)
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    y_ref = np.stack([a_s[i] @ b_s[i].T for i in range(Bn)])
+    bound = np.stack([np.abs(a_s[i]) @ np.abs(b_s[i]).T for i in range(Bn)])
+    ok = G.within_bound(y.cpu().numpy(), y_ref, bound)
+    assert ok.all(), f"{fmt}[{kernel}] {Bn}x{M}x{N}x{K}: {(~ok).sum()} entries outside the bound"
+
+
+@pytest.mark.parametrize("atoms", [True, False])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 384), (512, 256, 256), (1024, 768, 2048)])
+def test_backward_quantized_matches_oracle(atoms, M, N, K):
+    """dX and dW from operands the oracle quantized along their contraction
+    axes (NKI backward, introduction), with row-major or atom scales."""
+    bsmm = _bsmm()
+    g = torch.Generator().manual_seed(M + 2 * N + K)
+    dY = torch.randn(M, N, generator=g).to(torch.bfloat16).float().numpy()
+    W = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).float().numpy()
+    X = (torch.randn(M, K, generator=g) * 0.02).to(torch.bfloat16).float().numpy()
+    ops = {"dy_n": G.mx_quantize(dY, "cols", "e5m2"), "w_t": G.mx_quantize(W, "rows", "e5m2"),
+           "dy_t": G.mx_quantize(dY, "rows", "e5m2"), "x_t": G.mx_quantize(X, "rows", "e5m2")}
+    t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()  # noqa: E731
+    args = []
+    for c, s in ops.values():
+        R, Kc = c.shape
+        args += [t(c), t(encode_atoms(s[None], 1, R, Kc, "mxfp8_e5m2") if atoms else s)]
+    dX, dW = bsmm.linear_backward_quantized(*args, fp8="e5m2", scales_are_atoms=atoms)
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    op = {k: G.scaled_operand(F.decode(c, "e5m2"), F.decode(s, "ue8m0")) for k, (c, s) in ops.items()}
+    for got, a_s, b_s, what in ((dX, op["dy_n"], op["w_t"], "dX"), (dW, op["dy_t"], op["x_t"], "dW")):
+        ok = G.within_bound(got.float().cpu().numpy(), a_s @ b_s.T, np.abs(a_s) @ np.abs(b_s).T,
+                            out_round=G.BF16_HALF_ULP)
+        assert ok.all(), f"{what} (atoms={atoms}): {(~ok).sum()} entries outside the bound"

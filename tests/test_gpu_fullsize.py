@@ -1,9 +1,19 @@
 """Parity at the full benchmark sizes, in the launch configuration bench.py
 times: each test builds bench.py's workload object, runs one step through the
-C ABI, and checks sampled outputs against the oracle computed one entry at a
-time from the seeded raw inputs (rows/columns copied from the generator's
-output; nothing the library produced feeds the oracle).  Codes and scales of
-the sampled lines are checked bit-exact; outputs against the parity bound."""
+C ABI, and checks outputs against the oracle computed from the seeded raw
+inputs (rows and columns copied from the generator's output; nothing the
+library produced feeds the oracle).
+
+Sampling, per output matrix: 256 rows and 256 columns drawn at random give
+256 x 256 = 65,536 random entries, and the first and last 256 rows and
+columns are added, so that the four corner 256 x 256 tiles -- the ragged M
+tail among them -- are checked in full.  The reference for the whole grid of
+sampled rows x sampled columns is one float64 product of the oracle's scaled
+operands (``a_s[rows] @ b_s[cols].T``, the form its pins tie to the einsum of
+jax.nn.scaled_matmul, "Mathematically").  Codes and scales of the sampled
+lines are checked bit-exact; outputs against |y - y_ref| <= 2e-3 *
+sum_k |a_s * b_s| (plus half a bf16 ulp for bf16 outputs).  The INT8
+configuration is checked in full: every code, scale and output."""
 
 import gc
 
@@ -19,7 +29,8 @@ from oracle import quantize as Q
 
 pytestmark = pytest.mark.gpu
 REL = 2e-3
-N_SAMPLES = 48
+TILE = 256
+N_RANDOM = 256
 
 
 def _free():
@@ -29,11 +40,25 @@ def _free():
 
 def _check(y, y_ref, bound, what, out_round=0.0):
     ok = G.within_bound(y, y_ref, bound, REL, out_round)
-    assert ok.all(), f"{what}: {(~ok).sum()} of {ok.size} sampled entries outside the bound"
+    if not ok.all():
+        idx = np.argwhere(~ok)[:4].tolist()
+        raise AssertionError(f"{what}: {(~ok).sum()} of {ok.size} sampled entries outside the bound; first {idx}")
 
 
-def _rng(seed):
-    return np.random.default_rng(seed)
+def grid_lines(n, rng):
+    """N_RANDOM random lines of n, plus the first and the last TILE lines."""
+    rand = rng.choice(n, size=min(N_RANDOM, n), replace=False)
+    first = np.arange(min(TILE, n))
+    last = np.arange((n - 1) // TILE * TILE, n)
+    return np.unique(np.concatenate([rand, first, last]))
+
+
+def _rows(t, idx, device):
+    return t[torch.from_numpy(idx).to(device)]
+
+
+def _grid(t2d, rows, cols, device):
+    return t2d[torch.from_numpy(rows).to(device)][:, torch.from_numpy(cols).to(device)]
 
 
 @pytest.fixture(scope="module")
@@ -43,70 +68,70 @@ def device():
     return torch.device("cuda", 0)
 
 
+def test_grid_lines_cover_the_plan():
+    rng = np.random.default_rng(0)
+    for n in (237, 349, 4533, 704512):
+        lines = grid_lines(n, rng)
+        assert {0, n - 1} <= set(lines.tolist())
+        assert set(range((n - 1) // TILE * TILE, n)) <= set(lines.tolist())
+        assert lines.size >= min(n, N_RANDOM)
+
+
 def test_block_scaled_mm_sweep_sampled(device):
     """All eight Shapes-table problems, one bench step (quantize a, quantize
-    b, FP32-scale GEMM), ragged M tails included."""
+    b, FP32-scale GEMM)."""
     import block_scaled_precision_gemm_gb300 as bsmm
     wl = bench.GroupedWork(W.GROUPED_SWEEP, device)
     wl.step()
     torch.cuda.synchronize()
     assert bsmm.check_device_status()[0] == 0
-    rng = _rng(0)
+    rng = np.random.default_rng(0)
     for it in wl.items:
         p = it["p"]
-        rows = np.unique(np.concatenate([rng.integers(0, p.m, N_SAMPLES), [0, p.m - 1]]))
-        cols = rng.integers(0, p.n, rows.size)
-        groups = np.unique(cols // p.group_n)
+        rows, cols = grid_lines(p.m, rng), grid_lines(p.n, rng)
         # activations: the sampled rows, quantized per 1 x 128
-        a_rows = it["a_raw"][torch.from_numpy(rows).to(device)].cpu().numpy()
-        ca, sa = Q.quantize(a_rows, (1, p.group_k), "e4m3", "f32")
-        np.testing.assert_array_equal(it["aq"][torch.from_numpy(rows).to(device)].cpu().numpy(), ca)
-        np.testing.assert_array_equal(it["sa"][torch.from_numpy(rows).to(device)].cpu().numpy(), sa)
+        ca, sa = Q.quantize(_rows(it["a_raw"], rows, device).cpu().numpy(), (1, p.group_k), "e4m3", "f32")
+        np.testing.assert_array_equal(_rows(it["aq"], rows, device).cpu().numpy(), ca)
+        np.testing.assert_array_equal(_rows(it["sa"], rows, device).cpu().numpy(), sa)
         # weights: whole 128-row groups holding the sampled columns
-        b_rows = {}
-        for g in groups:
+        b_s = np.empty((cols.size, p.k))
+        for g in np.unique(cols // p.group_n):
             blk = it["b_raw"][g * p.group_n:(g + 1) * p.group_n].cpu().numpy()
             cb, sb = Q.quantize(blk, (p.group_n, p.group_k), "e4m3", "f32")
             np.testing.assert_array_equal(it["bq"][g * p.group_n:(g + 1) * p.group_n].cpu().numpy(), cb)
             np.testing.assert_array_equal(it["sb"][g].cpu().numpy(), sb[0])
-            b_rows[g] = (cb, sb)
-        got = it["y"][torch.from_numpy(rows).to(device), torch.from_numpy(cols).to(device)].cpu().numpy()
-        da = F.decode(ca, "e4m3")
-        db = np.stack([F.decode(b_rows[c // p.group_n][0][c % p.group_n], "e4m3") for c in cols])
-        sbs = np.stack([b_rows[c // p.group_n][1][0] for c in cols])
-        a_s = G.scaled_operand(da, sa)
-        b_s = G.scaled_operand(db, sbs)
-        y_ref = (a_s * b_s).sum(-1)
-        bound = np.abs(a_s * b_s).sum(-1)
-        _check(got, y_ref, bound, f"block_scaled_mm m={p.m} n={p.n} k={p.k}")
+            sel = np.flatnonzero(cols // p.group_n == g)
+            b_s[sel] = G.scaled_operand(F.decode(cb[cols[sel] % p.group_n], "e4m3"), np.repeat(sb, sel.size, 0))
+        a_s = G.scaled_operand(F.decode(ca, "e4m3"), sa)
+        got = _grid(it["y"], rows, cols, device).cpu().numpy()
+        _check(got, a_s @ b_s.T, np.abs(a_s) @ np.abs(b_s).T, f"block_scaled_mm m={p.m} n={p.n} k={p.k}")
     del wl
     _free()
 
 
-def test_int8_per_channel_sampled(device):
-    """B = D_in = D_out = 4096 with zeroed rows/columns; y within 1e-6 of
-    acc*sx*sw from exact integer sums; codes and scales bit-exact."""
+def test_int8_per_channel_full(device):
+    """B = D_in = D_out = 4096 with zeroed rows/columns, checked in full:
+    codes and scales bit-exact, the integer sums exact (a float64 product of
+    integer codes is exact below 2^53), y within 1e-6 of acc * s_x * s_w, and
+    a zero sum gives exactly 0."""
     wl = bench.Int8Work(W.INT8_4096, device)
     wl.step()
     torch.cuda.synchronize()
-    rng = _rng(1)
-    p = wl.p
-    zero_rows = W.zero_lines(p.B, p.zero_frac, W.INT8_4096.seed, W.S_ZERO_ROWS).numpy()
-    bs = np.concatenate([rng.integers(0, p.B, N_SAMPLES), zero_rows[:2]])
-    js = rng.integers(0, p.D_out, bs.size)
-    for b, j in zip(bs, js):
-        x = wl.x[b:b + 1].cpu().numpy()
-        w = wl.wt[:, j:j + 1].cpu().numpy()
-        ref = G.int8_channel(x, w)
-        np.testing.assert_array_equal(wl.out["x_q"][b].cpu().numpy(), ref["x_q"][0])
-        np.testing.assert_array_equal(wl.out["w_q"][:, j].cpu().numpy(), ref["w_q"][:, 0])
-        assert wl.out["x_scales"][b].item() == ref["x_scales"][0]
-        assert wl.out["w_scales"][j].item() == ref["w_scales"][0]
-        y = wl.out["y"][b, j].item()
-        yr = ref["y_ref"][0, 0]
-        assert abs(y - yr) <= 1e-6 * abs(yr), (b, j, y, yr)
-        if ref["acc"][0, 0] == 0:
-            assert y == 0.0
+    x, w = wl.x.cpu().numpy(), wl.wt.cpu().numpy()
+    x_q, x_s = Q.int8_per_row(x)
+    w_q, w_s = Q.int8_per_col(w)
+    np.testing.assert_array_equal(wl.out["x_q"].cpu().numpy(), x_q)
+    np.testing.assert_array_equal(wl.out["w_q"].cpu().numpy(), w_q)
+    np.testing.assert_array_equal(wl.out["x_scales"].cpu().numpy(), x_s)
+    np.testing.assert_array_equal(wl.out["w_scales"].cpu().numpy(), w_s)
+    acc = x_q.astype(np.float64) @ w_q.astype(np.float64)
+    y_ref = acc * x_s.astype(np.float64)[:, None] * w_s.astype(np.float64)[None, :]
+    y = wl.out["y"].cpu().numpy().astype(np.float64)
+    bad = np.abs(y - y_ref) > 1e-6 * np.abs(y_ref)
+    assert not bad.any(), f"{bad.sum()} entries beyond 1e-6 relative"
+    assert (y[acc == 0] == 0).all()
+    zero_rows = W.zero_lines(wl.p.B, wl.p.zero_frac, W.INT8_4096.seed, W.S_ZERO_ROWS).numpy()
+    assert (wl.out["x_scales"].cpu().numpy()[zero_rows] == 1.0).all()
     del wl
     _free()
 
@@ -114,72 +139,66 @@ def test_int8_per_channel_sampled(device):
 @pytest.mark.parametrize("workload", [W.MXFP8_BATCHED, W.NVFP4_SQUARE, W.MXFP4_SQUARE],
                          ids=["mxfp8", "nvfp4", "mxfp4"])
 def test_batched_scaled_matmul_sampled(device, workload):
-    """MXFP8 B=8 x 4096 x 4096 x 8192, NVFP4 and MXFP4 16384^3, one bench step."""
+    """MXFP8 B=8 x 4096 x 4096 x 8192, NVFP4 and MXFP4 16384^3, one bench
+    step; the first, the last and one random batch."""
     import block_scaled_precision_gemm_gb300 as bsmm
     wl = bench.MxWork(workload, device)
     wl.step()
     torch.cuda.synchronize()
     assert bsmm.check_device_status()[0] == 0
     p = wl.p
-    rng = _rng(2)
-    ib = rng.integers(0, p.B, N_SAMPLES)
-    im = np.concatenate([rng.integers(0, p.M, N_SAMPLES - 2), [0, p.M - 1]])
-    inn = np.concatenate([rng.integers(0, p.N, N_SAMPLES - 2), [p.N - 1, 0]])
-    idx_a = (torch.from_numpy(ib).to(device), torch.from_numpy(im).to(device))
-    idx_b = (torch.from_numpy(ib).to(device), torch.from_numpy(inn).to(device))
-    a, b = wl.a[idx_a].cpu().numpy(), wl.b[idx_b].cpu().numpy()
-    sa, sb = wl.sa[idx_a].cpu().numpy(), wl.sb[idx_b].cpu().numpy()
-    if p.fmt == "mxfp8":
-        da, db = F.decode(a, "e4m3"), F.decode(b, "e4m3")
-        dsa, dsb = F.decode(sa, "ue8m0"), F.decode(sb, "ue8m0")
-    elif p.fmt == "mxfp4":
-        da, db = F.decode(F.unpack_e2m1(a), "e2m1"), F.decode(F.unpack_e2m1(b), "e2m1")
-        dsa, dsb = F.decode(sa, "ue8m0"), F.decode(sb, "ue8m0")
-    else:
-        da, db = F.decode(F.unpack_e2m1(a), "e2m1"), F.decode(F.unpack_e2m1(b), "e2m1")
-        dsa, dsb = F.decode(sa, "ue4m3"), F.decode(sb, "ue4m3")
-    a_s, b_s = G.scaled_operand(da, dsa), G.scaled_operand(db, dsb)
-    y_ref = (a_s * b_s).sum(-1)
-    bound = np.abs(a_s * b_s).sum(-1)
-    y = wl.y[(idx_a[0], idx_a[1], torch.from_numpy(inn).to(device))].cpu().numpy()
-    _check(y, y_ref, bound, workload.name)
+    rng = np.random.default_rng(2)
+    fmt = p.fmt
+    code = "e4m3" if fmt == "mxfp8" else "e2m1"
+    scale = "ue4m3" if fmt == "nvfp4" else "ue8m0"
+
+    def operand(codes, scales, idx):
+        c, s = _rows(codes, idx, device).cpu().numpy(), _rows(scales, idx, device).cpu().numpy()
+        v = F.decode(c, code) if code == "e4m3" else F.decode(F.unpack_e2m1(c), "e2m1")
+        return G.scaled_operand(v, F.decode(s, scale))
+
+    for b in np.unique([0, p.B - 1, rng.integers(0, p.B)]):
+        rows, cols = grid_lines(p.M, rng), grid_lines(p.N, rng)
+        a_s, b_s = operand(wl.a[b], wl.sa[b], rows), operand(wl.b[b], wl.sb[b], cols)
+        got = _grid(wl.y[b], rows, cols, device).cpu().numpy()
+        _check(got, a_s @ b_s.T, np.abs(a_s) @ np.abs(b_s).T, f"{workload.name} batch {b}")
     del wl
     _free()
 
 
 def test_linear_backward_sampled(device):
-    """M=16384, N=K=8192 bf16: sampled dX and dW entries, each from the lines
-    of dY, W and X it contracts, quantized by the oracle along its own
-    contraction axis."""
+    """M=16384, N=K=8192 bf16: grids of dX and dW, each from the lines of dY,
+    W and X it contracts, quantized by the oracle along its own contraction
+    axis."""
     import block_scaled_precision_gemm_gb300 as bsmm
     wl = bench.BackwardWork(W.BACKWARD, device)
     wl.step()
     torch.cuda.synchronize()
     assert bsmm.check_device_status()[0] == 0
     p = wl.p
-    rng = _rng(3)
+    rng = np.random.default_rng(3)
     fp8 = p.fp8
 
-    def q_line(v, fmt):  # one contraction line (length multiple of 32), blocks of 32
-        c, s = Q.quantize(v[None, :], (1, 32), fmt, "ue8m0")
-        return G.scaled_operand(F.decode(c, fmt), F.decode(s, "ue8m0"))[0]
+    def q_rows(v):  # contraction along the rows' own axis, blocks of 32
+        c, s = Q.quantize(v, (1, 32), fp8, "ue8m0")
+        return G.scaled_operand(F.decode(c, fp8), F.decode(s, "ue8m0"))
 
-    ms, ks = rng.integers(0, p.M, N_SAMPLES), rng.integers(0, p.K, N_SAMPLES)
-    got, ref, bnd = [], [], []
-    for m, k in zip(ms, ks):
-        dy = wl.dY[m].float().cpu().numpy()
-        wcol = wl.W[:, k].float().cpu().numpy()
-        prod = q_line(dy, fmt=fp8) * q_line(wcol, fmt=fp8)
-        got.append(wl.dX[m, k].float().item()); ref.append(prod.sum()); bnd.append(np.abs(prod).sum())
-    _check(np.array(got), np.array(ref), np.array(bnd), "dX", G.BF16_HALF_ULP)
-    ns, ks = rng.integers(0, p.N, N_SAMPLES), rng.integers(0, p.K, N_SAMPLES)
-    got, ref, bnd = [], [], []
-    for n, k in zip(ns, ks):
-        dycol = wl.dY[:, n].float().cpu().numpy()
-        xcol = wl.X[:, k].float().cpu().numpy()
-        prod = q_line(dycol, fmt=fp8) * q_line(xcol, fmt=fp8)
-        got.append(wl.dW[n, k].float().item()); ref.append(prod.sum()); bnd.append(np.abs(prod).sum())
-    _check(np.array(got), np.array(ref), np.array(bnd), "dW", G.BF16_HALF_ULP)
+    def q_cols(v):  # contraction down the columns: the transposed operand
+        c, s = Q.quantize(v, (32, 1), fp8, "ue8m0", transpose_out=True)
+        return G.scaled_operand(F.decode(c, fp8), F.decode(s, "ue8m0"))
+
+    # dX [M, K] = dY [M, N] . W [N, K]
+    ms, ks = grid_lines(p.M, rng), grid_lines(p.K, rng)
+    dy = q_rows(_rows(wl.dY, ms, device).float().cpu().numpy())
+    wt = q_cols(wl.W[:, torch.from_numpy(ks).to(device)].float().cpu().numpy())
+    _check(_grid(wl.dX, ms, ks, device).float().cpu().numpy(), dy @ wt.T, np.abs(dy) @ np.abs(wt).T, "dX",
+           G.BF16_HALF_ULP)
+    # dW [N, K] = dY^T [N, M] . X [M, K]
+    ns, ks = grid_lines(p.N, rng), grid_lines(p.K, rng)
+    dyt = q_cols(wl.dY[:, torch.from_numpy(ns).to(device)].float().cpu().numpy())
+    xt = q_cols(wl.X[:, torch.from_numpy(ks).to(device)].float().cpu().numpy())
+    _check(_grid(wl.dW, ns, ks, device).float().cpu().numpy(), dyt @ xt.T, np.abs(dyt) @ np.abs(xt).T, "dW",
+           G.BF16_HALF_ULP)
     del wl
     _free()
 
