@@ -456,21 +456,22 @@ def peak_tflops(peaks, kind, sustained):
         "int8": f"{key} (the INT8 matmul runs exactly on the bf16 tensor cores)"}[kind]
 
 
-def power_capped(clocks):
-    """The timed region ran under the power cap: the sampler saw
-    sw_power_cap active."""
-    return "sw_power_cap" in clocks.get("reasons", [])
+SUSTAINED_REGION_S = 2.0
 
 
-def run_gpu(args):
-    rank, world, local = dist_env()
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    dist_init(world, "nccl")
+def use_sustained_peak(clocks, region_s):
+    """The sustained bf16 figure was measured back to back for seconds under
+    the power cap; it is the denominator only for a timed region that is
+    itself seconds long and ran under the cap (sw_power_cap active).  A
+    shorter region is a burst, whatever the sampler saw."""
+    return region_s >= SUSTAINED_REGION_S and "sw_power_cap" in clocks.get("reasons", [])
+
+
+def measure(workload, args, device, rank, world, local, cpu_seconds):
+    """Runs one workload: warm-up, the timed region (CUDA events on the
+    launching stream, clocks sampled), the end-to-end leg, the CPU oracle
+    leg.  Returns the record's fields (rank 0 prints them)."""
     import block_scaled_precision_gemm_gb300 as bsmm
-    bsmm.lib()
-
-    workload = selected_workload(args)
     wl = make_work(workload, device)
     torch.cuda.synchronize()
 
@@ -543,14 +544,15 @@ def run_gpu(args):
                "d2h_bytes_per_step": wl.d2h, "steps": e2e_steps}
 
     clocks = clk.summary()
-    # the peak follows the samples inside the timed region alone: a region too
-    # short to be sampled has not reached the sustained regime
     in_region = clk.summary(region)
-    capped = power_capped(in_region)
+    region_s = region[1] - region[0]
+    sustained = use_sustained_peak(in_region, region_s)
     peaks, peak_src = load_peaks()
-    peak, peak_how = peak_tflops(peaks, wl.peak_kind, capped)
-    peak_how += ("; sw_power_cap was active in the timed region" if capped else
-                 f"; no power cap among the {in_region['samples']} samples inside the timed region")
+    peak, peak_how = peak_tflops(peaks, wl.peak_kind, sustained)
+    capped_seen = "sw_power_cap" in in_region.get("reasons", [])
+    peak_how += (f"; the {region_s:.2f} s timed region ran under the power cap" if sustained else
+                 f"; a {region_s:.2f} s timed region is a burst"
+                 + (" (sw_power_cap seen in it)" if capped_seen else ""))
     clocks["timed_region_samples"] = in_region["samples"]
     clocks["timed_region_reasons"] = in_region["reasons"]
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
@@ -563,39 +565,79 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(workload, min_seconds=args.cpu_seconds)
+        cpu = cpu_baseline(workload, min_seconds=cpu_seconds)
 
+    cfg = describe(workload)
+    cfg["l2"] = "inputs larger than L2 (%.2f GB resident inputs per step)" % (wl.input_bytes() / 1e9)
+    cfg["parallelism"] = f"replicas x{world}"
+    rec = {
+        "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_max_ms / args.steps, 4), "dtype": wl.dtype,
+        "config": cfg,
+        "pct_of_peak": round(100 * value / peak, 2),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    del wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+# The default run's other configurations, each a sub-record of the headline
+# line: the pages' remaining workloads and the next format (MXFP4).
+SUB_CONFIGS = ("int8", "mxfp8", "nvfp4", "backward", "mxfp4")
+
+
+def run_gpu(args):
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    import block_scaled_precision_gemm_gb300 as bsmm
+    bsmm.lib()
+
+    head = measure(selected_workload(args), args, device, rank, world, local, args.cpu_seconds)
+    subs = {}
+    if args.workload is None and not args.problem and not args.headline_only:
+        for key in SUB_CONFIGS:
+            rec = measure(WORKLOADS_BY_KEY[key], args, device, rank, world, local, args.sub_cpu_seconds)
+            if key == "mxfp4":
+                rec["note"] = "next format (MXFP4: E2M1 codes, UE8M0 scale per 32), at the NVFP4 size"
+            subs[key] = rec
     if rank == 0:
-        cfg = describe(workload)
-        cfg["l2"] = "inputs larger than L2 (%.2f GB resident inputs per step)" % (wl.input_bytes() / 1e9)
-        cfg["parallelism"] = f"replicas x{world}"
         line = {
             "metric": "block-scaled GEMM TFLOPS (2MNK/t) and % of GB300 dense FP8/FP4 tensor peak",
-            "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(t_max_ms / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "value": head["value"], "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
             "data": "synthetic (seeded draws with the pages' shapes and distributions)",
-            "config": cfg,
-            "pct_of_peak": round(100 * value / peak, 2),
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": wl.launches_per_step * args.steps,
-            "clocks": clocks,
+            "config": head["config"],
+            "pct_of_peak": head["pct_of_peak"],
+            "roofline": head["roofline"],
+            "cpu_baseline": head["cpu_baseline"],
+            "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"] + sum(r["gpu_launches"] for r in subs.values()),
+            "clocks": head["clocks"],
         }
+        if subs:
+            line["gpu_launches_headline"] = head["gpu_launches"]
+            line["configs"] = subs
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
-# the dominant kernel or call, from ncu captures of the same workloads
-# (profiles/traffic_by_workload.md); absent until captured for the kernels as
-# they stand.  sweep: the mean over the step's 8 GEMM launches.  mxfp8,
+# the dominant kernel or call, from ncu captures of the same workloads;
+# None until captured for the kernels as they stand.  sweep: the mean over the step's 8 GEMM launches.  mxfp8,
 # nvfp4, mxfp4: the GEMM launch (the scale relayouts add under 1%).
 # backward (5 launches) and int8 (3): the whole call.
 TRAFFIC_PER_LAUNCH = {
-    W.GROUPED_SWEEP.name: 1_971_545_000,
+    W.GROUPED_SWEEP.name: None,
     W.MXFP8_BATCHED.name: 1_325_603_584,
     W.NVFP4_SQUARE.name: 4_285_872_000,
     W.MXFP4_SQUARE.name: 2_458_361_000,
@@ -759,7 +801,7 @@ def selected_workload(args) -> W.Workload:
     if args.problem:
         m, n, k = (int(v) for v in args.problem.split(","))
         return W.Workload(f"block_scaled_mm m={m} n={n} k={k}", W.GROUPED_SWEEP.seed, (W.Grouped(m, n, k),))
-    return WORKLOADS_BY_KEY[args.workload]
+    return WORKLOADS_BY_KEY[args.workload or "sweep"]
 
 
 WORKLOADS_BY_KEY = {"sweep": W.GROUPED_SWEEP, "small": W.GROUPED_SMALL, "int8": W.INT8_4096,
@@ -773,7 +815,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS_BY_KEY), default="sweep")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS_BY_KEY), default=None,
+                    help="one configuration alone (default: the sweep headline with every other "
+                         "configuration as a sub-record)")
+    ap.add_argument("--headline-only", action="store_true", help="the default run without the sub-records")
+    ap.add_argument("--sub-cpu-seconds", type=float, default=4.0,
+                    help="CPU oracle seconds for each sub-record's baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")

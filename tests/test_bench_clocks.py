@@ -62,10 +62,11 @@ def test_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     assert s["reasons"] == ["unavailable"] and s["samples"] == 0
 
 
-def test_peak_follows_the_power_cap_seen():
-    """The roofline denominator: the burst bf16 figure for a region that ran
-    below the power cap, the sustained one for a region that ran under it;
-    FP8 and FP4 scale it by the nominal dense ratios 2 and 6."""
+def test_peak_is_burst_unless_a_seconds_long_region_ran_under_the_cap():
+    """The roofline denominator: the burst bf16 figure, unless the timed
+    region lasted seconds (as the sustained figure's own measurement did) and
+    ran under the power cap; FP8 and FP4 scale it by the nominal dense ratios
+    2 and 6."""
     import bench
     peaks = {"bf16_tflops": 1971.4, "bf16_tflops_sustained": 1745.6}
     assert bench.peak_tflops(peaks, "fp8", False)[0] == 2 * 1971.4
@@ -73,9 +74,11 @@ def test_peak_follows_the_power_cap_seen():
     assert bench.peak_tflops(peaks, "fp4", False)[0] == 6 * 1971.4
     assert bench.peak_tflops(peaks, "int8", True)[0] == 1745.6
     assert "bf16_tflops_sustained" in bench.peak_tflops(peaks, "fp8", True)[1]
-    assert bench.power_capped({"reasons": ["sw_power_cap"]})
-    assert not bench.power_capped({"reasons": []})
-    assert not bench.power_capped({"reasons": ["unavailable"]})
+    capped = {"reasons": ["sw_power_cap"]}
+    assert bench.use_sustained_peak(capped, 3.0)
+    assert not bench.use_sustained_peak(capped, 0.58)  # a sub-second region is a burst
+    assert not bench.use_sustained_peak({"reasons": []}, 3.0)
+    assert not bench.use_sustained_peak({"reasons": ["unavailable"]}, 3.0)
 
 
 def test_summary_of_a_sub_window(fake_smi):
