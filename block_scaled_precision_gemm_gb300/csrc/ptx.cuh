@@ -406,6 +406,18 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Two bfloat16 lanes at once: each lane of the result has the larger
+// magnitude of the two inputs' lanes (its sign is the XOR of theirs, which
+// callers discard).  Exact: a maximum rounds nothing.
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// The magnitudes of a bfloat16 pair's low and high lanes as binary32.
+__device__ __forceinline__ float bf16_lo_abs(uint32_t v) { return fabsf(__uint_as_float(v << 16)); }
+__device__ __forceinline__ float bf16_hi_abs(uint32_t v) { return fabsf(__uint_as_float(v & 0xFFFF0000u)); }
+
 // --------------------------------------------------------------------------
 // Conversions (round to nearest even, saturate to the largest finite value)
 // --------------------------------------------------------------------------

@@ -576,8 +576,10 @@ constexpr int kCol2TileBytes = kColTileR * kCol2C * 2;  // 32 KB of bf16
 // DUAL: the same tiles are also quantized along their rows (1 x 32 blocks,
 // untransposed output described by p2: codes, scales and their layout), so
 // an array both GEMMs of the backward read along different axes (dY) is
-// read from HBM once.
-template <bool POW2, bool DUAL>
+// read from HBM once.  CODE (E4M3 or E5M2) is fixed at compile time, and
+// block maxima are taken on the bf16 pairs as loaded (packed max of
+// magnitudes): the kernel is bound by instruction issue, not by HBM.
+template <bool POW2, bool DUAL, int CODE>
 __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant__ CUtensorMap tm, QP p, int tiles_c,
                                                           int64_t n_tiles, int* status, uint64_t timeout_ns, QP p2) {
   extern __shared__ uint8_t qsm_raw[];
@@ -622,68 +624,72 @@ __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant_
     const int nc = static_cast<int>(p.cols - c0 < kCol2C ? p.cols - c0 : kCol2C);
     if (ok) {
       const uint32_t* tile = reinterpret_cast<const uint32_t*>(ring + st * kCol2TileBytes);
-#pragma unroll
-      for (int r = 0; r < 32; ++r) w[r] = tile[(32 * part + r) * (kCol2C / 2) + cp];
       if constexpr (DUAL) {
-        // along the rows: thread t takes tile row t / 2, columns 64 (t % 2)
-        // .. +63 (two blocks of 32).  Register k holds the row's 16-byte chunk
-        // (k + row) % 8, so that the eight threads of a load phase (four
-        // rows) hit different banks.
-        const int rr = t >> 1, hh = t & 1;
-        const int rot = rr & 7;
-        const uint4* src = reinterpret_cast<const uint4*>(tile + rr * (kCol2C / 2) + hh * 32);
-        uint4 q[8];
+        // along the rows: thread t takes 32-column block t % 4 of tile rows
+        // t / 4 and t / 4 + 64, so that four lanes cover a row and every code
+        // store writes whole 128-byte lines.  Rows are 256 bytes apart (the
+        // same banks), so each lane reads its block's four 16-byte chunks in
+        // the order rotated by rot: the eight lanes of a load phase (two rows
+        // x four blocks) then hit eight different bank groups.
+        const int blk = t & 3;
+        const int64_t gcol = c0 + 32 * blk;
+        constexpr int kScaleType = POW2 ? BSMM_SCALE_UE8M0 : BSMM_SCALE_UE4M3;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) q[k] = src[(k + rot) & 7];
-        float mb[2] = {0.f, 0.f};
+        for (int pass = 0; pass < 2; ++pass) {
+          const int rr = (t >> 2) + 64 * pass;
+          const int rot = 2 * (rr & 1) + (blk >> 1);
+          const uint4* src = reinterpret_cast<const uint4*>(tile + rr * (kCol2C / 2) + 16 * blk);
+          uint4 q[4];  // q[j] is the block's 16-byte chunk (j + rot) % 4
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t u[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
-          float m = 0.f;
+          for (int j = 0; j < 4; ++j) q[j] = src[(j + rot) & 3];
+          uint32_t m = 0u;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[j] << 16)), fabsf(__uint_as_float(u[j] & 0xFFFF0000u))));
-          const bool hi_blk = ((k + rot) & 7) >= 4;
-          mb[0] = hi_blk ? mb[0] : fmaxf(mb[0], m);
-          mb[1] = hi_blk ? fmaxf(mb[1], m) : mb[1];
-        }
-        const Scale sc0 = make_scale(mb[0], p2.code, p2.scale);
-        const Scale sc1 = make_scale(mb[1], p2.code, p2.scale);
-        const int64_t grow = r0 + rr;
-        const int64_t gcol = c0 + 64 * hh;
-        if (grow < p.rows) {
-          uint8_t* drow = reinterpret_cast<uint8_t*>(p2.codes) + grow * p2.ld_codes + gcol;
+            m = bf16x2_max_abs(m, bf16x2_max_abs(bf16x2_max_abs(q[j].x, q[j].y), bf16x2_max_abs(q[j].z, q[j].w)));
+          const Scale sc = make_scale(fmaxf(bf16_lo_abs(m), bf16_hi_abs(m)), CODE, kScaleType);
+          uint2 v[4];  // codes of chunk (j + rot) % 4
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int lc = (k + rot) & 7;  // the chunk's 8 columns: gcol + 8 lc ..
-            const Scale& sc = lc >= 4 ? sc1 : sc0;
-            const uint32_t lo = encode4<POW2>(__uint_as_float(q[k].x << 16), __uint_as_float(q[k].x & 0xFFFF0000u),
-                                              __uint_as_float(q[k].y << 16), __uint_as_float(q[k].y & 0xFFFF0000u),
-                                              sc, p2.code);
-            const uint32_t hi = encode4<POW2>(__uint_as_float(q[k].z << 16), __uint_as_float(q[k].z & 0xFFFF0000u),
-                                              __uint_as_float(q[k].w << 16), __uint_as_float(q[k].w & 0xFFFF0000u),
-                                              sc, p2.code);
-            if (gcol + 8 * lc < p.cols) *reinterpret_cast<uint2*>(drow + 8 * lc) = make_uint2(lo, hi);
+          for (int j = 0; j < 4; ++j) {
+            v[j].x = encode4<POW2>(__uint_as_float(q[j].x << 16), __uint_as_float(q[j].x & 0xFFFF0000u),
+                                   __uint_as_float(q[j].y << 16), __uint_as_float(q[j].y & 0xFFFF0000u), sc, CODE);
+            v[j].y = encode4<POW2>(__uint_as_float(q[j].z << 16), __uint_as_float(q[j].z & 0xFFFF0000u),
+                                   __uint_as_float(q[j].w << 16), __uint_as_float(q[j].w & 0xFFFF0000u), sc, CODE);
           }
-          // the row's scales for blocks gcol / 32 and gcol / 32 + 1 (cols % 32 == 0)
-          const int64_t kb = gcol / 32;
-          if (gcol < p.cols)
-            reinterpret_cast<uint8_t*>(p2.scales)[scale_index(p2, grow, kb)] = static_cast<uint8_t>(sc0.stored);
-          if (gcol + 32 < p.cols)
-            reinterpret_cast<uint8_t*>(p2.scales)[scale_index(p2, grow, kb + 1)] = static_cast<uint8_t>(sc1.stored);
+          // back into column order: rotate by rot (two conditional steps)
+          if (rot & 1) {
+            const uint2 l = v[3];
+            v[3] = v[2];
+            v[2] = v[1];
+            v[1] = v[0];
+            v[0] = l;
+          }
+          if (rot & 2) {
+            const uint2 a0 = v[0], a1 = v[1];
+            v[0] = v[2];
+            v[1] = v[3];
+            v[2] = a0;
+            v[3] = a1;
+          }
+          const int64_t grow = r0 + rr;
+          if (grow < p.rows && gcol < p.cols) {  // cols % 32 == 0: a block is all in or all out
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p2.codes) + grow * p2.ld_codes + gcol);
+            dst[0] = make_uint4(v[0].x, v[0].y, v[1].x, v[1].y);
+            dst[1] = make_uint4(v[2].x, v[2].y, v[3].x, v[3].y);
+            reinterpret_cast<uint8_t*>(p2.scales)[scale_index(p2, grow, gcol / 32)] = static_cast<uint8_t>(sc.stored);
+          }
         }
       }
+#pragma unroll
+      for (int r = 0; r < 32; ++r) w[r] = tile[(32 * part + r) * (kCol2C / 2) + cp];
     }
     if (__syncthreads_or(!ok)) break;  // every thread has read stage st (or the CTA gives up together)
     if (t == 0 && issued < my_n) issue(issued++);
-    float m0 = 0.f, m1 = 0.f;  // rows past the array read as zero
+    uint32_t mc = 0u;  // packed maxima of the two columns; rows past the array read as zero
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      m0 = fmaxf(m0, fabsf(__uint_as_float(w[r] << 16)));
-      m1 = fmaxf(m1, fabsf(__uint_as_float(w[r] & 0xFFFF0000u)));
-    }
-    const Scale s0 = make_scale(m0, p.code, p.scale);
-    const Scale s1 = make_scale(m1, p.code, p.scale);
+    for (int r = 0; r < 32; ++r) mc = bf16x2_max_abs(mc, w[r]);
+    constexpr int kColScale = POW2 ? BSMM_SCALE_UE8M0 : BSMM_SCALE_UE4M3;
+    const Scale s0 = make_scale(bf16_lo_abs(mc), CODE, kColScale);
+    const Scale s1 = make_scale(bf16_hi_abs(mc), CODE, kColScale);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int col = 2 * cp + h;
@@ -694,7 +700,7 @@ __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant_
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           f[j] = __uint_as_float(h ? (w[4 * g + j] & 0xFFFF0000u) : (w[4 * g + j] << 16));
-        q[g] = encode4<POW2>(f[0], f[1], f[2], f[3], h ? s1 : s0, p.code);
+        q[g] = encode4<POW2>(f[0], f[1], f[2], f[3], h ? s1 : s0, CODE);
       }
       uint8_t* row = ostg + col * kColTileR;
       *reinterpret_cast<uint4*>(row + (((2 * part) ^ (col & 7)) * 16)) = make_uint4(q[0], q[1], q[2], q[3]);
@@ -892,8 +898,8 @@ __global__ void __launch_bounds__(256) quant_any(QP p) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-template <bool POW2, bool DUAL = false>
-cudaError_t launch_cols_tma2(const QP& p, const DeviceCtx* ctx, cudaStream_t s, const QP& p2 = QP{}) {
+template <bool POW2, bool DUAL, int CODE>
+cudaError_t launch_cols_tma2_code(const QP& p, const DeviceCtx* ctx, cudaStream_t s, const QP& p2) {
   CUtensorMap tm;
   if (!make_tmap_3d(&tm, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.cols, p.rows, 1, kCol2C, kColTileR, false))
     return cudaErrorInvalidValue;
@@ -901,12 +907,20 @@ cudaError_t launch_cols_tma2(const QP& p, const DeviceCtx* ctx, cudaStream_t s, 
   const int64_t n_tiles = static_cast<int64_t>(tiles_c) * ceil_div(p.rows, kColTileR);
   const int smem = kColStages * kCol2TileBytes + 128 + kColStages * 8;
   cudaError_t e =
-      cudaFuncSetAttribute(quant_cols_tma2<POW2, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(quant_cols_tma2<POW2, DUAL, CODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 2);
-  quant_cols_tma2<POW2, DUAL><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
+  quant_cols_tma2<POW2, DUAL, CODE><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
       tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns(), p2);
   return cudaGetLastError();
+}
+
+// The 8-bit code formats this kernel takes (E4M3, E5M2), as a template
+// parameter.
+template <bool POW2, bool DUAL = false>
+cudaError_t launch_cols_tma2(const QP& p, const DeviceCtx* ctx, cudaStream_t s, const QP& p2 = QP{}) {
+  return p.code == BSMM_E4M3 ? launch_cols_tma2_code<POW2, DUAL, BSMM_E4M3>(p, ctx, s, p2)
+                             : launch_cols_tma2_code<POW2, DUAL, BSMM_E5M2>(p, ctx, s, p2);
 }
 
 template <bool POW2>
@@ -980,7 +994,7 @@ cudaError_t launch_quantize_dual(const QuantRequest& qc, const QuantRequest& qr,
                         qc.transpose && qc.br == 32 && qc.bc == 1 && !qr.transpose && qr.br == 1 && qr.bc == 32 &&
                         qc.code == qr.code && qc.code != BSMM_E2M1 && qc.code != BSMM_INT8 && one_byte &&
                         qc.ld_x == qc.cols && qr.ld_x == qr.cols && qc.cols % 32 == 0 && aligned(qc.x, 16) &&
-                        aligned(qc.codes, 16) && qc.ld_codes % 32 == 0 && aligned(qr.codes, 8) && qr.ld_codes % 8 == 0;
+                        aligned(qc.codes, 16) && qc.ld_codes % 32 == 0 && aligned(qr.codes, 16) && qr.ld_codes % 16 == 0;
   if (!eligible) {
     cudaError_t e = launch_quantize(qc, s);
     return e != cudaSuccess ? e : launch_quantize(qr, s);
