@@ -12,7 +12,7 @@
 //   i8_quant_rows   one CTA per row of x: absmax, scale, codes into x_q and a
 //                   zero-padded K-major copy [B, Kp] the matmul reads (bf16,
 //                   or int8 for the fallback below).
-//   i8_quant_w_strip  all of w in one launch: a cluster of four CTAs per
+//   i8_quant_w_strip  all of w in one launch: a cluster of eight CTAs per
 //                   strip of 32 columns takes the column maxima (combined
 //                   through distributed shared memory), then the codes in the
 //                   page's layout [D_in, D_out] and transposed [D_out, Kp].
@@ -264,17 +264,21 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
 }
 
 // All of w's per-column quantization in one kernel.  A strip of 32 columns
-// goes to a cluster of four CTAs, CTA q taking rows q Kp/4 .. (q+1) Kp/4 - 1.
+// goes to a cluster of eight CTAs, CTA q taking rows q Kp/8 .. (q+1) Kp/8 - 1.
 // Thread (warp, lane) owns columns 4 (lane % 8) .. +3 of the strip and, in
 // each step of 256 rows, the 8 consecutive rows 8 (4 warp + lane / 8) .. +7.
 // Pass 1: column maxima of the CTA's rows (8 x 16-byte loads in flight per
-// thread); the four CTAs combine them through distributed shared memory.
-// Pass 2 reads the rows again -- from L2 when w fits there, as all strips
-// are in flight at once -- and writes the codes into w_q [D_in, D_out] (32
+// thread); the eight CTAs combine them through distributed shared memory.
+// Pass 2 reads the rows again -- from L2 when w fits there -- and writes the
+// codes into w_q [D_in, D_out] (32
 // bytes a row per strip) and into wqT [D_out, Kp], where a thread's 8 codes
 // of one column are 8 consecutive elements of a row (zero codes for rows
 // >= D_in).  Needs D_out % 4 == 0, w 16-byte and w_q 4-byte aligned.
-constexpr int kStrip = 32, kStripSplit = 4;
+// Eight CTAs a strip give 1.7 waves of CTAs at 4 per SM: the second wave's
+// DRAM pass overlaps the first wave's second pass (measured at D = 4096:
+// 42 us with four CTAs a strip in one wave, 37 us with eight, 54 with two,
+// 42 with sixteen).
+constexpr int kStrip = 32, kStripSplit = 8;
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(256, 4) i8_quant_w_strip(const float* __restri
   const int64_t n4 = D_out / 4;
   const float4* base = reinterpret_cast<const float4*>(w) + (jc / 4);
   const uint32_t q = cluster_ctarank();
-  const int64_t Kq = Kp / kStripSplit;  // a multiple of 32
+  const int64_t Kq = Kp / kStripSplit;  // a multiple of 16 (Kp % 128 == 0)
   const int64_t rbeg = q * Kq, rend = rbeg + Kq;
   const int64_t dend = D_in < rend ? D_in : rend;
   // pass 1: column maxima of this CTA's rows
@@ -338,7 +342,7 @@ __global__ void __launch_bounds__(256, 4) i8_quant_w_strip(const float* __restri
     for (int i = 1; i < 8; ++i) mm = fmaxf(mm, red[i][t]);
     part_max[t] = mm;
   }
-  cluster_sync();  // the four CTAs' partial maxima are visible
+  cluster_sync();  // the strip's partial maxima are visible
   if (t < kStrip) {
     const uint32_t a = smem_u32(&part_max[t]);
     float mm = 0.f;
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(256, 4) i8_quant_w_strip(const float* __restri
   }
   cluster_sync();  // peers have read part_max; sc is visible to the CTA
   const float s0 = sc[4 * cg], s1 = sc[4 * cg + 1], s2 = sc[4 * cg + 2], s3 = sc[4 * cg + 3];
-  // pass 2: codes, 256 rows at a time (rend - i0 is a multiple of 32, so a
+  // pass 2: codes, 256 rows at a time (rend - i0 is a multiple of 8, so a
   // thread's 8 rows are all below rend or all at or above it)
   for (int64_t i0 = rbeg; i0 < rend; i0 += 256) {
     const int64_t ir = i0 + 8 * rsub;
