@@ -140,8 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + C::NACC;
   uint64_t* done = tempty + C::NACC;
-  uint64_t* red_full = done + 1;              // split K, in the leader: the peers' partials are staged
-  uint64_t* red_empty = red_full + kEpiWarps;  // split K, in each peer: the leader has read them
+  uint64_t* red_full = done + 1;              // split K, in a block's owner: the peers' partials are staged
+  uint64_t* red_empty = red_full + kEpiWarps;  // split K, in each peer: the owner has read them
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_empty + kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int never_abort_storage = 0;  // drains ignore the CTA abort flag
@@ -402,38 +402,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if constexpr (MODE == kF32Scale) {
         if (p.splits > 1) {
-          // Split K: each peer stages its partial sums (32 rows x 64 columns
-          // per warp, 16-byte units rotated by lane) and signals the leader,
-          // which adds them in rank order and stores the tile.
+          // Split K, reduce-scatter: the 32 x 64 block of epilogue warp ew is
+          // summed and stored by rank ew % splits.  Every other rank stages
+          // its partial of that block (16-byte units rotated by lane) and
+          // signals the owner, which adds the partials and hands the staging
+          // buffers back.  Each rank reads (splits - 1) x 8 KB per block it
+          // owns instead of one rank reading them all.
+          const int owner = ew % p.splits;
           const uint32_t part = smem_u32(my_stg);
-          if (krank != 0) {
-            if (!mbar_wait_acq_cluster(&red_empty[ew], rph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteSplitK))
+          if (krank != owner) {
+            if (!mbar_spin_acq_cluster(&red_empty[ew], rph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteSplitK))
               break;
 #pragma unroll
             for (int j = 0; j < COLS / 4; ++j)
               *reinterpret_cast<float4*>(my_stg + 16 * (lane * 16 + (j ^ (lane & 15)))) =
                   make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
             __syncwarp();
-            if (lane == 0) mbar_arrive_release_cluster(mapa_shared(smem_u32(&red_full[ew]), 0));
+            if (lane == 0)
+              mbar_arrive_release_cluster(mapa_shared(smem_u32(&red_full[ew]), static_cast<uint32_t>(owner)));
             rph ^= 1u;
             continue;
           }
-          if (!mbar_wait_acq_cluster(&red_full[ew], rph, p.timeout_ns, abort_flag, p.status, kSiteSplitK)) break;
-          for (int r = 1; r < p.splits; ++r) {
+          if (!mbar_spin_acq_cluster(&red_full[ew], rph, p.timeout_ns, abort_flag, p.status, kSiteSplitK)) break;
+          // The owner adds the peers' blocks to its own in the fixed order
+          // owner + 1, owner + 2, .. (mod splits): deterministic for a given
+          // split count.  A peer's whole block is requested at once (16 reads
+          // in flight, each a round trip to another SM) before it is added.
+          for (int i = 1; i < p.splits; ++i) {
+            const int r = owner + i < p.splits ? owner + i : owner + i - p.splits;
             const uint32_t peer = mapa_shared(part, static_cast<uint32_t>(r));
+            float4 v[COLS / 4];
+#pragma unroll
+            for (int j = 0; j < COLS / 4; ++j) v[j] = ld_shared_cluster_v4(peer + 16 * (lane * 16 + (j ^ (lane & 15))));
 #pragma unroll
             for (int j = 0; j < COLS / 4; ++j) {
-              const float4 v = ld_shared_cluster_v4(peer + 16 * (lane * 16 + (j ^ (lane & 15))));
-              acc[4 * j] += v.x;
-              acc[4 * j + 1] += v.y;
-              acc[4 * j + 2] += v.z;
-              acc[4 * j + 3] += v.w;
+              acc[4 * j] += v[j].x;
+              acc[4 * j + 1] += v[j].y;
+              acc[4 * j + 2] += v[j].z;
+              acc[4 * j + 3] += v[j].w;
             }
           }
           __syncwarp();
           if (lane == 0)
-            for (int r = 1; r < p.splits; ++r)
-              mbar_arrive_release_cluster(mapa_shared(smem_u32(&red_empty[ew]), static_cast<uint32_t>(r)));
+            for (int r = 0; r < p.splits; ++r)
+              if (r != owner) mbar_arrive_release_cluster(mapa_shared(smem_u32(&red_empty[ew]), static_cast<uint32_t>(r)));
           rph ^= 1u;
         }
       }
@@ -865,15 +877,16 @@ cudaError_t launch_grouped_gemm(const GroupedGemmRequest& r, cudaStream_t s, std
   p.a_scales = r.a_scales;
   p.b_scales = r.b_scales;
   p.kb = static_cast<int>(r.K / 128);
-  // Split K in two when the tiles leave half the SMs idle and each half keeps
-  // at least 16 K tiles.  Measured (one-CTA kernel, us for 1 / 2 splits):
-  // m=512 n=2048 k=8192 29.3 / 23.5, m=237 n=k=4096 17.9 / 17.7, m=349
-  // n=k=2048 13.2 / 15.7 (8 K tiles a split: the tile's fixed costs, pipeline
-  // fill, cross-CTA sum and store, outweigh the shorter K loop).  Eight
-  // splits of m=256 n=1024 k=16384 ran slower than one (66.4 / 52.3).
-  // BSMM_GROUPED_SPLITK=n forces n splits, up to 8 (at least one K tile each).
+  // Split K: double the splits (up to 4) while the clusters still fit on the
+  // SMs at once and each split keeps at least 16 K tiles.  Measured (device
+  // time, CUDA-graph replay, us for 1 / 2 / 4 splits): m=237 n=k=4096
+  // 16.2 / 15.2 / 27.0; m=512 n=2048 k=8192 27.4 / 21.2 / 32.8; m=256 n=1024
+  // k=16384 49.2 / 31.2 / 22.6; m=349 n=k=2048 10.2 / 11.7 (8 K tiles a
+  // split: the fixed costs of a cluster launch and of the cross-CTA sum
+  // outweigh the shorter K loop).  Beyond the SM count, or past 4 splits, the
+  // clusters run in more than one round and it is slower again.
   int splits = 1;
-  if (2 * p.num_tiles <= ctx->num_sms && p.k_tiles >= 32) splits = 2;
+  while (splits < 4 && p.num_tiles * 2 * splits <= ctx->num_sms && p.k_tiles >= 32 * splits) splits *= 2;
   if (const char* fs = std::getenv("BSMM_GROUPED_SPLITK")) splits = std::max(1, std::min({8, std::atoi(fs), p.k_tiles}));
   p.kpb = static_cast<int>(ceil_div(p.k_tiles, splits));
   p.splits = static_cast<int>(ceil_div(p.k_tiles, p.kpb));  // no empty split

@@ -298,6 +298,36 @@ __device__ __forceinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t pa
     }
   }
 }
+// mbar_wait_acq_cluster without the suspend-time hint: for barriers whose
+// arrivals all come from other CTAs of the cluster, where a suspended waiter
+// was measured to sleep out its hint (about 2 us per wait) instead of waking
+// at the phase's completion.
+__device__ __forceinline__ bool mbar_test_acq_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_spin_acq_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                                      volatile int* abort, int* status, int site) {
+  if (mbar_test_acq_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_acq_cluster(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      record_timeout(status, site);
+      return false;
+    }
+  }
+}
 // 16 bytes of another CTA's shared memory (cluster-window address).
 __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
   float4 v;

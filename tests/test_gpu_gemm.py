@@ -79,8 +79,9 @@ def test_grouped_parity_each_kernel(monkeypatch, kernel, m, n, k):
 @pytest.mark.parametrize("m,n,k", [(349, 256, 2048), (237, 384, 1280), (64, 128, 640)])
 def test_grouped_split_k(monkeypatch, splits, m, n, k):
     """Split K on the one-CTA FP32-scale kernel (a cluster of `splits` CTAs
-    per tile, partial sums added in rank order through distributed shared
-    memory), including splits that do not divide the K tiles evenly."""
+    per tile; each 32 x 64 block's partials summed by one rank, in a fixed
+    order, through distributed shared memory), including splits that do not
+    divide the K tiles evenly."""
     monkeypatch.setenv("BSMM_GROUPED_KERNEL", "single")
     monkeypatch.setenv("BSMM_GROUPED_SPLITK", str(splits))
     y, y_ref, bound = run_grouped(*grouped_inputs(m, n, k, seed=m + 7 * splits))
