@@ -186,6 +186,12 @@ class Work:
     peak_kind = "fp8"
     dtype = "e4m3 (f32 accumulate)"
 
+    def quantizer_report(self, steps):
+        """Per-kernel HBM throughput of the step's quantizers, from CUDA events
+        on the launching stream (None where the quantizers run inside one
+        library call with the GEMM and cannot be timed apart)."""
+        return None
+
     def _timed(self, events, flops, fn):
         if events is None:
             return fn()
@@ -235,12 +241,34 @@ class GroupedWork(Work):
 
     def step(self, events=None):
         b = self.bsmm
+        qe = self.qevents if events is not None else None
         for it in self.items:
             p = it["p"]
-            b.quantize(it["a_raw"], (1, p.group_k), "e4m3", "f32", codes=it["aq"], scales=it["sa"])
-            b.quantize(it["b_raw"], (p.group_n, p.group_k), "e4m3", "f32", codes=it["bq"], scales=it["sb"])
+            # algorithmic bytes: float32 read, one code byte and the scales written
+            a_bytes = 4 * p.m * p.k + p.m * p.k + 4 * p.m * (p.k // p.group_k)
+            b_bytes = 4 * p.n * p.k + p.n * p.k + 4 * (p.n // p.group_n) * (p.k // p.group_k)
+            self._timed(qe["quant_rows (a, 1x128)"] if qe else None, a_bytes, lambda: b.quantize(
+                it["a_raw"], (1, p.group_k), "e4m3", "f32", codes=it["aq"], scales=it["sa"]))
+            self._timed(qe["quant_tile (b, 128x128)"] if qe else None, b_bytes, lambda: b.quantize(
+                it["b_raw"], (p.group_n, p.group_k), "e4m3", "f32", codes=it["bq"], scales=it["sb"]))
             self._timed(events, 2.0 * p.m * p.n * p.k, lambda: b.gemm_grouped(
                 it["aq"], it["bq"], it["sa"], it["sb"], p.group_n, p.group_k, y=it["y"]))
+
+    qevents = None
+
+    def start_quantizer_timing(self):
+        self.qevents = {"quant_rows (a, 1x128)": [], "quant_tile (b, 128x128)": []}
+
+    def quantizer_report(self, steps):
+        if not self.qevents:
+            return None
+        out = {}
+        for name, evs in self.qevents.items():
+            ms = sum(a.elapsed_time(b) for a, b, _ in evs)
+            nbytes = sum(n for _, _, n in evs)
+            out[name] = {"gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "us_per_step": round(1e3 * ms / steps, 1),
+                         "bytes_per_step": int(nbytes / steps)}
+        return out
 
     def setup_host(self):
         # one pinned buffer per direction, sized for the largest problem, reused
@@ -420,6 +448,49 @@ class BackwardWork(Work):
         self._timed(events, self.flops, lambda: self.bsmm.linear_backward(
             self.dY, self.W, self.X, self.p.fp8, dX=self.dX, dW=self.dW, workspace=self.ws))
 
+    def _quantized_operands(self):
+        """The four operands the call leaves in its workspace, in the order and
+        alignment the header documents: codes, then atoms, each part on a
+        256-byte boundary."""
+        p, ws, out, off = self.p, self.ws, [], 0
+        for rows, cols in ((p.M, p.N), (p.K, p.N), (p.N, p.M), (p.K, p.M)):
+            codes = ws[off:off + rows * cols].view(rows, cols)
+            off += -(-rows * cols // 256) * 256
+            n = self.bsmm.scale_atoms_size(1, rows, cols, p.fp8, "ue8m0")
+            out += [codes, ws[off:off + n]]
+            off += -(-n // 256) * 256
+        return out
+
+    def quantizer_report(self, steps):
+        """The call's quantization phase (the dual dY quantizer and the W^T and
+        X^T quantizers) as the call's time minus that of the same two GEMMs
+        run from the operands it quantized (bsmm_linear_backward_quantized on
+        its workspace); CUDA events on the launching stream."""
+        p = self.p
+        ops = self._quantized_operands()
+        dX, dW = torch.empty_like(self.dX), torch.empty_like(self.dW)
+        gemms = lambda: self.bsmm.linear_backward_quantized(*ops, fp8=p.fp8, scales_are_atoms=True,  # noqa: E731
+                                                           dX=dX, dW=dW)
+        full = lambda: self.step()  # noqa: E731
+        t = {}
+        for name, fn in (("call", full), ("gemms", gemms)):
+            for _ in range(3):
+                fn()
+            a, b = _ev(), _ev()
+            a.record()
+            for _ in range(steps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            t[name] = a.elapsed_time(b) / steps
+        q_ms = t["call"] - t["gemms"]
+        nbytes = (2 * p.M * p.N + 2 * p.M * p.N + 2 * p.M * p.N // 32     # dY read once, codes along both axes
+                  + 2 * p.N * p.K + p.N * p.K + p.N * p.K // 32           # W -> W^T
+                  + 2 * p.M * p.K + p.M * p.K + p.M * p.K // 32)          # X -> X^T
+        return {"quantization phase (dual dY, W^T, X^T)": {
+            "gbs": round(nbytes / (q_ms * 1e-3) / 1e9, 1), "us_per_step": round(1e3 * q_ms, 1),
+            "bytes_per_step": int(nbytes), "how": "call time minus the two GEMMs from its quantized operands"}}
+
     def config(self):
         p = self.p
         return {"M": p.M, "N": p.N, "K": p.K, "fp8": p.fp8,
@@ -487,6 +558,8 @@ def measure(workload, args, device, rank, world, local, cpu_seconds):
         raise RuntimeError(f"device status {st} (site {site}) after warm-up")
 
     events = []
+    if hasattr(wl, "start_quantizer_timing"):
+        wl.start_quantizer_timing()
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
@@ -563,6 +636,11 @@ def measure(workload, args, device, rank, world, local, cpu_seconds):
                 "peak_source": f"{peak_src}: {peak_how}",
                 "share_of_step": round(dom_ms / elapsed_ms, 4)}
 
+    quant = wl.quantizer_report(args.steps)
+    if quant:
+        hbm = load_peaks()[0]["hbm_gbs"]
+        for q in quant.values():
+            q["frac_of_hbm"] = round(q["gbs"] / hbm, 3)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(workload, min_seconds=cpu_seconds)
@@ -581,6 +659,8 @@ def measure(workload, args, device, rank, world, local, cpu_seconds):
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if quant:
+        rec["quantizers"] = quant
     del wl
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -623,6 +703,8 @@ def run_gpu(args):
             "gpu_launches": head["gpu_launches"] + sum(r["gpu_launches"] for r in subs.values()),
             "clocks": head["clocks"],
         }
+        if "quantizers" in head:
+            line["quantizers"] = head["quantizers"]
         if subs:
             line["gpu_launches_headline"] = head["gpu_launches"]
             line["configs"] = subs

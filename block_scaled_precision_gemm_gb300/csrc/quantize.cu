@@ -738,19 +738,21 @@ __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant_
 // 128 x 128 blocks
 // ---------------------------------------------------------------------------
 template <typename In, bool POW2>
-// Lane l of warp w owns columns 4l .. 4l+3 of rows w, w+8, ..., w+120: every
-// load instruction of a warp reads one whole tile row (512 bytes of FP32,
-// 256 of bf16) and every store writes that row's 128 codes.
-__global__ void __launch_bounds__(256) quant_tile(QP p) {
-  __shared__ float wmax[8];
+// 512 threads: lane l of warp w owns columns 4l .. 4l+3 of rows w, w+16, ...,
+// w+112, so every load instruction of a warp reads one whole tile row (512
+// bytes of FP32, 256 of bf16) and every store writes that row's 128 codes.
+// Sixteen warps of 32 values each (rather than eight of 64) keep four CTAs
+// on an SM, so one CTA's loads overlap another's divisions.
+__global__ void __launch_bounds__(512) quant_tile(QP p) {
+  __shared__ float wmax[16];
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
   const In* x = reinterpret_cast<const In*>(p.x) + (r0 + warp) * p.ld_x + c0 + 4 * lane;
-  float v[64];  // v[4k + j]: row warp + 8k, column 4 lane + j
+  float v[32];  // v[4k + j]: row warp + 16k, column 4 lane + j
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const In* src = x + static_cast<int64_t>(8 * k) * p.ld_x;
+  for (int k = 0; k < 8; ++k) {
+    const In* src = x + static_cast<int64_t>(16 * k) * p.ld_x;
     if constexpr (sizeof(In) == 4) {
       const float4 q = __ldg(reinterpret_cast<const float4*>(src));
       v[4 * k] = q.x;
@@ -767,20 +769,20 @@ __global__ void __launch_bounds__(256) quant_tile(QP p) {
   }
   float m = 0.f;
 #pragma unroll
-  for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(v[i]));
+  for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (lane == 0) wmax[warp] = m;
   __syncthreads();
   m = wmax[0];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
+  for (int i = 1; i < 16; ++i) m = fmaxf(m, wmax[i]);
   const Scale sc = make_scale(m, p.code, p.scale);
   if (t == 0) store_scale(p.scales, blockIdx.y * p.ld_scales + blockIdx.x, p.scale, sc.stored);
   uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
+  for (int k = 0; k < 8; ++k) {
     const uint32_t w = encode4<POW2>(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], sc, p.code);
-    const int64_t e = (r0 + warp + 8 * k) * p.ld_codes + c0 + 4 * lane;
+    const int64_t e = (r0 + warp + 16 * k) * p.ld_codes + c0 + 4 * lane;
     if (p.code == BSMM_E2M1)
       *reinterpret_cast<uint16_t*>(out + e / 2) = static_cast<uint16_t>(w);
     else
@@ -963,7 +965,7 @@ cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
                                                                                       n_tiles);
   } else if (p.br == 128 && p.bc == 128 && !p.transpose && x_vec && codes16) {
     dim3 grid(static_cast<unsigned>(p.cols / 128), static_cast<unsigned>(p.rows / 128));
-    quant_tile<In, POW2><<<grid, 256, 0, s>>>(p);
+    quant_tile<In, POW2><<<grid, 512, 0, s>>>(p);
   } else if (p.br == 1 && p.bc == p.cols && !p.transpose) {
     quant_wrow<In, POW2><<<static_cast<unsigned>(p.rows), 256, 0, s>>>(p);
   } else if (p.bc == 1 && p.br == p.rows) {
