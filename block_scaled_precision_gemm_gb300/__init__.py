@@ -31,7 +31,7 @@ import torch
 __all__ = [
     "BsmmError", "lib", "library_path", "quantize", "gemm", "gemm_noalloc", "gemm_grouped", "int8_channel",
     "linear_backward", "gemm_workspace_size", "int8_channel_workspace_size",
-    "linear_backward_workspace_size", "check_device_status", "selftest_wait_timeout",
+    "linear_backward_workspace_size", "check_device_status", "selftest_wait_timeout", "selftest_quotient",
     "scale_atoms_size", "quantize_atoms", "gemm_atoms", "linear_backward_quantized",
     "set_wait_timeout_ns", "version",
     "F32", "BF16", "E4M3", "E5M2", "E2M1", "INT8", "SCALE_F32", "SCALE_UE8M0", "SCALE_UE4M3",
@@ -69,6 +69,7 @@ _SIGS = {
     "bsmm_set_wait_timeout_ns": ([ctypes.c_uint64], None),
     "bsmm_check_device_status": ([_P, ctypes.POINTER(_INT)], _INT),
     "bsmm_selftest_wait_timeout": ([ctypes.c_uint64, _P], _INT),
+    "bsmm_selftest_quotient": ([ctypes.c_uint64, ctypes.c_uint64, _P, _P], _INT),
     "bsmm_quantize": ([_P, _INT, _I64, _I64, _I64, _INT, _INT, _INT, _INT, _INT, _P, _I64, _P, _I64, _P], _INT),
     "bsmm_gemm_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
     "bsmm_gemm": ([_I64, _I64, _I64, _I64, _P, _INT, _P, _INT, _P, _I64, _P, _I64, _INT, _P, _INT, _P, _SZ, _P],
@@ -194,6 +195,17 @@ def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
 # --------------------------------------------------------------------------- #
 # quantize                                                                    #
 # --------------------------------------------------------------------------- #
+
+def selftest_quotient(pairs: int, seed: int = 0, device=None) -> int:
+    """Pairs on which the quantizers' block quotient disagrees with the
+    hardware division (bsmm_selftest_quotient); 0 is the expected answer."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    bad = torch.zeros(1, dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().bsmm_selftest_quotient(int(pairs), int(seed) & (2**64 - 1), _ptr(bad), _stream(None)),
+               "bsmm_selftest_quotient")
+        return int(bad.item())
+
 
 def quantize(x: torch.Tensor, block, code="e4m3", scale="f32", transpose=False, codes=None, scales=None,
              stream=None):

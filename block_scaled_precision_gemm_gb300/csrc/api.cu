@@ -203,6 +203,13 @@ bsmm_status bsmm_selftest_wait_timeout(uint64_t timeout_ns, bsmm_stream_t stream
   return launched(launch_selftest_wait(timeout_ns, reinterpret_cast<cudaStream_t>(stream)), "selftest launch");
 }
 
+bsmm_status bsmm_selftest_quotient(uint64_t pairs, uint64_t seed, uint64_t* mismatches, bsmm_stream_t stream) {
+  if (!mismatches) return fail(BSMM_ERR_INVALID_ARG, "mismatches is NULL");
+  return launched(launch_selftest_quotient(pairs, seed, reinterpret_cast<unsigned long long*>(mismatches),
+                                           reinterpret_cast<cudaStream_t>(stream)),
+                  "selftest launch");
+}
+
 bsmm_status bsmm_quantize(const void* x, bsmm_dtype x_type, int64_t rows, int64_t cols, int64_t ld_x,
                           int block_rows, int block_cols, bsmm_dtype code_type, bsmm_scale_type scale_type,
                           int transpose_out, void* codes, int64_t ld_codes, void* scales, int64_t ld_scales,

@@ -32,6 +32,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quotient.cuh"
 
 namespace bsmm {
 namespace {
@@ -41,9 +42,34 @@ constexpr int kKpAlign = 128;  // padded K, elements per operand row (int8: 128-
 __device__ __forceinline__ float i8_scale(float absmax) {
   return absmax == 0.f ? 1.f : __fdiv_rn(absmax, 127.f);
 }
-__device__ __forceinline__ int8_t i8_code(float v, float s) {
-  const float q = fminf(fmaxf(__fdiv_rn(v, s), -127.f), 127.f);
+// round(clamp(v / s, -127, 127)), ties to even; y = block_recip(s).
+__device__ __forceinline__ int8_t i8_code(float v, float s, float y) {
+  const float q = fminf(fmaxf(y != 0.f ? quot_rn(v, s, y) : __fdiv_rn(v, s), -127.f), 127.f);
   return static_cast<int8_t>(__float2int_rn(q));
+}
+
+// The same for two elements, kept as floats t = q + 1.5 * 2^23: adding the
+// constant rounds the clamped quotient q to the nearest integer k (ties to
+// even: the ulp there is 1) and leaves k in the low bits of t's significand,
+// so t's low byte is k's two's-complement byte, and t - 1.5 * 2^23 is k as
+// an exact float (+0 for k = 0), whose upper 16 bits are k in bfloat16.
+// As with the division, a NaN element clamps to -127.
+constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
+__device__ __forceinline__ float2 i8_round2(float v0, float v1, float s, float y) {
+  float2 q = y != 0.f ? quot2_rn_int(make_float2(v0, v1), s, y) : make_float2(__fdiv_rn(v0, s), __fdiv_rn(v1, s));
+  q.x = fminf(fmaxf(q.x, -127.f), 127.f);
+  q.y = fminf(fmaxf(q.y, -127.f), 127.f);
+  return __fadd2_rn(q, make_float2(kRoundMagic, kRoundMagic));
+}
+// Code bytes of four rounded elements, element a lowest.
+__device__ __forceinline__ uint32_t i8_bytes4(float ta, float tb, float tc, float td) {
+  return __byte_perm(__byte_perm(__float_as_uint(ta), __float_as_uint(tb), 0x0040),
+                     __byte_perm(__float_as_uint(tc), __float_as_uint(td), 0x0040), 0x5410);
+}
+// bfloat16 copies of two rounded elements, element a in the low half.
+__device__ __forceinline__ uint32_t i8_bf16x2(float ta, float tb) {
+  const float2 k = __fadd2_rn(make_float2(ta, tb), make_float2(-kRoundMagic, -kRoundMagic));
+  return __byte_perm(__float_as_uint(k.x), __float_as_uint(k.y), 0x7632);
 }
 template <typename Pad>
 __device__ __forceinline__ Pad pad_code(int8_t q);
@@ -72,10 +98,10 @@ __global__ void __launch_bounds__(256) i8_quant_rows(const float* __restrict__ x
   m = wmax[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
-  const float s = i8_scale(m);
+  const float s = i8_scale(m), y = block_recip(s);
   if (threadIdx.x == 0) xs[r] = s;
   for (int64_t c = threadIdx.x; c < Kp; c += 256) {
-    const int8_t q = c < D ? i8_code(__ldg(row + c), s) : int8_t(0);
+    const int8_t q = c < D ? i8_code(__ldg(row + c), s, y) : int8_t(0);
     if (c < D) xq[r * D + c] = q;
     xq_pad[r * Kp + c] = pad_code<Pad>(q);
   }
@@ -107,19 +133,15 @@ __global__ void __launch_bounds__(256) i8_quant_rows_reg(const float* __restrict
   m = wmax[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
-  const float s = i8_scale(m);
+  const float s = i8_scale(m), y = block_recip(s);
   if (threadIdx.x == 0) xs[r] = s;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int c4 = threadIdx.x + 256 * i;
     if (c4 < n4) {
-      const int8_t q0 = i8_code(v[i].x, s), q1 = i8_code(v[i].y, s), q2 = i8_code(v[i].z, s), q3 = i8_code(v[i].w, s);
-      *reinterpret_cast<char4*>(xq + r * D + 4 * c4) = make_char4(q0, q1, q2, q3);
-      const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(q0))) |
-                          (static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(q1))) << 16);
-      const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(q2))) |
-                          (static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(q3))) << 16);
-      *reinterpret_cast<uint2*>(xb + r * Kp + 4 * c4) = make_uint2(lo, hi);
+      const float2 t01 = i8_round2(v[i].x, v[i].y, s, y), t23 = i8_round2(v[i].z, v[i].w, s, y);
+      *reinterpret_cast<uint32_t*>(xq + r * D + 4 * c4) = i8_bytes4(t01.x, t01.y, t23.x, t23.y);
+      *reinterpret_cast<uint2*>(xb + r * Kp + 4 * c4) = make_uint2(i8_bf16x2(t01.x, t01.y), i8_bf16x2(t23.x, t23.y));
     }
   }
   for (int64_t c = D + threadIdx.x; c < Kp; c += 256) xb[r * Kp + c] = __int2bfloat16_rn(0);
@@ -210,7 +232,7 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
   const int t = threadIdx.x;
   const int jj = t & 63, ig = t >> 6;  // column in tile, row group (16 rows each)
   const int64_t j = j0 + jj;
-  const float s = j < D_out ? i8_scale(__uint_as_float(colmax[j])) : 1.f;
+  const float s = j < D_out ? i8_scale(__uint_as_float(colmax[j])) : 1.f, y = block_recip(s);
   if (blockIdx.y == 0 && ig == 0 && j < D_out) ws[j] = s;
   float v[16];  // all sixteen loads in flight before any arithmetic
 #pragma unroll
@@ -224,7 +246,7 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
     const int64_t i = i0 + ii;
     int8_t q = 0;
     if (i < D_in && j < D_out) {
-      q = i8_code(v[k], s);
+      q = i8_code(v[k], s, y);
       wq[i * D_out + j] = q;
     }
     tile[ii][jj] = q;
@@ -267,10 +289,13 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
 // goes to a cluster of eight CTAs, CTA q taking rows q Kp/8 .. (q+1) Kp/8 - 1.
 // Thread (warp, lane) owns columns 4 (lane % 8) .. +3 of the strip and, in
 // each step of 256 rows, the 8 consecutive rows 8 (4 warp + lane / 8) .. +7.
-// Pass 1: column maxima of the CTA's rows (8 x 16-byte loads in flight per
-// thread); the eight CTAs combine them through distributed shared memory.
-// Pass 2 reads the rows again -- from L2 when w fits there -- and writes the
-// codes into w_q [D_in, D_out] (32
+// Pass 1: column maxima of the CTA's rows; the eight CTAs combine them
+// through distributed shared memory.  Up to 512 rows a CTA (D_in <= 4096)
+// the rows stay in registers between the passes (RES = 2: 16 x 16-byte
+// loads in flight per thread, two CTAs per SM), so w is read once; beyond
+// that pass 1 streams them (8 loads in flight) and pass 2 reads them again,
+// from L2 when w fits there.
+// Pass 2 writes the codes into w_q [D_in, D_out] (32
 // bytes a row per strip) and into wqT [D_out, Kp], where a thread's 8 codes
 // of one column are 8 consecutive elements of a row (zero codes for rows
 // >= D_in).  Needs D_out % 4 == 0, w 16-byte and w_q 4-byte aligned.
@@ -278,19 +303,19 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
 // DRAM pass overlaps the first wave's second pass (measured at D = 4096:
 // 42 us with four CTAs a strip in one wave, 37 us with eight, 54 with two,
 // 42 with sixteen).
-constexpr int kStrip = 32, kStripSplit = 8;
+constexpr int kStrip = 32, kStripSplit = 8, kStripResident = 2;
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
-template <typename Pad>
-__global__ void __launch_bounds__(256, 4) i8_quant_w_strip(const float* __restrict__ w, int64_t D_in, int64_t D_out,
-                                                        int64_t Kp, int8_t* __restrict__ wq, float* __restrict__ ws,
-                                                        Pad* __restrict__ wqT) {
+template <typename Pad, int RES>
+__global__ void __launch_bounds__(256, RES ? 2 : 4) i8_quant_w_strip(const float* __restrict__ w, int64_t D_in,
+                                                                  int64_t D_out, int64_t Kp, int8_t* __restrict__ wq,
+                                                                  float* __restrict__ ws, Pad* __restrict__ wqT) {
   __shared__ float red[8][kStrip];
   __shared__ float part_max[kStrip];
-  __shared__ float sc[kStrip];
+  __shared__ float sc[kStrip], yc[kStrip];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int cg = lane & 7;
   const int rsub = (warp << 2) | (lane >> 3);  // 0..31
@@ -305,7 +330,25 @@ __global__ void __launch_bounds__(256, 4) i8_quant_w_strip(const float* __restri
   const int64_t dend = D_in < rend ? D_in : rend;
   // pass 1: column maxima of this CTA's rows
   float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (col_ok) {
+  float4 keep[RES ? RES : 1][8];  // RES > 0: all of the CTA's rows, held for pass 2
+  if constexpr (RES > 0) {
+#pragma unroll
+    for (int it = 0; it < RES; ++it)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t r = rbeg + 256 * it + 8 * rsub + u;
+        keep[it][u] = (col_ok && r < dend) ? __ldg(base + r * n4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+    for (int it = 0; it < RES; ++it)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        m.x = fmaxf(m.x, fabsf(keep[it][u].x));
+        m.y = fmaxf(m.y, fabsf(keep[it][u].y));
+        m.z = fmaxf(m.z, fabsf(keep[it][u].z));
+        m.w = fmaxf(m.w, fabsf(keep[it][u].w));
+      }
+  } else if (col_ok) {
     for (int64_t r0 = rbeg; r0 < dend; r0 += 256) {
       float4 v[8];
 #pragma unroll
@@ -350,50 +393,56 @@ __global__ void __launch_bounds__(256, 4) i8_quant_w_strip(const float* __restri
     for (int c = 0; c < kStripSplit; ++c) mm = fmaxf(mm, ld_shared_cluster_f32(mapa_shared(a, c)));
     const float sv = i8_scale(mm);
     sc[t] = sv;
+    yc[t] = block_recip(sv);
     if (q == 0 && j0 + t < D_out) ws[j0 + t] = sv;
   }
   cluster_sync();  // peers have read part_max; sc is visible to the CTA
-  const float s0 = sc[4 * cg], s1 = sc[4 * cg + 1], s2 = sc[4 * cg + 2], s3 = sc[4 * cg + 3];
+  float scol[4], ycol[4];  // the thread's four columns
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    scol[c] = sc[4 * cg + c];
+    ycol[c] = yc[4 * cg + c];
+  }
   // pass 2: codes, 256 rows at a time (rend - i0 is a multiple of 8, so a
   // thread's 8 rows are all below rend or all at or above it)
-  for (int64_t i0 = rbeg; i0 < rend; i0 += 256) {
-    const int64_t ir = i0 + 8 * rsub;
+  const int n_it = RES ? RES : static_cast<int>((rend - rbeg + 255) / 256);
+#pragma unroll
+  for (int it = 0; it < n_it; ++it) {
+    const int64_t ir = rbeg + 256 * static_cast<int64_t>(it) + 8 * rsub;
     if (ir >= rend) break;
     float4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      v[u] = (col_ok && ir + u < dend) ? __ldg(base + (ir + u) * n4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    uint32_t code[8];  // row u: the four columns' codes, low byte first
-#pragma unroll
     for (int u = 0; u < 8; ++u) {
-      code[u] = static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[u].x, s0))) |
-                (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[u].y, s1))) << 8) |
-                (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[u].z, s2))) << 16) |
-                (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[u].w, s3))) << 24);
-      if (col_ok && ir + u < dend) *reinterpret_cast<uint32_t*>(wq + (ir + u) * D_out + jc) = code[u];
+      if constexpr (RES > 0)
+        v[u] = keep[it][u];
+      else
+        v[u] = (col_ok && ir + u < dend) ? __ldg(base + (ir + u) * n4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float2 t[4][4];  // column c, rows 2g and 2g + 1, rounded (i8_round2)
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      t[0][g] = i8_round2(v[2 * g].x, v[2 * g + 1].x, scol[0], ycol[0]);
+      t[1][g] = i8_round2(v[2 * g].y, v[2 * g + 1].y, scol[1], ycol[1]);
+      t[2][g] = i8_round2(v[2 * g].z, v[2 * g + 1].z, scol[2], ycol[2]);
+      t[3][g] = i8_round2(v[2 * g].w, v[2 * g + 1].w, scol[3], ycol[3]);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {  // row u: the four columns' codes, low byte first
+      const int g = u >> 1;
+      const uint32_t code = (u & 1) ? i8_bytes4(t[0][g].y, t[1][g].y, t[2][g].y, t[3][g].y)
+                                    : i8_bytes4(t[0][g].x, t[1][g].x, t[2][g].x, t[3][g].x);
+      if (col_ok && ir + u < dend) *reinterpret_cast<uint32_t*>(wq + (ir + u) * D_out + jc) = code;
     }
     if (wqT != nullptr && col_ok) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {  // column jc + c: rows ir .. ir+7
         Pad* dst = wqT + (jc + c) * Kp + ir;
         if constexpr (sizeof(Pad) == 1) {
-          uint32_t lo = 0, hi = 0;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            lo |= ((code[u] >> (8 * c)) & 0xFFu) << (8 * u);
-            hi |= ((code[u + 4] >> (8 * c)) & 0xFFu) << (8 * u);
-          }
-          *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+          *reinterpret_cast<uint2*>(dst) = make_uint2(i8_bytes4(t[c][0].x, t[c][0].y, t[c][1].x, t[c][1].y),
+                                                      i8_bytes4(t[c][2].x, t[c][2].y, t[c][3].x, t[c][3].y));
         } else {
-          uint32_t word[4];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int8_t a = static_cast<int8_t>((code[2 * g] >> (8 * c)) & 0xFFu);
-            const int8_t b = static_cast<int8_t>((code[2 * g + 1] >> (8 * c)) & 0xFFu);
-            word[g] = static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(a))) |
-                      (static_cast<uint32_t>(__bfloat16_as_ushort(__int2bfloat16_rn(b))) << 16);
-          }
-          *reinterpret_cast<uint4*>(dst) = make_uint4(word[0], word[1], word[2], word[3]);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(i8_bf16x2(t[c][0].x, t[c][0].y), i8_bf16x2(t[c][1].x, t[c][1].y),
+                                                      i8_bf16x2(t[c][2].x, t[c][2].y), i8_bf16x2(t[c][3].x, t[c][3].y));
         }
       }
     }
@@ -436,6 +485,8 @@ cudaError_t side_join(int dev, cudaStream_t main) {
 
 template <typename Pad>
 cudaError_t launch_w_strip(const Int8Request& r, int64_t Kp, Pad* wqT, cudaStream_t s) {
+  // up to 512 rows per CTA stay in registers between the two passes
+  const bool resident = Kp / kStripSplit <= 256 * kStripResident;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -448,7 +499,10 @@ cudaError_t launch_w_strip(const Int8Request& r, int64_t Kp, Pad* wqT, cudaStrea
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, i8_quant_w_strip<Pad>, r.w, static_cast<int64_t>(r.D_in),
+  if (resident)
+    return cudaLaunchKernelEx(&cfg, i8_quant_w_strip<Pad, kStripResident>, r.w, static_cast<int64_t>(r.D_in),
+                              static_cast<int64_t>(r.D_out), Kp, r.w_q, r.w_scales, wqT);
+  return cudaLaunchKernelEx(&cfg, i8_quant_w_strip<Pad, 0>, r.w, static_cast<int64_t>(r.D_in),
                             static_cast<int64_t>(r.D_out), Kp, r.w_q, r.w_scales, wqT);
 }
 

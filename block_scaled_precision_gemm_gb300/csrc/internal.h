@@ -146,6 +146,7 @@ cudaError_t launch_int8_gemm_pair(const Int8Request& r, const void* xb, const vo
                                   std::string* why);
 
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t s);
+cudaError_t launch_selftest_quotient(uint64_t pairs, uint64_t seed, unsigned long long* bad, cudaStream_t s);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

@@ -3,7 +3,9 @@
 // Rule (atrex-bench #002 block_scaled_mm, Input Generation; TensorTonic "Int8
 // Matmul with Per-Channel Scales", problem statement): per block, absmax =
 // largest |x|; scale from absmax (see make_scale); code = round(x / scale)
-// with saturation.  All arithmetic is binary32 with IEEE division.
+// with saturation.  All arithmetic is binary32; every quotient is the
+// correctly rounded IEEE x / scale (quotient.cuh: a per-block reciprocal and
+// two exact-remainder corrections, or a plain division).
 //
 // Kernels:
 //   quant_rows   1 x {16,32,64,128} blocks along the contiguous axis; a
@@ -19,6 +21,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quotient.cuh"
 
 namespace bsmm {
 namespace {
@@ -60,7 +63,7 @@ __device__ __forceinline__ float ue4m3_value(uint32_t b) {
 
 struct Scale {
   float s;          // the divisor
-  float inv;        // 1/s when s is a power of two (exact), else 0
+  float inv;        // POW2: 1/s (exact); else RN(1/s) for quotient.cuh, or 0 (divide)
   uint32_t stored;  // what is written: binary32 bits or the scale byte
 };
 
@@ -72,7 +75,7 @@ __device__ __forceinline__ Scale make_scale(float absmax, int code, int scale) {
     // FP8/FP4 (atrex-bench): max(absmax/qmax, 1e-10).
     const float s = (code == BSMM_INT8) ? (absmax == 0.f ? 1.f : r) : fmaxf(r, 1e-10f);
     out.s = s;
-    out.inv = 0.f;
+    out.inv = block_recip(s);
     out.stored = __float_as_uint(s);
   } else if (scale == BSMM_SCALE_UE8M0) {
     // Smallest power of two not below r: 2^ceil(log2 r), exponent in [-127,127].
@@ -108,7 +111,7 @@ __device__ __forceinline__ Scale make_scale(float absmax, int code, int scale) {
     }
     out.stored = b;
     out.s = ue4m3_value(b);
-    out.inv = 0.f;
+    out.inv = block_recip(out.s);
   }
   return out;
 }
@@ -120,13 +123,24 @@ __device__ __forceinline__ uint32_t int8_code(float q) {
 }
 
 // x / s, correctly rounded: a multiply by the exact reciprocal when s is a
-// power of two (POW2), IEEE division otherwise.
+// power of two (POW2), else quotient.cuh's corrected product, or a division
+// for divisors outside its range.
 template <bool POW2>
 __device__ __forceinline__ float quot(float x, const Scale& sc) {
   if constexpr (POW2)
     return x * sc.inv;
   else
-    return __fdiv_rn(x, sc.s);
+    return sc.inv != 0.f ? quot_rn(x, sc.s, sc.inv) : __fdiv_rn(x, sc.s);
+}
+
+template <bool POW2>
+__device__ __forceinline__ float2 quot2(float x0, float x1, const Scale& sc) {
+  if constexpr (POW2)
+    return make_float2(x0 * sc.inv, x1 * sc.inv);
+  else if (sc.inv != 0.f)
+    return quot2_rn(make_float2(x0, x1), sc.s, sc.inv);
+  else
+    return make_float2(__fdiv_rn(x0, sc.s), __fdiv_rn(x1, sc.s));
 }
 
 __device__ __forceinline__ uint32_t pack4(float q0, float q1, float q2, float q3, int code) {
@@ -144,7 +158,20 @@ __device__ __forceinline__ uint32_t pack4(float q0, float q1, float q2, float q3
 // the low byte) or 2 bytes (E2M1, element 0 in the low nibble).
 template <bool POW2>
 __device__ __forceinline__ uint32_t encode4(float x0, float x1, float x2, float x3, const Scale& sc, int code) {
-  return pack4(quot<POW2>(x0, sc), quot<POW2>(x1, sc), quot<POW2>(x2, sc), quot<POW2>(x3, sc), code);
+  const float2 q01 = quot2<POW2>(x0, x1, sc), q23 = quot2<POW2>(x2, x3, sc);
+  return pack4(q01.x, q01.y, q23.x, q23.y, code);
+}
+
+// The same where the block's quotients take the corrected product (POW2, or
+// sc.inv != 0), with no per-element test.
+template <bool POW2>
+__device__ __forceinline__ uint32_t encode4_fast(float x0, float x1, float x2, float x3, const Scale& sc, int code) {
+  if constexpr (POW2) {
+    return pack4(x0 * sc.inv, x1 * sc.inv, x2 * sc.inv, x3 * sc.inv, code);
+  } else {
+    const float2 q01 = quot2_rn(make_float2(x0, x1), sc.s, sc.inv), q23 = quot2_rn(make_float2(x2, x3), sc.s, sc.inv);
+    return pack4(q01.x, q01.y, q23.x, q23.y, code);
+  }
 }
 
 // One code (8-bit formats) or one nibble (E2M1).
@@ -741,10 +768,11 @@ template <typename In, bool POW2>
 // 512 threads: lane l of warp w owns columns 4l .. 4l+3 of rows w, w+16, ...,
 // w+112, so every load instruction of a warp reads one whole tile row (512
 // bytes of FP32, 256 of bf16) and every store writes that row's 128 codes.
-// Sixteen warps of 32 values each (rather than eight of 64) keep four CTAs
-// on an SM, so one CTA's loads overlap another's divisions.
+// Sixteen warps of 32 values each (rather than eight of 64): two CTAs on an
+// SM, so one CTA's loads overlap another's encoding.
 __global__ void __launch_bounds__(512) quant_tile(QP p) {
   __shared__ float wmax[16];
+  __shared__ Scale tile_sc;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
@@ -773,20 +801,32 @@ __global__ void __launch_bounds__(512) quant_tile(QP p) {
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (lane == 0) wmax[warp] = m;
   __syncthreads();
-  m = wmax[0];
-#pragma unroll
-  for (int i = 1; i < 16; ++i) m = fmaxf(m, wmax[i]);
-  const Scale sc = make_scale(m, p.code, p.scale);
-  if (t == 0) store_scale(p.scales, blockIdx.y * p.ld_scales + blockIdx.x, p.scale, sc.stored);
+  // warp 0 takes the tile's maximum and scale (the divisions once per tile)
+  if (warp == 0) {
+    m = lane < 16 ? wmax[lane] : 0.f;
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) {
+      const Scale s0 = make_scale(m, p.code, p.scale);
+      tile_sc = s0;
+      store_scale(p.scales, blockIdx.y * p.ld_scales + blockIdx.x, p.scale, s0.stored);
+    }
+  }
+  __syncthreads();
+  const Scale sc = tile_sc;
   uint8_t* out = reinterpret_cast<uint8_t*>(p.codes);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t w = encode4<POW2>(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], sc, p.code);
+  auto put = [&](int k, uint32_t w) {
     const int64_t e = (r0 + warp + 16 * k) * p.ld_codes + c0 + 4 * lane;
     if (p.code == BSMM_E2M1)
       *reinterpret_cast<uint16_t*>(out + e / 2) = static_cast<uint16_t>(w);
     else
       *reinterpret_cast<uint32_t*>(out + e) = w;
+  };
+  if (POW2 || sc.inv != 0.f) {  // the whole tile takes the same path
+#pragma unroll
+    for (int k = 0; k < 8; ++k) put(k, encode4_fast<POW2>(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], sc, p.code));
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) put(k, encode4<POW2>(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], sc, p.code));
   }
 }
 
@@ -1004,6 +1044,86 @@ cudaError_t launch_quantize_dual(const QuantRequest& qc, const QuantRequest& qr,
   const QP pc = to_qp(qc), pr = to_qp(qr);
   return qc.scale == BSMM_SCALE_UE8M0 ? launch_cols_tma2<true, true>(pc, ctx, s, pr)
                                       : launch_cols_tma2<false, true>(pc, ctx, s, pr);
+}
+
+namespace {
+// ---------------------------------------------------------------------------
+// Self-test: quotient.cuh against the hardware's correctly rounded division
+// ---------------------------------------------------------------------------
+// splitmix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+// generators", OOPSLA 2014): pair i draws from the hashes of seed + 2i, +1.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// One (x, s) pair: s in [2^-80, 2^126) with a random exponent and a random,
+// all-ones or zero significand; x one of
+//   0, 1  x = RN(t s) for a random quotient t with |t| in [2^-100, 2^18),
+//   2     x = RN(m s) nudged by up to two ulps, m a rounding midpoint
+//         (2j + 1) 2^(k-1) of the code grids (k in [-17, 7]): quotients
+//         that sit on or next to a tie,
+//   3     |x| < 2^-100: subnormals, zeros and tiny normals.
+// Counts a pair as bad unless the scalar and the packed forms agree bit for
+// bit with __fdiv_rn when neither |x| nor |x / s| is below 2^-100, and
+// otherwise give a quotient below 2^-19 with x's sign (as __fdiv_rn does).
+__global__ void __launch_bounds__(256) selftest_quotient_kernel(uint64_t pairs, uint64_t seed,
+                                                                unsigned long long* bad) {
+  unsigned long long nbad = 0;
+  for (uint64_t i = blockIdx.x * 256ull + threadIdx.x; i < pairs; i += gridDim.x * 256ull) {
+    const uint64_t h1 = splitmix64(seed + 2 * i), h2 = splitmix64(seed + 2 * i + 1);
+    const int es = -80 + static_cast<int>(h1 % 206u);
+    const uint32_t skind = static_cast<uint32_t>(h1 >> 8) & 7u;
+    const uint32_t sman = skind == 0 ? 0x7FFFFFu : (skind == 1 ? 0u : static_cast<uint32_t>(h1 >> 16) & 0x7FFFFFu);
+    const float s = __uint_as_float((static_cast<uint32_t>(es + 127) << 23) | sman);
+    const uint32_t sign = static_cast<uint32_t>(h2 >> 63) << 31;
+    const uint32_t xkind = static_cast<uint32_t>(h2) & 3u;
+    float x;
+    if (xkind < 2) {
+      const int d = -100 + static_cast<int>((h2 >> 2) % 118u);
+      const float t = __uint_as_float((static_cast<uint32_t>(d + 127) << 23) | (static_cast<uint32_t>(h2 >> 9) & 0x7FFFFFu));
+      x = __fmul_rn(t, s);
+    } else if (xkind == 2) {
+      const int k = -17 + static_cast<int>((h2 >> 2) % 25u);
+      const float m = ldexpf(static_cast<float>(2 * (static_cast<int>(h2 >> 8) & 255) + 1), k - 1);
+      const int nudge = static_cast<int>((h2 >> 16) % 5u) - 2;
+      x = __uint_as_float(__float_as_uint(__fmul_rn(m, s)) + nudge);
+    } else {
+      x = __uint_as_float(static_cast<uint32_t>(h2 >> 2) % (27u << 23));  // below 2^-100
+    }
+    x = __uint_as_float(__float_as_uint(x) | sign);
+    if (!(fabsf(x) < 0x1p127f)) continue;  // a nudge or product past the finite range
+    const float y = block_recip(s);
+    const float r = __fdiv_rn(x, s), nr = __fdiv_rn(-x, s);
+    const float q = quot_rn(x, s, y);
+    const float2 q2 = quot2_rn(make_float2(x, -x), s, y);
+    const float2 qi = quot2_rn_int(make_float2(x, -x), s, y);
+    bool ok;
+    if (fabsf(x) >= 0x1p-100f && fabsf(r) >= 0x1p-100f) {
+      ok = y != 0.f && __float_as_uint(q) == __float_as_uint(r) && __float_as_uint(q2.x) == __float_as_uint(r) &&
+           __float_as_uint(q2.y) == __float_as_uint(nr) && qi.x == r && qi.y == nr;
+    } else {
+      const uint32_t sx = __float_as_uint(x) & 0x80000000u;
+      ok = y != 0.f && fabsf(q) < 0x1p-19f && fabsf(q2.x) < 0x1p-19f && fabsf(q2.y) < 0x1p-19f &&
+           fabsf(qi.x) < 0x1p-19f && fabsf(qi.y) < 0x1p-19f && (__float_as_uint(q) & 0x80000000u) == sx &&
+           (__float_as_uint(q2.x) & 0x80000000u) == sx && (__float_as_uint(q2.y) & 0x80000000u) != sx &&
+           fabsf(r) < 0x1p-19f;
+    }
+    nbad += ok ? 0 : 1;
+  }
+  if (nbad) atomicAdd(bad, nbad);
+}
+}  // namespace
+
+cudaError_t launch_selftest_quotient(uint64_t pairs, uint64_t seed, unsigned long long* bad, cudaStream_t s) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  const uint64_t want = (pairs + 255) / 256;
+  const unsigned grid = static_cast<unsigned>(std::max<uint64_t>(1, std::min<uint64_t>(want, 8ull * ctx->num_sms)));
+  selftest_quotient_kernel<<<grid, 256, 0, s>>>(pairs, seed, bad);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s) {

@@ -107,6 +107,17 @@ bsmm_status bsmm_check_device_status(bsmm_stream_t stream, int* where);
  * returns.  Used to test the timeout path without faulting a GPU. */
 bsmm_status bsmm_selftest_wait_timeout(uint64_t timeout_ns, bsmm_stream_t stream);
 
+/* Diagnostic with no counterpart on the pages.  Every quantizer computes its
+ * binary32 quotient x / scale through one correctly rounded reciprocal per
+ * block and two exact-remainder correction steps (Markstein's method) instead
+ * of a division per element.  This checks that form against the hardware's
+ * IEEE division on `pairs` pseudo-random (x, s) pairs generated from `seed`
+ * on the GPU (divisors in [2^-80, 2^126), quotients on and next to rounding
+ * ties, tiny x), and adds the number of disagreements to the 64-bit counter at
+ * the device address `mismatches`, which the caller zeroes.  Asynchronous on
+ * `stream`; BSMM_ERR_INVALID_ARG if `mismatches` is NULL. */
+bsmm_status bsmm_selftest_quotient(uint64_t pairs, uint64_t seed, uint64_t* mismatches, bsmm_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Quantizer                                                                */
 /* ------------------------------------------------------------------------ */

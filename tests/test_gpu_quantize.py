@@ -5,6 +5,8 @@ the degenerate cases of the method: an all-zero row and column, negative
 zeros, quotients deep in the subnormal range and one value near the binary32
 maximum."""
 
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -99,3 +101,84 @@ def test_empty_input_launches_nothing():
     x = torch.empty((0, 128), device="cuda")
     c, s = bsmm.quantize(x, (1, 128), "e4m3", "f32")
     assert c.shape == (0, 128) and s.shape == (0, 1)
+
+
+def test_block_quotient_equals_ieee_division():
+    """Every quantizer divides through one correctly rounded reciprocal per
+    block and two exact-remainder corrections (Markstein's method) instead of
+    a division per element.  On 2 x 2^32 pseudo-random pairs -- divisors with
+    random, all-ones and zero significands, quotients on and next to the code
+    grids' rounding ties, tiny x -- it must agree bit for bit with the
+    hardware's correctly rounded division (bsmm_selftest_quotient)."""
+    import block_scaled_precision_gemm_gb300 as bsmm
+    for seed in (1, 2**40 + 7):
+        assert bsmm.selftest_quotient(1 << 32, seed) == 0
+
+
+def tie_input(rows, cols, block, code, seed):
+    """Blocks whose elements divide by the block's scale onto rounding ties of
+    the code grid, or one or two ulps beside them.  Each block holds its
+    absmax A once; the scale is s = A / qmax in binary32 (the method's FP32
+    scale), and the other elements are RN(m s) nudged by -2..2 ulps, with m a
+    midpoint between neighbouring codes (INT8: k + 1/2), so that x / s lands
+    within a few ulps of a tie."""
+    rng = np.random.default_rng(seed)
+    if code == "int8":
+        qmax = 127.0
+        mids = np.arange(-127, 127) + 0.5
+    else:
+        v = np.unique(np.abs(F.table(code)[np.isfinite(F.table(code))]))
+        mids = (v[:-1] + v[1:]) / 2
+        mids = np.concatenate([mids, -mids])
+        qmax = F.max_finite(code)
+    br, bc = block
+    x = np.empty((rows, cols), np.float32)
+    for i in range(0, rows, br):
+        for j in range(0, cols, bc):
+            A = np.float32(np.exp2(rng.uniform(-20, 20)))
+            if rng.random() < 0.3:  # an all-ones significand scale
+                A = (np.float32(np.exp2(np.floor(rng.uniform(-20, 20)))) * np.float32(2 - 2**-23)).astype(np.float32)
+            s = np.float32(A / np.float32(qmax))
+            m = rng.choice(mids, size=(br, bc))
+            blk = (m * np.float64(s)).astype(np.float32)
+            blk = (blk.view(np.int32) + rng.integers(-2, 3, size=blk.shape).astype(np.int32)).view(np.float32)
+            blk = np.clip(blk, -A, A)
+            blk.flat[rng.integers(0, br * bc)] = A
+            x[i:i + br, j:j + bc] = blk
+    return torch.from_numpy(x)
+
+
+@pytest.mark.parametrize("code,block", [("e4m3", (1, 128)), ("e5m2", (1, 128)), ("int8", (1, 128)),
+                                        ("e4m3", (128, 128)), ("int8", (128, 128)), ("e4m3", (32, 1)),
+                                        ("e4m3", (1, 16))])
+def test_quotients_on_rounding_ties(code, block):
+    import block_scaled_precision_gemm_gb300 as bsmm
+    x = tie_input(256, 512, block, code, seed=zlib.crc32(f"{code}{block}".encode()))
+    codes, scales = bsmm.quantize(x.cuda(), block, code, "f32")
+    torch.cuda.synchronize()
+    rc, rs = oracle_quantize(x, block, code, "f32", False)
+    got_c = codes.cpu().numpy()
+    if code == "int8":
+        got_c = got_c.astype(np.int8)
+    np.testing.assert_array_equal(got_c, rc)
+    np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint32), np.asarray(rs, np.float32).view(np.uint32))
+    assert bsmm.check_device_status()[0] == 0
+
+
+@pytest.mark.parametrize("B,D_in,D_out", [(256, 512, 384), (130, 4096, 256), (64, 4224, 128)])
+def test_int8_channel_codes_on_rounding_ties(B, D_in, D_out):
+    """The INT8 call's own quantizers (x per row, w per column, the latter
+    with the rows held in registers up to 4096 and streamed beyond) on
+    quotients at and beside k + 1/2."""
+    import block_scaled_precision_gemm_gb300 as bsmm
+    x = tie_input(B, D_in, (1, D_in), "int8", seed=B + D_in)
+    w = tie_input(D_in, D_out, (D_in, 1), "int8", seed=D_in + D_out)
+    out = bsmm.int8_channel(x.cuda(), w.cuda())
+    torch.cuda.synchronize()
+    xq, xs = Q.int8_per_row(x.numpy())
+    wq, ws = Q.int8_per_col(w.numpy())
+    np.testing.assert_array_equal(out["x_q"].cpu().numpy(), xq)
+    np.testing.assert_array_equal(out["w_q"].cpu().numpy(), wq)
+    np.testing.assert_array_equal(out["x_scales"].cpu().numpy().view(np.uint32), np.asarray(xs, np.float32).view(np.uint32))
+    np.testing.assert_array_equal(out["w_scales"].cpu().numpy().view(np.uint32), np.asarray(ws, np.float32).view(np.uint32))
+    assert bsmm.check_device_status()[0] == 0
