@@ -186,11 +186,48 @@ class Work:
     peak_kind = "fp8"
     dtype = "e4m3 (f32 accumulate)"
 
-    def quantizer_report(self, steps):
-        """Per-kernel HBM throughput of the step's quantizers, from CUDA events
-        on the launching stream (None where the quantizers run inside one
-        library call with the GEMM and cannot be timed apart)."""
-        return None
+    def quantizer_bytes(self):
+        """[(label, kernel name, algorithmic bytes per launch)] for the step's
+        quantizer launches, in launch order (a name that repeats is matched
+        in turn); empty where the step has none."""
+        return []
+
+    def quantizer_report(self, launches, steps):
+        """Per-kernel HBM throughput of the step's quantizers from the
+        library's own per-launch CUDA events (bsmm.trace over `steps` untimed
+        steps), and the span from the first quantizer's start to the last
+        one's end."""
+        want = self.quantizer_bytes()
+        if not want:
+            return None
+        out, spans = {}, []
+        per_step = len(launches) // steps
+        for st in range(steps):
+            mine = launches[st * per_step:(st + 1) * per_step]
+            used = [False] * len(mine)
+            t_lo, t_hi, nbytes = None, None, 0
+            for label, kname, nb in want:
+                i = next(i for i, (n, _, _) in enumerate(mine) if n == kname and not used[i])
+                used[i] = True
+                _, t0, ms = mine[i]
+                e = out.setdefault(label, {"kernel": kname, "ms": 0.0, "bytes": 0})
+                e["ms"] += ms
+                e["bytes"] += nb
+                t_lo = t0 if t_lo is None else min(t_lo, t0)
+                t_hi = t0 + ms if t_hi is None else max(t_hi, t0 + ms)
+                nbytes += nb
+            spans.append((t_hi - t_lo, nbytes))
+        rep = {}
+        for label, e in out.items():
+            rep[label] = {"kernel": e["kernel"], "gbs": round(e["bytes"] / (e["ms"] * 1e-3) / 1e9, 1),
+                          "us_per_step": round(1e3 * e["ms"] / steps, 2), "bytes_per_step": int(e["bytes"] / steps)}
+        if len(want) > 1:
+            ms = sum(t for t, _ in spans)
+            nb = sum(b for _, b in spans)
+            rep["all quantizers, first start to last end"] = {
+                "gbs": round(nb / (ms * 1e-3) / 1e9, 1), "us_per_step": round(1e3 * ms / steps, 2),
+                "bytes_per_step": int(nb / steps)}
+        return rep
 
     def _timed(self, events, flops, fn):
         if events is None:
@@ -235,40 +272,32 @@ class GroupedWork(Work):
                 "sb": torch.empty((p.n // p.group_n, p.k // p.group_k), dtype=torch.float32, device=device),
                 "y": torch.empty((p.m, p.n), dtype=torch.float32, device=device)})
         self.flops = sum(2.0 * it["p"].m * it["p"].n * it["p"].k for it in self.items)
-        self.launches_per_step = 3 * len(self.items)
         self.inputs = [t for it in self.items for t in (it["a_raw"], it["b_raw"])]
         self.outputs = [it["y"] for it in self.items]
 
     def step(self, events=None):
         b = self.bsmm
-        qe = self.qevents if events is not None else None
         for it in self.items:
             p = it["p"]
-            # algorithmic bytes: float32 read, one code byte and the scales written
-            a_bytes = 4 * p.m * p.k + p.m * p.k + 4 * p.m * (p.k // p.group_k)
-            b_bytes = 4 * p.n * p.k + p.n * p.k + 4 * (p.n // p.group_n) * (p.k // p.group_k)
-            self._timed(qe["quant_rows (a, 1x128)"] if qe else None, a_bytes, lambda: b.quantize(
-                it["a_raw"], (1, p.group_k), "e4m3", "f32", codes=it["aq"], scales=it["sa"]))
-            self._timed(qe["quant_tile (b, 128x128)"] if qe else None, b_bytes, lambda: b.quantize(
-                it["b_raw"], (p.group_n, p.group_k), "e4m3", "f32", codes=it["bq"], scales=it["sb"]))
+            b.quantize(it["a_raw"], (1, p.group_k), "e4m3", "f32", codes=it["aq"], scales=it["sa"])
+            b.quantize(it["b_raw"], (p.group_n, p.group_k), "e4m3", "f32", codes=it["bq"], scales=it["sb"])
             self._timed(events, 2.0 * p.m * p.n * p.k, lambda: b.gemm_grouped(
                 it["aq"], it["bq"], it["sa"], it["sb"], p.group_n, p.group_k, y=it["y"]))
 
-    qevents = None
-
-    def start_quantizer_timing(self):
-        self.qevents = {"quant_rows (a, 1x128)": [], "quant_tile (b, 128x128)": []}
-
-    def quantizer_report(self, steps):
-        if not self.qevents:
-            return None
-        out = {}
-        for name, evs in self.qevents.items():
-            ms = sum(a.elapsed_time(b) for a, b, _ in evs)
-            nbytes = sum(n for _, _, n in evs)
-            out[name] = {"gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "us_per_step": round(1e3 * ms / steps, 1),
-                         "bytes_per_step": int(nbytes / steps)}
+    def quantizer_bytes(self):
+        # algorithmic bytes: float32 read, one code byte and the scales written
+        out = []
+        for it in self.items:
+            p = it["p"]
+            out.append(("quant_rows (a, 1x128)", "quant_rows", 4 * p.m * p.k + p.m * p.k + 4 * p.m * (p.k // p.group_k)))
+            out.append(("quant_tile (b, 128x128)", "quant_tile",
+                        4 * p.n * p.k + p.n * p.k + 4 * (p.n // p.group_n) * (p.k // p.group_k)))
         return out
+
+    def quantizer_report(self, launches, steps):
+        rep = Work.quantizer_report(self, launches, steps)
+        rep.pop("all quantizers, first start to last end", None)  # the GEMMs run between them
+        return rep
 
     def setup_host(self):
         # one pinned buffer per direction, sized for the largest problem, reused
@@ -352,12 +381,19 @@ class Int8Work(Work):
         self.ws = torch.empty(bsmm.int8_channel_workspace_size(p.B, p.D_in, p.D_out), dtype=torch.uint8,
                               device=device)
         self.flops = 2.0 * p.B * p.D_in * p.D_out
-        self.launches_per_step = 3  # x quantizer, w strip quantizer (side stream), the matmul
         self.inputs, self.outputs = [self.x, self.wt], [self.out["y"]]
 
     def step(self, events=None):
         self._timed(events, self.flops, lambda: self.bsmm.int8_channel(self.x, self.wt, out=self.out,
                                                                       workspace=self.ws))
+
+    def quantizer_bytes(self):
+        # float32 read, int8 codes, the matmul's zero-padded bf16 copy, FP32 scales
+        p = self.p
+        Kp = -(-p.D_in // 128) * 128
+        return [("i8_quant_w_strip (w per column, second stream)", "i8_quant_w_strip",
+                 4 * p.D_in * p.D_out + p.D_in * p.D_out + 2 * p.D_out * Kp + 4 * p.D_out),
+                ("i8_quant_rows_reg (x per row)", "i8_quant_rows_reg", 4 * p.B * p.D_in + p.B * p.D_in + 2 * p.B * Kp + 4 * p.B)]
 
     def config(self):
         p = self.p
@@ -407,7 +443,6 @@ class MxWork(Work):
         self.ws = torch.empty(bsmm.gemm_workspace_size(p.B, p.M, p.N, p.K, self.types[0]), dtype=torch.uint8,
                               device=device)
         self.flops = 2.0 * p.B * p.M * p.N * p.K
-        self.launches_per_step = 3
         self.inputs, self.outputs = [self.a, self.b, self.sa, self.sb], [self.y]
 
     def step(self, events=None):
@@ -441,7 +476,6 @@ class BackwardWork(Work):
         self.ws = torch.empty(bsmm.linear_backward_workspace_size(p.M, p.N, p.K), dtype=torch.uint8,
                               device=device)
         self.flops = 2 * 2.0 * p.M * p.N * p.K
-        self.launches_per_step = 5  # dual quantizer on dY, W^T and X^T quantizers, two GEMMs
         self.inputs, self.outputs = [self.dY, self.W, self.X], [self.dX, self.dW]
 
     def step(self, events=None):
@@ -461,35 +495,14 @@ class BackwardWork(Work):
             off += -(-n // 256) * 256
         return out
 
-    def quantizer_report(self, steps):
-        """The call's quantization phase (the dual dY quantizer and the W^T and
-        X^T quantizers) as the call's time minus that of the same two GEMMs
-        run from the operands it quantized (bsmm_linear_backward_quantized on
-        its workspace); CUDA events on the launching stream."""
+    def quantizer_bytes(self):
+        # bf16 read once, E5M2 codes and UE8M0 scales (one per 32) written
         p = self.p
-        ops = self._quantized_operands()
-        dX, dW = torch.empty_like(self.dX), torch.empty_like(self.dW)
-        gemms = lambda: self.bsmm.linear_backward_quantized(*ops, fp8=p.fp8, scales_are_atoms=True,  # noqa: E731
-                                                           dX=dX, dW=dW)
-        full = lambda: self.step()  # noqa: E731
-        t = {}
-        for name, fn in (("call", full), ("gemms", gemms)):
-            for _ in range(3):
-                fn()
-            a, b = _ev(), _ev()
-            a.record()
-            for _ in range(steps):
-                fn()
-            b.record()
-            torch.cuda.synchronize()
-            t[name] = a.elapsed_time(b) / steps
-        q_ms = t["call"] - t["gemms"]
-        nbytes = (2 * p.M * p.N + 2 * p.M * p.N + 2 * p.M * p.N // 32     # dY read once, codes along both axes
-                  + 2 * p.N * p.K + p.N * p.K + p.N * p.K // 32           # W -> W^T
-                  + 2 * p.M * p.K + p.M * p.K + p.M * p.K // 32)          # X -> X^T
-        return {"quantization phase (dual dY, W^T, X^T)": {
-            "gbs": round(nbytes / (q_ms * 1e-3) / 1e9, 1), "us_per_step": round(1e3 * q_ms, 1),
-            "bytes_per_step": int(nbytes), "how": "call time minus the two GEMMs from its quantized operands"}}
+        M, N, K = p.M, p.N, p.K
+        return [("quant_cols_tma2 dual (dY along N and along M)", "quant_cols_tma2 (dual)",
+                 2 * M * N + 2 * (M * N + M * N // 32)),
+                ("quant_cols_tma2 (W along N -> W^T)", "quant_cols_tma2", 2 * N * K + N * K + N * K // 32),
+                ("quant_cols_tma2 (X along M -> X^T)", "quant_cols_tma2", 2 * M * K + M * K + M * K // 32)]
 
     def config(self):
         p = self.p
@@ -558,8 +571,6 @@ def measure(workload, args, device, rank, world, local, cpu_seconds):
         raise RuntimeError(f"device status {st} (site {site}) after warm-up")
 
     events = []
-    if hasattr(wl, "start_quantizer_timing"):
-        wl.start_quantizer_timing()
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
@@ -636,7 +647,21 @@ def measure(workload, args, device, rank, world, local, cpu_seconds):
                 "peak_source": f"{peak_src}: {peak_how}",
                 "share_of_step": round(dom_ms / elapsed_ms, 4)}
 
-    quant = wl.quantizer_report(args.steps)
+    # per-kernel times from the library's own events, over a few untimed steps
+    trace_steps = 3
+    with bsmm.trace() as launches:
+        for _ in range(trace_steps):
+            wl.step()
+    kernels = {}
+    for name, _, ms in launches:
+        k = kernels.setdefault(name, {"launches": 0, "us": 0.0})
+        k["launches"] += 1
+        k["us"] += 1e3 * ms
+    for k in kernels.values():
+        k["launches"] = k["launches"] // trace_steps
+        k["us"] = round(k["us"] / trace_steps, 2)
+    launches_per_step = len(launches) // trace_steps
+    quant = wl.quantizer_report(launches, trace_steps)
     if quant:
         hbm = load_peaks()[0]["hbm_gbs"]
         for q in quant.values():
@@ -656,7 +681,9 @@ def measure(workload, args, device, rank, world, local, cpu_seconds):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": wl.launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
+        "kernels_per_step": {"how": "bsmm.trace: the library's CUDA events around each of its launches, mean of "
+                                    f"{trace_steps} untimed steps", **kernels},
         "clocks": clocks,
     }
     if quant:

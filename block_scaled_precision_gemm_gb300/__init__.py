@@ -31,7 +31,7 @@ import torch
 __all__ = [
     "BsmmError", "lib", "library_path", "quantize", "gemm", "gemm_noalloc", "gemm_grouped", "int8_channel",
     "linear_backward", "gemm_workspace_size", "int8_channel_workspace_size",
-    "linear_backward_workspace_size", "check_device_status", "selftest_wait_timeout", "selftest_quotient",
+    "linear_backward_workspace_size", "check_device_status", "selftest_wait_timeout", "selftest_quotient", "trace",
     "scale_atoms_size", "quantize_atoms", "gemm_atoms", "linear_backward_quantized",
     "set_wait_timeout_ns", "version",
     "F32", "BF16", "E4M3", "E5M2", "E2M1", "INT8", "SCALE_F32", "SCALE_UE8M0", "SCALE_UE4M3",
@@ -70,6 +70,11 @@ _SIGS = {
     "bsmm_check_device_status": ([_P, ctypes.POINTER(_INT)], _INT),
     "bsmm_selftest_wait_timeout": ([ctypes.c_uint64, _P], _INT),
     "bsmm_selftest_quotient": ([ctypes.c_uint64, ctypes.c_uint64, _P, _P], _INT),
+    "bsmm_trace_start": ([], _INT),
+    "bsmm_trace_stop": ([], _INT),
+    "bsmm_trace_count": ([], _INT),
+    "bsmm_trace_read": ([_INT, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float),
+                         ctypes.POINTER(ctypes.c_float)], _INT),
     "bsmm_quantize": ([_P, _INT, _I64, _I64, _I64, _INT, _INT, _INT, _INT, _INT, _P, _I64, _P, _I64, _P], _INT),
     "bsmm_gemm_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
     "bsmm_gemm": ([_I64, _I64, _I64, _I64, _P, _INT, _P, _INT, _P, _I64, _P, _I64, _INT, _P, _INT, _P, _SZ, _P],
@@ -205,6 +210,27 @@ def selftest_quotient(pairs: int, seed: int = 0, device=None) -> int:
         _check(lib().bsmm_selftest_quotient(int(pairs), int(seed) & (2**64 - 1), _ptr(bad), _stream(None)),
                "bsmm_selftest_quotient")
         return int(bad.item())
+
+
+class trace:
+    """Per-kernel timing of everything the library launches inside the block
+    (bsmm_trace_*): ``with trace() as launches: ...`` leaves in ``launches``
+    one ``(kernel, start_ms, ms)`` per launch, in launch order, start
+    relative to the first launch.  Reading them waits for those kernels."""
+
+    def __enter__(self):
+        self.launches = []
+        _check(lib().bsmm_trace_start(), "bsmm_trace_start")
+        return self.launches
+
+    def __exit__(self, *exc):
+        L = lib()
+        L.bsmm_trace_stop()
+        for i in range(L.bsmm_trace_count()):
+            name, t0, ms = ctypes.c_char_p(), ctypes.c_float(), ctypes.c_float()
+            _check(L.bsmm_trace_read(i, ctypes.byref(name), ctypes.byref(t0), ctypes.byref(ms)), "bsmm_trace_read")
+            self.launches.append((name.value.decode(), t0.value, ms.value))
+        return False
 
 
 def quantize(x: torch.Tensor, block, code="e4m3", scale="f32", transpose=False, codes=None, scales=None,

@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "internal.h"
 
@@ -88,6 +89,55 @@ bool make_tmap_3d(CUtensorMap* tm, const void* base, CUtensorMapDataType dtype, 
                               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// ---- per-kernel timing ------------------------------------------------------
+namespace {
+struct TraceRec {
+  const char* name;
+  int device;
+  cudaEvent_t e0, e1;
+  bool ok;
+};
+std::atomic<bool> g_trace_on{false};
+std::mutex g_trace_mu;
+std::vector<TraceRec> g_trace;
+
+void trace_clear_locked() {
+  for (TraceRec& r : g_trace) {
+    if (r.e0) cudaEventDestroy(r.e0);
+    if (r.e1) cudaEventDestroy(r.e1);
+  }
+  g_trace.clear();
+}
+}  // namespace
+
+bool trace_on() { return g_trace_on.load(std::memory_order_relaxed); }
+
+// Event failures never change what the launch itself returns: the record is
+// kept, marked unusable, and the CUDA error state is cleared.
+int trace_begin(const char* name, cudaStream_t s) {
+  TraceRec r{name, 0, nullptr, nullptr, false};
+  r.ok = cudaGetDevice(&r.device) == cudaSuccess && cudaEventCreate(&r.e0) == cudaSuccess &&
+         cudaEventCreate(&r.e1) == cudaSuccess && cudaEventRecord(r.e0, s) == cudaSuccess;
+  if (!r.ok) cudaGetLastError();
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  g_trace.push_back(r);
+  return static_cast<int>(g_trace.size()) - 1;
+}
+
+void trace_end(int idx, cudaStream_t s) {
+  cudaEvent_t e1 = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (idx < 0 || idx >= static_cast<int>(g_trace.size()) || !g_trace[idx].ok) return;
+    e1 = g_trace[idx].e1;
+  }
+  if (cudaEventRecord(e1, s) != cudaSuccess) {
+    cudaGetLastError();
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (idx < static_cast<int>(g_trace.size())) g_trace[idx].ok = false;
+  }
 }
 
 }  // namespace bsmm
@@ -208,6 +258,52 @@ bsmm_status bsmm_selftest_quotient(uint64_t pairs, uint64_t seed, uint64_t* mism
   return launched(launch_selftest_quotient(pairs, seed, reinterpret_cast<unsigned long long*>(mismatches),
                                            reinterpret_cast<cudaStream_t>(stream)),
                   "selftest launch");
+}
+
+bsmm_status bsmm_trace_start(void) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  trace_clear_locked();
+  g_trace_on.store(true);
+  return BSMM_OK;
+}
+
+bsmm_status bsmm_trace_stop(void) {
+  g_trace_on.store(false);
+  return BSMM_OK;
+}
+
+int bsmm_trace_count(void) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  return static_cast<int>(g_trace.size());
+}
+
+bsmm_status bsmm_trace_read(int i, const char** name, float* start_ms, float* ms) {
+  TraceRec r, first;
+  {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (i < 0 || i >= static_cast<int>(g_trace.size())) return fail(BSMM_ERR_INVALID_ARG, "trace index out of range");
+    r = g_trace[i];
+    first = g_trace[0];
+  }
+  if (name) *name = r.name;
+  if (!r.ok) return fail(BSMM_ERR_CUDA, "this launch's events could not be recorded");
+  int old = 0;
+  cudaError_t e = cudaGetDevice(&old);
+  if (e == cudaSuccess && old != r.device) e = cudaSetDevice(r.device);
+  if (e == cudaSuccess) e = cudaEventSynchronize(r.e1);
+  float t = 0.f, t0 = 0.f;
+  if (e == cudaSuccess && ms) e = cudaEventElapsedTime(&t, r.e0, r.e1);
+  if (e == cudaSuccess && start_ms) {
+    if (first.ok && first.device == r.device)
+      e = cudaEventElapsedTime(&t0, first.e0, r.e0);
+    else
+      t0 = 0.f;
+  }
+  if (old != r.device) cudaSetDevice(old);
+  if (e != cudaSuccess) return cuda_fail(e, "trace event");
+  if (ms) *ms = t;
+  if (start_ms) *start_ms = t0;
+  return BSMM_OK;
 }
 
 bsmm_status bsmm_quantize(const void* x, bsmm_dtype x_type, int64_t rows, int64_t cols, int64_t ld_x,

@@ -166,7 +166,10 @@ cudaError_t launch_mx_gemm_generic(const MxGemmRequest& r, int64_t K_a, int64_t 
   p.y_bf16 = r.y_bf16 ? 1 : 0;
   dim3 grid(static_cast<unsigned>(ceil_div(r.N, GT)), static_cast<unsigned>(ceil_div(r.M, GT)),
             static_cast<unsigned>(r.B));
-  gemm_generic<<<grid, 256, 0, s>>>(p);
+  {
+    TraceScope tr("gemm_generic", s);
+    gemm_generic<<<grid, 256, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

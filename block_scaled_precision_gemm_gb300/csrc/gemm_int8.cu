@@ -304,6 +304,8 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
 // 42 us with four CTAs a strip in one wave, 37 us with eight, 54 with two,
 // 42 with sixteen).
 constexpr int kStrip = 32, kStripSplit = 8, kStripResident = 2;
+constexpr int kStripCG = kStrip / 4;                  // 16-byte column groups per row
+constexpr int kStripRows = 8 * (256 / kStripCG);      // rows per step of 256 threads
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
@@ -313,12 +315,12 @@ template <typename Pad, int RES>
 __global__ void __launch_bounds__(256, RES ? 2 : 4) i8_quant_w_strip(const float* __restrict__ w, int64_t D_in,
                                                                   int64_t D_out, int64_t Kp, int8_t* __restrict__ wq,
                                                                   float* __restrict__ ws, Pad* __restrict__ wqT) {
-  __shared__ float red[8][kStrip];
+  __shared__ float red[8][kStrip];  // [warp][column]
   __shared__ float part_max[kStrip];
   __shared__ float sc[kStrip], yc[kStrip];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int cg = lane & 7;
-  const int rsub = (warp << 2) | (lane >> 3);  // 0..31
+  const int cg = lane % kStripCG;
+  const int rsub = warp * (32 / kStripCG) + lane / kStripCG;  // 8-row group of the step
   const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kStrip;
   const int64_t jc = j0 + 4 * cg;
   const bool col_ok = jc < D_out;  // D_out % 4 == 0: all four in or all out
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(256, RES ? 2 : 4) i8_quant_w_strip(const float
     for (int it = 0; it < RES; ++it)
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int64_t r = rbeg + 256 * it + 8 * rsub + u;
+        const int64_t r = rbeg + kStripRows * it + 8 * rsub + u;
         keep[it][u] = (col_ok && r < dend) ? __ldg(base + r * n4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(256, RES ? 2 : 4) i8_quant_w_strip(const float
         m.w = fmaxf(m.w, fabsf(keep[it][u].w));
       }
   } else if (col_ok) {
-    for (int64_t r0 = rbeg; r0 < dend; r0 += 256) {
+    for (int64_t r0 = rbeg; r0 < dend; r0 += kStripRows) {
       float4 v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -366,13 +368,13 @@ __global__ void __launch_bounds__(256, RES ? 2 : 4) i8_quant_w_strip(const float
     }
   }
 #pragma unroll
-  for (int o = 8; o < 32; o <<= 1) {  // over the lanes holding the same columns
+  for (int o = kStripCG; o < 32; o <<= 1) {  // over the lanes holding the same columns
     m.x = fmaxf(m.x, __shfl_xor_sync(0xffffffffu, m.x, o));
     m.y = fmaxf(m.y, __shfl_xor_sync(0xffffffffu, m.y, o));
     m.z = fmaxf(m.z, __shfl_xor_sync(0xffffffffu, m.z, o));
     m.w = fmaxf(m.w, __shfl_xor_sync(0xffffffffu, m.w, o));
   }
-  if (lane < 8) {
+  if (lane < kStripCG) {
     red[warp][4 * lane + 0] = m.x;
     red[warp][4 * lane + 1] = m.y;
     red[warp][4 * lane + 2] = m.z;
@@ -405,10 +407,10 @@ __global__ void __launch_bounds__(256, RES ? 2 : 4) i8_quant_w_strip(const float
   }
   // pass 2: codes, 256 rows at a time (rend - i0 is a multiple of 8, so a
   // thread's 8 rows are all below rend or all at or above it)
-  const int n_it = RES ? RES : static_cast<int>((rend - rbeg + 255) / 256);
+  const int n_it = RES ? RES : static_cast<int>((rend - rbeg + kStripRows - 1) / kStripRows);
 #pragma unroll
   for (int it = 0; it < n_it; ++it) {
-    const int64_t ir = rbeg + 256 * static_cast<int64_t>(it) + 8 * rsub;
+    const int64_t ir = rbeg + kStripRows * static_cast<int64_t>(it) + 8 * rsub;
     if (ir >= rend) break;
     float4 v[8];
 #pragma unroll
@@ -486,7 +488,7 @@ cudaError_t side_join(int dev, cudaStream_t main) {
 template <typename Pad>
 cudaError_t launch_w_strip(const Int8Request& r, int64_t Kp, Pad* wqT, cudaStream_t s) {
   // up to 512 rows per CTA stay in registers between the two passes
-  const bool resident = Kp / kStripSplit <= 256 * kStripResident;
+  const bool resident = Kp / kStripSplit <= kStripRows * kStripResident;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -499,6 +501,7 @@ cudaError_t launch_w_strip(const Int8Request& r, int64_t Kp, Pad* wqT, cudaStrea
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  TraceScope tr("i8_quant_w_strip", s);
   if (resident)
     return cudaLaunchKernelEx(&cfg, i8_quant_w_strip<Pad, kStripResident>, r.w, static_cast<int64_t>(r.D_in),
                               static_cast<int64_t>(r.D_out), Kp, r.w_q, r.w_scales, wqT);
@@ -677,9 +680,15 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   if (r.B == 0) {  // w alone: column maxima, then codes and scales (no transposed copy)
     const int rows_per_cta = 256;
     dim3 g1(static_cast<unsigned>(ceil_div(r.D_out, 32)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
-    i8_colmax<<<g1, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
+    {
+      TraceScope tr("i8_colmax", s);
+      i8_colmax<<<g1, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
+    }
     dim3 g2(static_cast<unsigned>(ceil_div(r.D_out, 64)), static_cast<unsigned>(Kp / 64));
-    i8_quant_cols<int8_t><<<g2, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales, nullptr);
+    {
+      TraceScope tr("i8_quant_cols", s);
+      i8_quant_cols<int8_t><<<g2, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales, nullptr);
+    }
     return cudaGetLastError();
   }
   // w's quantization beside x's on the side stream (tensor-core path)
@@ -695,19 +704,27 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xpad);
   const unsigned nrows = static_cast<unsigned>(r.B);
   if (tc && rows_vec) {
-    if (r.D_in <= 1024)
+    if (r.D_in <= 1024) {
+      TraceScope tr("i8_quant_rows_reg", s);
       i8_quant_rows_reg<1><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
-    else if (r.D_in <= 2048)
+    } else if (r.D_in <= 2048) {
+      TraceScope tr("i8_quant_rows_reg", s);
       i8_quant_rows_reg<2><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
-    else if (r.D_in <= 4096)
+    } else if (r.D_in <= 4096) {
+      TraceScope tr("i8_quant_rows_reg", s);
       i8_quant_rows_reg<4><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
-    else
+    } else {
+      TraceScope tr("i8_quant_rows_reg", s);
       i8_quant_rows_reg<8><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
-  } else if (tc)
+    }
+  } else if (tc) {
+    TraceScope tr("i8_quant_rows", s);
     i8_quant_rows<__nv_bfloat16><<<nrows, 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales, xb);
-  else
+  } else {
+    TraceScope tr("i8_quant_rows", s);
     i8_quant_rows<int8_t><<<static_cast<unsigned>(r.B), 256, 0, s>>>(r.x, r.D_in, Kp, r.x_q, r.x_scales,
                                                                      reinterpret_cast<int8_t*>(xpad));
+  }
   if (side) {
     e = side_join(ctx->device, s);
     if (e != cudaSuccess) return e;
@@ -717,20 +734,29 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   } else if ((r.D_out % 4) == 0 && (reinterpret_cast<uintptr_t>(r.w) & 15) == 0) {
     const int rows_per_cta = 256;
     dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 128)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
-    i8_colmax4<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
+    {
+      TraceScope tr("i8_colmax4", s);
+      i8_colmax4<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
+    }
   } else {
     const int rows_per_cta = 256;
     dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 32)), static_cast<unsigned>(ceil_div(r.D_in, rows_per_cta)));
-    i8_colmax<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
+    {
+      TraceScope tr("i8_colmax", s);
+      i8_colmax<<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, rows_per_cta, colmax);
+    }
   }
   if (!w_strip) {
     dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, 64)), static_cast<unsigned>(Kp / 64));
-    if (tc)
+    if (tc) {
+      TraceScope tr("i8_quant_cols", s);
       i8_quant_cols<__nv_bfloat16><<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales,
                                                         reinterpret_cast<__nv_bfloat16*>(wpadT));
-    else
+    } else {
+      TraceScope tr("i8_quant_cols", s);
       i8_quant_cols<int8_t><<<grid, 256, 0, s>>>(r.w, r.D_in, r.D_out, Kp, colmax, r.w_q, r.w_scales,
                                                  reinterpret_cast<int8_t*>(wpadT));
+    }
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -744,9 +770,12 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   e = cudaFuncSetAttribute(i8_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(ceil_div(r.D_out, GN)), static_cast<unsigned>(ceil_div(r.B, GM)));
-  i8_gemm<<<grid, 256, smem, s>>>(reinterpret_cast<const int8_t*>(xpad), reinterpret_cast<const int8_t*>(wpadT),
-                                  static_cast<int>(r.B), static_cast<int>(r.D_out), static_cast<int>(Kp), r.x_scales,
-                                  r.w_scales, r.y, r.acc);
+  {
+    TraceScope tr("i8_gemm", s);
+    i8_gemm<<<grid, 256, smem, s>>>(reinterpret_cast<const int8_t*>(xpad), reinterpret_cast<const int8_t*>(wpadT),
+                                    static_cast<int>(r.B), static_cast<int>(r.D_out), static_cast<int>(Kp), r.x_scales,
+                                    r.w_scales, r.y, r.acc);
+  }
   return cudaGetLastError();
 }
 

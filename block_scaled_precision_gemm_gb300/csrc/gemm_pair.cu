@@ -821,7 +821,12 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   }
   const int clusters = std::max(1, std::min(p.num_tiles, max_clusters));
   cfg.gridDim = dim3(2 * clusters);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, tsa, tsb, p);
+  {
+    constexpr const char* kNames[] = {"tc_gemm_pair<F32>", "tc_gemm_pair<MXF8>", "tc_gemm_pair<NVF4>",
+                                      "tc_gemm_pair<I8>", "tc_gemm_pair<MXF4>"};
+    TraceScope tr(kNames[MODE], s);
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, tsa, tsb, p);
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -39,6 +39,11 @@ namespace bsmm {
 namespace {
 
 enum Mode { kF32Scale = 0, kMXF8 = 1, kNVF4 = 2 };
+// Names the trace records give the one-CTA kernel's launches.
+constexpr const char* mode_trace_name(int mode, bool split_k) {
+  return split_k ? "tc_gemm<F32> split-K"
+                 : (mode == kF32Scale ? "tc_gemm<F32>" : (mode == kMXF8 ? "tc_gemm<MXF8>" : "tc_gemm<NVF4>"));
+}
 
 constexpr int BM = 128;          // rows per tile (TMEM lanes)
 constexpr int BK_BYTES = 128;    // K bytes per stage: 128 FP8 or 256 FP4 elements
@@ -670,7 +675,10 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     p.splits = 1;
     p.kpb = p.k_tiles;
     const int grid = std::max(1, std::min(p.num_tiles, ctx->num_sms));
-    kern<<<grid, kThreads, C::SMEM, s>>>(ta, tb, ty, p);
+    {
+      TraceScope tr(mode_trace_name(MODE, false), s);
+      kern<<<grid, kThreads, C::SMEM, s>>>(ta, tb, ty, p);
+    }
     return cudaGetLastError();
   }
   // split K: clusters of `splits` CTAs, one tile per cluster at a time, as
@@ -693,6 +701,7 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CU
   if (e != cudaSuccess) return e;
   const int ncl = std::max(1, std::min(p.num_tiles, fit));
   cfg.gridDim = dim3(static_cast<unsigned>(ncl * p.splits));
+  TraceScope tr(mode_trace_name(MODE, true), s);
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
 }
 
@@ -759,9 +768,12 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
     const int RT = rt_rows(R);
     const int64_t words = r.B * RT * static_cast<int64_t>((ks4 + 7) / 8) * 128;
     const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(words, 256), ctx->num_sms * 16));
-    sf_relayout<<<blocks, 256, 0, s>>>(src, reinterpret_cast<uint32_t*>(dst), static_cast<int>(r.B),
-                                       static_cast<int>(R), KS, RT, ks4, pad, static_cast<int>(KU),
-                                       static_cast<int>(KS / KU));
+    {
+      TraceScope tr("sf_relayout", s);
+      sf_relayout<<<blocks, 256, 0, s>>>(src, reinterpret_cast<uint32_t*>(dst), static_cast<int>(r.B),
+                                         static_cast<int>(R), KS, RT, ks4, pad, static_cast<int>(KU),
+                                         static_cast<int>(KS / KU));
+    }
   };
   if (mf4 || (!want_single && (want_pair ? storable : mx_pair_eligible(r, ctx)))) {
     const int atoms = nv ? 4 : (mf4 ? 2 : 1);
@@ -774,20 +786,26 @@ cudaError_t launch_mx_gemm(const MxGemmRequest& r, cudaStream_t s, std::string* 
     const uint8_t* use_a = sfa;
     const uint8_t* use_b = sfb;
     if (atoms > 1) {
-      sf_relayout_pair<<<ga, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
-                                          static_cast<int>(r.M), KS, RTa, static_cast<int>(k_tiles), atoms, 1, sa, 1,
-                                          0, pad, static_cast<int>(r.K_a), r.sf_atoms ? 1 : static_cast<int>(KS / r.K_a),
-                                          src_rta, ks4);
+      {
+        TraceScope tr("sf_relayout_pair", s);
+        sf_relayout_pair<<<ga, 256, 0, s>>>(r.a_scales, reinterpret_cast<uint32_t*>(sfa), static_cast<int>(r.B),
+                                            static_cast<int>(r.M), KS, RTa, static_cast<int>(k_tiles), atoms, 1, sa,
+                                            1, 0, pad, static_cast<int>(r.K_a),
+                                            r.sf_atoms ? 1 : static_cast<int>(KS / r.K_a), src_rta, ks4);
+      }
     } else if (r.sf_atoms) {  // one atom per K tile: the pair layout is the plain one
       use_a = r.a_scales;
     } else {
       plain_atoms(r.a_scales, sfa, r.M, r.K_a);
     }
     if (pair_b_replicated(atoms)) {
-      sf_relayout_pair<<<gb, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
-                                          static_cast<int>(r.N), KS, RTb / 2, static_cast<int>(k_tiles), atoms, 2, sb,
-                                          0, 1, pad, static_cast<int>(r.K_b), r.sf_atoms ? 1 : static_cast<int>(KS / r.K_b),
-                                          src_rtb, ks4);
+      {
+        TraceScope tr("sf_relayout_pair", s);
+        sf_relayout_pair<<<gb, 256, 0, s>>>(r.b_scales, reinterpret_cast<uint32_t*>(sfb), static_cast<int>(r.B),
+                                            static_cast<int>(r.N), KS, RTb / 2, static_cast<int>(k_tiles), atoms, 2,
+                                            sb, 0, 1, pad, static_cast<int>(r.K_b),
+                                            r.sf_atoms ? 1 : static_cast<int>(KS / r.K_b), src_rtb, ks4);
+      }
     } else if (r.sf_atoms) {
       use_b = r.b_scales;
     } else {
@@ -949,7 +967,10 @@ cudaError_t launch_mx_gemm_noalloc(const MxGemmRequest& r, cudaStream_t s, std::
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t s) {
   const DeviceCtx* ctx = device_ctx();
   if (!ctx) return cudaErrorInitializationError;
-  selftest_wait_kernel<<<1, 32, 0, s>>>(timeout_ns, ctx->status);
+  {
+    TraceScope tr("selftest_wait", s);
+    selftest_wait_kernel<<<1, 32, 0, s>>>(timeout_ns, ctx->status);
+  }
   return cudaGetLastError();
 }
 

@@ -16,6 +16,27 @@ void set_error(const std::string& msg);
 bsmm_status fail(bsmm_status st, const std::string& msg);
 bsmm_status cuda_fail(cudaError_t e, const char* what);
 
+// ---- per-kernel timing (bsmm_trace_*) -------------------------------------
+// While tracing is on, every launch of the library's kernels records a CUDA
+// event on its stream before and after itself.  A TraceScope placed just
+// before a launch statement does both (the second in its destructor, after
+// the launch); when tracing is off it costs one relaxed atomic load.
+bool trace_on();
+int trace_begin(const char* name, cudaStream_t s);  // record index, or -1
+void trace_end(int idx, cudaStream_t s);
+struct TraceScope {
+  TraceScope(const char* name, cudaStream_t s) : s_(s), idx_(trace_on() ? trace_begin(name, s) : -1) {}
+  ~TraceScope() {
+    if (idx_ >= 0) trace_end(idx_, s_);
+  }
+  TraceScope(const TraceScope&) = delete;
+  TraceScope& operator=(const TraceScope&) = delete;
+
+ private:
+  cudaStream_t s_;
+  int idx_;
+};
+
 // ---- per-device context ---------------------------------------------------
 struct DeviceCtx {
   int device = -1;

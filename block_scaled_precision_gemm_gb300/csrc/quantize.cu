@@ -952,8 +952,11 @@ cudaError_t launch_cols_tma2_code(const QP& p, const DeviceCtx* ctx, cudaStream_
       cudaFuncSetAttribute(quant_cols_tma2<POW2, DUAL, CODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 2);
-  quant_cols_tma2<POW2, DUAL, CODE><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
-      tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns(), p2);
+  {
+    TraceScope tr(DUAL ? "quant_cols_tma2 (dual)" : "quant_cols_tma2", s);
+    quant_cols_tma2<POW2, DUAL, CODE><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
+        tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns(), p2);
+  }
   return cudaGetLastError();
 }
 
@@ -976,8 +979,11 @@ cudaError_t launch_cols_tma(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(quant_cols_tma<POW2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 3);
-  quant_cols_tma<POW2><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
-      tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns());
+  {
+    TraceScope tr("quant_cols_tma", s);
+    quant_cols_tma<POW2><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
+        tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns());
+  }
   return cudaGetLastError();
 }
 
@@ -996,23 +1002,41 @@ cudaError_t dispatch(const QP& p, const DeviceCtx* ctx, cudaStream_t s) {
   if (p.br == 1 && pow2_small && !p.transpose && x_vec && codes16) {
     int64_t blocks = ceil_div(p.rows * (p.cols / kSlice), 256 * 2);
     blocks = std::min<int64_t>(blocks, static_cast<int64_t>(ctx->num_sms) * 8);
-    quant_rows<In, POW2><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(p);
+    {
+      TraceScope tr("quant_rows", s);
+      quant_rows<In, POW2><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(p);
+    }
   } else if (p.bc == 1 && pow2_small_r && (!p.transpose || (codes16 && p.ld_codes % 32 == 0))) {
     const int tiles_c = static_cast<int>(ceil_div(p.cols, kColTileC));
     const int64_t n_tiles = static_cast<int64_t>(tiles_c) * ceil_div(p.rows, kColTileR);
     const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 3);
-    quant_cols<In, POW2><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, 0, s>>>(p, x_vec ? 1 : 0, tiles_c,
-                                                                                      n_tiles);
+    {
+      TraceScope tr("quant_cols", s);
+      quant_cols<In, POW2><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, 0, s>>>(p, x_vec ? 1 : 0, tiles_c,
+                                                                                        n_tiles);
+    }
   } else if (p.br == 128 && p.bc == 128 && !p.transpose && x_vec && codes16) {
     dim3 grid(static_cast<unsigned>(p.cols / 128), static_cast<unsigned>(p.rows / 128));
-    quant_tile<In, POW2><<<grid, 512, 0, s>>>(p);
+    {
+      TraceScope tr("quant_tile", s);
+      quant_tile<In, POW2><<<grid, 512, 0, s>>>(p);
+    }
   } else if (p.br == 1 && p.bc == p.cols && !p.transpose) {
-    quant_wrow<In, POW2><<<static_cast<unsigned>(p.rows), 256, 0, s>>>(p);
+    {
+      TraceScope tr("quant_wrow", s);
+      quant_wrow<In, POW2><<<static_cast<unsigned>(p.rows), 256, 0, s>>>(p);
+    }
   } else if (p.bc == 1 && p.br == p.rows) {
-    quant_wcol<In, POW2><<<static_cast<unsigned>(ceil_div(p.cols, 32)), 256, 0, s>>>(p);
+    {
+      TraceScope tr("quant_wcol", s);
+      quant_wcol<In, POW2><<<static_cast<unsigned>(ceil_div(p.cols, 32)), 256, 0, s>>>(p);
+    }
   } else {
     const int64_t nblk = (p.rows / p.br) * (p.cols / p.bc);
-    quant_any<In, POW2><<<static_cast<unsigned>(ceil_div(nblk, 256)), 256, 0, s>>>(p);
+    {
+      TraceScope tr("quant_any", s);
+      quant_any<In, POW2><<<static_cast<unsigned>(ceil_div(nblk, 256)), 256, 0, s>>>(p);
+    }
   }
   return cudaGetLastError();
 }
@@ -1122,7 +1146,10 @@ cudaError_t launch_selftest_quotient(uint64_t pairs, uint64_t seed, unsigned lon
   if (!ctx) return cudaErrorInitializationError;
   const uint64_t want = (pairs + 255) / 256;
   const unsigned grid = static_cast<unsigned>(std::max<uint64_t>(1, std::min<uint64_t>(want, 8ull * ctx->num_sms)));
-  selftest_quotient_kernel<<<grid, 256, 0, s>>>(pairs, seed, bad);
+  {
+    TraceScope tr("selftest_quotient", s);
+    selftest_quotient_kernel<<<grid, 256, 0, s>>>(pairs, seed, bad);
+  }
   return cudaGetLastError();
 }
 

@@ -118,6 +118,25 @@ bsmm_status bsmm_selftest_wait_timeout(uint64_t timeout_ns, bsmm_stream_t stream
  * `stream`; BSMM_ERR_INVALID_ARG if `mismatches` is NULL. */
 bsmm_status bsmm_selftest_quotient(uint64_t pairs, uint64_t seed, uint64_t* mismatches, bsmm_stream_t stream);
 
+/* Per-kernel timing, with no counterpart on the pages (measurement aid).
+ * bsmm_trace_start() discards earlier records and turns recording on: from
+ * then on every launch of this library's kernels, from any host thread,
+ * records a CUDA event before and after itself on its own stream.
+ * bsmm_trace_stop() turns recording off; records stay readable until the
+ * next start.  bsmm_trace_count() is the number of launches recorded.
+ * bsmm_trace_read(i, ...) waits for launch i to finish and gives the
+ * kernel's name (a static string, or NULL pointers skipped), its start
+ * relative to launch 0's start in milliseconds (0 when launch 0 ran on
+ * another device), and its duration in milliseconds.  The events add a few
+ * microseconds of host time to each launch and small gaps between kernels;
+ * do not trace inside stream capture.  bsmm_trace_read returns
+ * BSMM_ERR_INVALID_ARG for an index out of range and BSMM_ERR_CUDA when that
+ * launch's events could not be recorded or read. */
+bsmm_status bsmm_trace_start(void);
+bsmm_status bsmm_trace_stop(void);
+int bsmm_trace_count(void);
+bsmm_status bsmm_trace_read(int i, const char** name, float* start_ms, float* ms);
+
 /* ------------------------------------------------------------------------ */
 /* Quantizer                                                                */
 /* ------------------------------------------------------------------------ */
