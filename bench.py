@@ -189,7 +189,8 @@ class Work:
     def quantizer_bytes(self):
         """[(label, kernel name, algorithmic bytes per launch)] for the step's
         quantizer launches, in launch order (a name that repeats is matched
-        in turn); empty where the step has none."""
+        in turn; a trailing * matches any kernel with that prefix); empty
+        where the step has none."""
         return []
 
     def quantizer_report(self, launches, steps):
@@ -207,10 +208,11 @@ class Work:
             used = [False] * len(mine)
             t_lo, t_hi, nbytes = None, None, 0
             for label, kname, nb in want:
-                i = next(i for i, (n, _, _) in enumerate(mine) if n == kname and not used[i])
+                i = next(i for i, (n, _, _) in enumerate(mine)
+                         if not used[i] and (n == kname or (kname.endswith("*") and n.startswith(kname[:-1]))))
                 used[i] = True
-                _, t0, ms = mine[i]
-                e = out.setdefault(label, {"kernel": kname, "ms": 0.0, "bytes": 0})
+                n, t0, ms = mine[i]
+                e = out.setdefault(label, {"kernel": n, "ms": 0.0, "bytes": 0})
                 e["ms"] += ms
                 e["bytes"] += nb
                 t_lo = t0 if t_lo is None else min(t_lo, t0)
@@ -391,7 +393,7 @@ class Int8Work(Work):
         # float32 read, int8 codes, the matmul's zero-padded bf16 copy, FP32 scales
         p = self.p
         Kp = -(-p.D_in // 128) * 128
-        return [("i8_quant_w_strip (w per column, second stream)", "i8_quant_w_strip",
+        return [("w per column (second stream)", "i8_quant_w_*",
                  4 * p.D_in * p.D_out + p.D_in * p.D_out + 2 * p.D_out * Kp + 4 * p.D_out),
                 ("i8_quant_rows_reg (x per row)", "i8_quant_rows_reg", 4 * p.B * p.D_in + p.B * p.D_in + 2 * p.B * Kp + 4 * p.B)]
 

@@ -82,6 +82,15 @@ __device__ __forceinline__ __nv_bfloat16 pad_code<__nv_bfloat16>(int8_t q) {
   return __int2bfloat16_rn(q);  // exact: |q| <= 127 < 2^8
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Pad is int8_t (fallback matmul) or __nv_bfloat16 (tensor-core matmul).
 template <typename Pad>
 __global__ void __launch_bounds__(256) i8_quant_rows(const float* __restrict__ x, int64_t D, int64_t Kp,
@@ -513,14 +522,6 @@ cudaError_t launch_w_strip(const Int8Request& r, int64_t Kp, Pad* wqT, cudaStrea
 constexpr int GM = 128, GN = 128, GK = 128, GSTAGES = 4;
 constexpr int G_STAGE_BYTES = (GM + GN) * GK;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)

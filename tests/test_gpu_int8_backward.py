@@ -88,6 +88,20 @@ def test_int8_each_kernel(monkeypatch, kernel, B, D_in, D_out):
     run_int8(x, w)
 
 
+@pytest.mark.parametrize("B,D_in,D_out", [(64, 4096, 4096), (100, 300, 72), (7, 1000, 4100), (130, 3968, 36),
+                                          (1, 64, 4), (33, 2048, 1028)])
+def test_int8_w_quantizer_shapes(B, D_in, D_out):
+    """w's per-column quantizer (rows held in registers for D_in <= 4096)
+    over many strips (D_out 4096 and 4100), a partial last strip (D_out not
+    a multiple of 32), column scales spread over e^[-4, 4] and a zero
+    column."""
+    g = torch.Generator().manual_seed(B + 3 * D_in + D_out)
+    x = torch.randn(B, D_in, generator=g).numpy()
+    w = (torch.randn(D_in, D_out, generator=g) * torch.exp(torch.empty(1, D_out).uniform_(-4, 4, generator=g))).numpy()
+    w[:, D_out // 3] = 0
+    run_int8(x, w)
+
+
 @pytest.mark.parametrize("D_in", [4096, 4096 + 1000])
 def test_int8_extreme_sums_tensor_core_path(D_in):
     """Codes all +-127 on the tensor-core path: every 1024-product chunk sums
