@@ -190,8 +190,14 @@ class Work:
         """[(label, kernel name, algorithmic bytes per launch)] for the step's
         quantizer launches, in launch order (a name that repeats is matched
         in turn; a trailing * matches any kernel with that prefix); empty
-        where the step has none."""
+        where the step has none.  A list of such lists gives alternatives
+        (the library picks kernels by shape and alignment): the first whose
+        kernels all ran is used."""
         return []
+
+    @staticmethod
+    def _matches(n, kname):
+        return n == kname or (kname.endswith("*") and n.startswith(kname[:-1]))
 
     def quantizer_report(self, launches, steps):
         """Per-kernel HBM throughput of the step's quantizers from the
@@ -201,15 +207,17 @@ class Work:
         want = self.quantizer_bytes()
         if not want:
             return None
-        out, spans = {}, []
         per_step = len(launches) // steps
+        if isinstance(want[0], list):  # alternatives
+            first = [n for n, _, _ in launches[:per_step]]
+            want = next(alt for alt in want if all(any(self._matches(n, k) for n in first) for _, k, _ in alt))
+        out, spans = {}, []
         for st in range(steps):
             mine = launches[st * per_step:(st + 1) * per_step]
             used = [False] * len(mine)
             t_lo, t_hi, nbytes = None, None, 0
             for label, kname, nb in want:
-                i = next(i for i, (n, _, _) in enumerate(mine)
-                         if not used[i] and (n == kname or (kname.endswith("*") and n.startswith(kname[:-1]))))
+                i = next(i for i, (n, _, _) in enumerate(mine) if not used[i] and self._matches(n, kname))
                 used[i] = True
                 n, t0, ms = mine[i]
                 e = out.setdefault(label, {"kernel": n, "ms": 0.0, "bytes": 0})
@@ -393,9 +401,9 @@ class Int8Work(Work):
         # float32 read, int8 codes, the matmul's zero-padded bf16 copy, FP32 scales
         p = self.p
         Kp = -(-p.D_in // 128) * 128
-        return [("w per column (second stream)", "i8_quant_w_*",
-                 4 * p.D_in * p.D_out + p.D_in * p.D_out + 2 * p.D_out * Kp + 4 * p.D_out),
-                ("i8_quant_rows_reg (x per row)", "i8_quant_rows_reg", 4 * p.B * p.D_in + p.B * p.D_in + 2 * p.B * Kp + 4 * p.B)]
+        w_bytes = 4 * p.D_in * p.D_out + p.D_in * p.D_out + 2 * p.D_out * Kp + 4 * p.D_out
+        x_bytes = 4 * p.B * p.D_in + p.B * p.D_in + 2 * p.B * Kp + 4 * p.B
+        return [("w per column (second stream)", "i8_quant_w_*", w_bytes), ("x per row", "i8_quant_rows*", x_bytes)]
 
     def config(self):
         p = self.p

@@ -308,10 +308,10 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
 // bytes a row per strip) and into wqT [D_out, Kp], where a thread's 8 codes
 // of one column are 8 consecutive elements of a row (zero codes for rows
 // >= D_in).  Needs D_out % 4 == 0, w 16-byte and w_q 4-byte aligned.
-// Eight CTAs a strip give 1.7 waves of CTAs at 4 per SM: the second wave's
-// DRAM pass overlaps the first wave's second pass (measured at D = 4096:
-// 42 us with four CTAs a strip in one wave, 37 us with eight, 54 with two,
-// 42 with sixteen).
+// At D = 4096 the eight CTAs a strip make 1024 CTAs, two per SM (3.4
+// waves).  Measured there (one launch, cold): 37 us with the rows held in
+// registers and 37 streamed twice, 35 with sixteen CTAs a strip, 45 with
+// 64-column strips; strip width and split are compile-time constants.
 constexpr int kStrip = 32, kStripSplit = 8, kStripResident = 2;
 constexpr int kStripCG = kStrip / 4;                  // 16-byte column groups per row
 constexpr int kStripRows = 8 * (256 / kStripCG);      // rows per step of 256 threads
