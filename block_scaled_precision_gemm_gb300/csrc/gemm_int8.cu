@@ -315,11 +315,6 @@ __global__ void __launch_bounds__(256) i8_quant_cols(const float* __restrict__ w
 constexpr int kStrip = 32, kStripSplit = 8, kStripResident = 2;
 constexpr int kStripCG = kStrip / 4;                  // 16-byte column groups per row
 constexpr int kStripRows = 8 * (256 / kStripCG);      // rows per step of 256 threads
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
 template <typename Pad, int RES>
 __global__ void __launch_bounds__(256, RES ? 2 : 4) i8_quant_w_strip(const float* __restrict__ w, int64_t D_in,
                                                                   int64_t D_out, int64_t Kp, int8_t* __restrict__ wq,

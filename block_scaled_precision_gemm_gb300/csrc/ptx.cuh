@@ -254,6 +254,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 // Arrive on an mbarrier given by its cluster-window address (possibly remote),
 // relaxed.  Used only to hand a tensor-memory buffer or a filled stage back
 // after tcgen05.wait::ld (or the TMA issue) has returned, so nothing that the
