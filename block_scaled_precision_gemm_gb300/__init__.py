@@ -223,9 +223,11 @@ class trace:
         _check(lib().bsmm_trace_start(), "bsmm_trace_start")
         return self.launches
 
-    def __exit__(self, *exc):
+    def __exit__(self, exc_type, exc, tb):
         L = lib()
         L.bsmm_trace_stop()
+        if exc_type is not None:  # leave the records unread; the block's exception propagates
+            return False
         for i in range(L.bsmm_trace_count()):
             name, t0, ms = ctypes.c_char_p(), ctypes.c_float(), ctypes.c_float()
             _check(L.bsmm_trace_read(i, ctypes.byref(name), ctypes.byref(t0), ctypes.byref(ms)), "bsmm_trace_read")
