@@ -151,8 +151,10 @@ bsmm_status bsmm_trace_read(int i, const char** name, float* start_ms, float* ms
  * [-127,127]; zero block -> 1), UE4M3 scale = E4M3(absmax/qmax) rounded to
  * nearest (zero block -> 1, a scale rounding to 0 -> 2^-9).  qmax is the
  * code format's largest value: E4M3 448, E5M2 57344, E2M1 6, INT8 127.
- * All arithmetic is binary32 with IEEE division (x/scale, never x*(1/scale));
- * rounding is to nearest, ties to even; floating codes saturate.
+ * All arithmetic is binary32; each code comes from the correctly rounded
+ * quotient x/scale, as IEEE division gives it (not x*(1/scale) rounded
+ * twice; see bsmm_selftest_quotient for how it is computed); rounding is to
+ * nearest, ties to even; floating codes saturate.
  * Inputs are taken to be finite: the pages give no rule for NaN or
  * infinity, the library does not look for them, and a block holding one gets
  * unspecified codes and scale.
