@@ -170,3 +170,18 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
         b.gemm_workspace_size(1, 128, 128, 128, "e4m3")
     with pytest.raises(RuntimeError, match="is missing"):
         b.version()
+
+
+def test_trace_and_selftest_argument_checks_without_gpu(lib):
+    """The trace store is host state: start clears it, an empty trace reads
+    as out of range, stop leaves it; the quotient self-test refuses a NULL
+    counter before any launch."""
+    import block_scaled_precision_gemm_gb300 as b
+    assert lib.bsmm_trace_start() == b.OK
+    assert lib.bsmm_trace_count() == 0
+    name, t0, ms = ctypes.c_char_p(), ctypes.c_float(), ctypes.c_float()
+    assert lib.bsmm_trace_read(0, ctypes.byref(name), ctypes.byref(t0), ctypes.byref(ms)) == b.ERR_INVALID_ARG
+    assert lib.bsmm_trace_read(-1, None, None, None) == b.ERR_INVALID_ARG
+    assert lib.bsmm_trace_stop() == b.OK
+    assert lib.bsmm_trace_count() == 0
+    assert lib.bsmm_selftest_quotient(16, 1, None, None) == b.ERR_INVALID_ARG
