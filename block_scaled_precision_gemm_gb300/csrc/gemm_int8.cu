@@ -641,11 +641,19 @@ __global__ void __launch_bounds__(256) i8_gemm(const int8_t* __restrict__ A, con
 
 }  // namespace
 
+// The split matmul's counters (kSplitTilesMax x 32) and int32 partial tiles.
+constexpr size_t kSplitCntBytes = static_cast<size_t>(kSplitTilesMax) * 32 * 4;
+size_t int8_split_bytes(int64_t B, int64_t D_out) {
+  const int64_t tiles = ceil_div(B, 256) * ceil_div(D_out, 256);
+  return kSplitCntBytes + static_cast<size_t>(int8_split_units(tiles)) * 256 * 256 * 4;
+}
+
 size_t int8_workspace_bytes(int64_t B, int64_t D_in, int64_t D_out) {
-  // room for the bf16 operand copies (the fallback's int8 copies fit inside)
+  // room for the bf16 operand copies (the fallback's int8 copies fit
+  // inside), then the split matmul's counters and partial sums
   const int64_t Kp = ceil_div(D_in, kKpAlign) * kKpAlign;
   return align_up(static_cast<size_t>(D_out) * 4, 256) + align_up(static_cast<size_t>(B) * Kp * 2, 256) +
-         align_up(static_cast<size_t>(D_out) * Kp * 2, 256);
+         align_up(static_cast<size_t>(D_out) * Kp * 2, 256) + int8_split_bytes(B, D_out);
 }
 
 cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
@@ -656,6 +664,7 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   unsigned* colmax = reinterpret_cast<unsigned*>(ws);
   uint8_t* xpad = ws + align_up(static_cast<size_t>(r.D_out) * 4, 256);
   uint8_t* wpadT = xpad + align_up(static_cast<size_t>(r.B) * Kp * 2, 256);
+  uint8_t* split = wpadT + align_up(static_cast<size_t>(r.D_out) * Kp * 2, 256);  // B > 0 only
   // The tensor-core path stores y (and the int32 sums) through TMA: 16-byte
   // rows and bases.  BSMM_INT8_KERNEL=mma forces the fallback.
   const char* force = std::getenv("BSMM_INT8_KERNEL");
@@ -699,6 +708,10 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
                         (reinterpret_cast<uintptr_t>(r.x_q) & 3) == 0 && r.D_in <= 8192;
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xpad);
   const unsigned nrows = static_cast<unsigned>(r.B);
+  if (tc) {  // the split matmul's counters start from zero
+    e = cudaMemsetAsync(split, 0, kSplitCntBytes, s);
+    if (e != cudaSuccess) return e;
+  }
   if (tc && rows_vec) {
     if (r.D_in <= 1024) {
       TraceScope tr("i8_quant_rows_reg", s);
@@ -758,7 +771,11 @@ cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (tc) {
     std::string why;
-    e = launch_int8_gemm_pair(r, xpad, wpadT, Kp, s, &why);
+    // BSMM_INT8_SPLIT=0 keeps every tile whole
+    const char* no_split = std::getenv("BSMM_INT8_SPLIT");
+    const bool split_ok = !(no_split && std::strcmp(no_split, "0") == 0);
+    e = launch_int8_gemm_pair(r, xpad, wpadT, Kp, split_ok ? reinterpret_cast<int32_t*>(split + kSplitCntBytes) : nullptr,
+                              split_ok ? reinterpret_cast<unsigned*>(split) : nullptr, s, &why);
     if (e != cudaSuccess && !why.empty()) set_error(why);
     return e;
   }

@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <atomic>
 #include <cstring>
 
@@ -135,6 +136,23 @@ struct PairParams {
   uint64_t timeout_ns;
 };
 
+// kPairI8's work units: first each tile from whole_tiles on as `split` K
+// ranges of k_split K blocks, then tiles [0, whole_tiles) whole (num_units
+// in all).  The parts come first so that the extra work of each part's end
+// overlaps a whole tile's MMAs in the other TMEM buffer.  A part leaves its
+// int32 sums in split_ws [tile - whole_tiles][part][32 warp slots][2048] and
+// counts itself in split_cnt [tile - whole_tiles][32 warp slots]; the last
+// part of a warp slot adds the others' sums and writes y.  (The other modes
+// keep the plain parameters: a larger parameter block made the FP32-scale
+// epilogue spill.)
+struct PairSplitParams : PairParams {
+  int32_t* split_ws;
+  unsigned* split_cnt;
+  int whole_tiles, split, k_split, num_units;
+};
+template <int MODE>
+using PairArgs = std::conditional_t<MODE == kPairI8, PairSplitParams, PairParams>;
+
 __device__ __forceinline__ void decode_pair_tile(const PairParams& p, int t, int& b, int& mb, int& nb) {
   const int per_batch = p.m_tiles * p.n_tiles;
   b = t / per_batch;
@@ -145,6 +163,30 @@ __device__ __forceinline__ void decode_pair_tile(const PairParams& p, int t, int
   const int rows = min(GROUP_M, p.m_tiles - g * GROUP_M);
   mb = g * GROUP_M + within % rows;
   nb = within / rows;
+}
+
+// Work unit u: tile t, K blocks [k0, k1), and the part's index (-1: whole tile).
+struct PairUnit {
+  int t, k0, k1, part;
+};
+// Only kPairI8 splits; the other modes' units are their tiles.
+template <int MODE>
+__device__ __forceinline__ PairUnit pair_unit(const PairArgs<MODE>& p, int u) {
+  if constexpr (MODE == kPairI8) {
+    const int parts = p.num_units - p.whole_tiles;
+    if (u < parts) {
+      const int part = u % p.split;
+      const int k0 = part * p.k_split;
+      return {p.whole_tiles + u / p.split, k0, min(p.k_tiles, k0 + p.k_split), part};
+    }
+    return {u - parts, 0, p.k_tiles, -1};
+  }
+  return {u, 0, p.k_tiles, -1};
+}
+template <int MODE>
+__device__ __forceinline__ int pair_units(const PairArgs<MODE>& p) {
+  if constexpr (MODE == kPairI8) return p.num_units;
+  return p.num_tiles;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2_pair(float lo, float hi) {
@@ -186,7 +228,7 @@ template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmSFA,
-                 const __grid_constant__ CUtensorMap tmSFB, const PairParams p) {
+                 const __grid_constant__ CUtensorMap tmSFB, const PairArgs<MODE> p) {
   using C = PCfg<MODE>;
   constexpr int STAGES = C::STAGES;
   constexpr int NACC = C::NACC;
@@ -249,10 +291,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
-      for (int t = cid; ok && t < p.num_tiles; t += ncl) {
+      for (int u = cid; ok && u < pair_units<MODE>(p); u += ncl) {
+        const PairUnit w = pair_unit<MODE>(p, u);
         int b, mb, nb;
-        decode_pair_tile(p, t, b, mb, nb);
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        decode_pair_tile(p, w.t, b, mb, nb);
+        for (int kt = w.k0; kt < w.k1; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteProducer)) {
             ok = false;
             break;
@@ -392,15 +435,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         int stage = 0, tb = 0;
         uint32_t phase = 0, tph = 0;
         bool ok = true;
-        for (int t = cid; ok && t < p.num_tiles; t += ncl) {
-          for (int k0 = 0; ok && k0 < p.k_tiles; k0 += p.chunk) {
+        for (int u = cid; ok && u < pair_units<MODE>(p); u += ncl) {
+          const PairUnit w = pair_unit<MODE>(p, u);
+          for (int k0 = w.k0; ok && k0 < w.k1; k0 += p.chunk) {
             if (!mbar_wait(&tempty[tb], tph ^ 1u, p.timeout_ns, abort_flag, p.status, kSiteMmaTmem)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t d = tmem + static_cast<uint32_t>(tb * PN);
-            const int k1 = k0 + p.chunk < p.k_tiles ? k0 + p.chunk : p.k_tiles;
+            const int k1 = k0 + p.chunk < w.k1 ? k0 + p.chunk : w.k1;
             for (int kt = k0; kt < k1; ++kt) {
               if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status, kSiteMmaFull)) {
                 ok = false;
@@ -566,9 +610,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int tb = 0;
     uint32_t tph = 0;
-    for (int t = cid; t < p.num_tiles; t += ncl) {
+    for (int u = cid; u < pair_units<MODE>(p); u += ncl) {
+      const PairUnit w = pair_unit<MODE>(p, u);
       int b, mb, nb;
-      decode_pair_tile(p, t, b, mb, nb);
+      decode_pair_tile(p, w.t, b, mb, nb);
       const int row0 = mb * PM + static_cast<int>(rank) * HALF + q * 32;
       const int row = row0 + lane;
       const int col0 = nb * PN + g * COLS;
@@ -649,7 +694,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // exact integer below 2^24, converted exactly and added
 #pragma unroll
         for (int i = 0; i < COLS / 2; ++i) acc[i] = make_float2(0.f, 0.f);  // int 0 has the same bits
-        for (int kt = 0; kt < p.k_tiles; kt += p.chunk) {
+        for (int kt = w.k0; kt < w.k1; kt += p.chunk) {
           if (!mbar_wait(&tfull[tb], tph, p.timeout_ns, abort_flag, p.status, kSiteEpilogue)) {
             ok = false;
             break;
@@ -758,6 +803,42 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (row0 >= p.M || !col_ok) continue;  // this warp's box lies outside y
       if constexpr (MODE == kPairI8) {
+        const PairUnit wu = pair_unit<MODE>(p, u);  // recomputed: not live across the K loop
+        if (wu.part >= 0) {
+          // One K range of a split tile: this warp's 32 x 64 int32 sums go
+          // to the part's slot; the part that counts last for this warp slot
+          // adds the other parts' sums (integer adds: any order is exact)
+          // and writes y.  No part waits for another.  A warp slot's 8 KB
+          // hold 16-byte unit i of lane l at (32 i + l), so that every store
+          // and load instruction moves 512 contiguous bytes.
+          const int tail = wu.t - p.whole_tiles;
+          const int slot = static_cast<int>(rank) * EPI_WARPS + ew;
+          int32_t* slot_ws = p.split_ws + static_cast<size_t>(tail) * p.split * (PM * PN) + slot * (32 * COLS);
+          int4* mine = reinterpret_cast<int4*>(slot_ws + static_cast<size_t>(wu.part) * (PM * PN)) + lane;
+#pragma unroll
+          for (int i = 0; i < COLS / 4; ++i)
+            mine[32 * i] = make_int4(__float_as_int(acc[2 * i].x), __float_as_int(acc[2 * i].y),
+                                     __float_as_int(acc[2 * i + 1].x), __float_as_int(acc[2 * i + 1].y));
+          __threadfence();
+          __syncwarp();
+          unsigned before = 0;
+          if (lane == 0) before = atomicAdd(p.split_cnt + tail * (2 * EPI_WARPS) + slot, 1u);
+          before = __shfl_sync(0xffffffffu, before, 0);
+          if (before != static_cast<unsigned>(p.split - 1)) continue;
+          __threadfence();
+          for (int o = 0; o < p.split; ++o) {
+            if (o == wu.part) continue;
+            const int4* other = reinterpret_cast<const int4*>(slot_ws + static_cast<size_t>(o) * (PM * PN)) + lane;
+#pragma unroll
+            for (int i = 0; i < COLS / 4; ++i) {
+              const int4 v = __ldcg(other + 32 * i);
+              acc[2 * i] = make_float2(__int_as_float(__float_as_int(acc[2 * i].x) + v.x),
+                                       __int_as_float(__float_as_int(acc[2 * i].y) + v.y));
+              acc[2 * i + 1] = make_float2(__int_as_float(__float_as_int(acc[2 * i + 1].x) + v.z),
+                                           __int_as_float(__float_as_int(acc[2 * i + 1].y) + v.w));
+            }
+          }
+        }
         if (p.store_acc) store_box_f32(&tmSFA, my_stg, acc, col0, row0, b, lane);  // int32 bits as they are
         // y = (float(acc) * s_x[row]) * s_w[col], in that order
         const float sxr = row < p.M ? __ldg(p.sx + row) : 0.f;
@@ -794,7 +875,7 @@ std::atomic<int> g_pair_clusters[5][64] = {};
 
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const CUtensorMap& tsa,
-                        const CUtensorMap& tsb, const PairParams& p, const DeviceCtx* ctx, cudaStream_t s,
+                        const CUtensorMap& tsb, const PairArgs<MODE>& p, const DeviceCtx* ctx, cudaStream_t s,
                         std::string* why) {
   using C = PCfg<MODE>;
   auto kern = tc_gemm_pair<MODE>;
@@ -839,13 +920,40 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     max_clusters = n;
     g_pair_clusters[MODE][ctx->device].store(n, std::memory_order_relaxed);
   }
-  const int clusters = std::max(1, std::min(p.num_tiles, max_clusters));
+  PairArgs<MODE> q = p;
+  int units = q.num_tiles;
+  if constexpr (MODE == kPairI8) {
+    q.whole_tiles = q.num_units = q.num_tiles;
+    q.split = 1;
+    q.k_split = q.k_tiles;
+    if (q.split_ws && q.split_cnt) {
+      // The last wave's tiles (all of them when there are fewer tiles than
+      // clusters) split their K blocks over the clusters that would idle:
+      // S = clusters / tail parts, at most kSplitMax, each a whole number of
+      // exact chunks where K allows.
+      const int tail = q.num_tiles % max_clusters;
+      int split = tail > 0 ? std::min(kSplitMax, max_clusters / tail) : 1;
+      if (split >= 2) {
+        int k_split = static_cast<int>(ceil_div(q.k_tiles, split));
+        if (k_split > q.chunk) k_split = static_cast<int>(ceil_div(k_split, q.chunk)) * q.chunk;
+        split = static_cast<int>(ceil_div(q.k_tiles, k_split));
+        if (split >= 2 && tail <= kSplitTilesMax && tail * split <= kSplitUnitsMax) {
+          q.whole_tiles = q.num_tiles - tail;
+          q.split = split;
+          q.k_split = k_split;
+          q.num_units = q.whole_tiles + tail * split;
+        }
+      }
+    }
+    units = q.num_units;
+  }
+  const int clusters = std::max(1, std::min(units, max_clusters));
   cfg.gridDim = dim3(2 * clusters);
   {
     constexpr const char* kNames[] = {"tc_gemm_pair<F32>", "tc_gemm_pair<MXF8>", "tc_gemm_pair<NVF4>",
                                       "tc_gemm_pair<I8>", "tc_gemm_pair<MXF4>"};
     TraceScope tr(kNames[MODE], s);
-    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, tsa, tsb, p);
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, tsa, tsb, q);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -961,8 +1069,8 @@ cudaError_t launch_mx_gemm_pair(const MxGemmRequest& r, const MxAtoms& at, cudaS
   return launch_pair<kPairMXF8>(ta, tb, ty, tsa, tsb, p, ctx, s, why);
 }
 
-cudaError_t launch_int8_gemm_pair(const Int8Request& r, const void* xb, const void* wbT, int64_t Kp, cudaStream_t s,
-                                  std::string* why) {
+cudaError_t launch_int8_gemm_pair(const Int8Request& r, const void* xb, const void* wbT, int64_t Kp,
+                                  int32_t* split_ws, unsigned* split_cnt, cudaStream_t s, std::string* why) {
   const DeviceCtx* ctx = device_ctx();
   if (!ctx) return cudaErrorInitializationError;
   // The bf16 operands are moved as bytes: a 128-byte K block is 64 codes.
@@ -976,7 +1084,7 @@ cudaError_t launch_int8_gemm_pair(const Int8Request& r, const void* xb, const vo
     return cudaErrorInvalidValue;
   }
   if (!r.acc) tacc = ty;  // not read: store_acc = 0
-  PairParams p{};
+  PairSplitParams p{};
   p.M = static_cast<int>(r.B);
   p.N = static_cast<int>(r.D_out);
   p.K = static_cast<int>(r.D_in);
@@ -991,6 +1099,8 @@ cudaError_t launch_int8_gemm_pair(const Int8Request& r, const void* xb, const vo
   // 16,516,096 < 2^24 in magnitude: every FP32 partial is an exact integer.
   p.chunk = 16;
   p.store_acc = r.acc ? 1 : 0;
+  p.split_ws = split_ws;
+  p.split_cnt = split_cnt;
   p.status = ctx->status;
   p.timeout_ns = wait_timeout_ns();
   // kind::f16: D = F32 (bits 4-5 = 1), A = B = BF16 (bits 7-9, 10-12 = 1), K-major, N = 256, M = 256 (pair).

@@ -162,9 +162,15 @@ size_t int8_workspace_bytes(int64_t B, int64_t D_in, int64_t D_out);
 cudaError_t launch_int8_channel(const Int8Request& r, cudaStream_t s);
 // The exact INT8 matmul on bf16 tensor cores (gemm_pair.cu): xb [B, Kp] and
 // wbT [D_out, Kp] are bf16 codes, K-major, zero beyond D_in (Kp % 64 == 0);
-// writes r.y and, if non-null, r.acc.
-cudaError_t launch_int8_gemm_pair(const Int8Request& r, const void* xb, const void* wbT, int64_t Kp, cudaStream_t s,
-                                  std::string* why);
+// writes r.y and, if non-null, r.acc.  The tiles of its last, partial wave
+// split their K blocks into up to kSplitMax parts over the clusters that
+// would otherwise idle: split_cnt holds kSplitTilesMax x 32 zeroed counters
+// and split_ws int32 tiles of 256 x 256 for int8_split_units(tiles) parts
+// (no split when either is null).
+constexpr int kSplitMax = 4, kSplitTilesMax = 64, kSplitUnitsMax = 128;
+inline int64_t int8_split_units(int64_t tiles) { return tiles * kSplitMax < kSplitUnitsMax ? tiles * kSplitMax : kSplitUnitsMax; }
+cudaError_t launch_int8_gemm_pair(const Int8Request& r, const void* xb, const void* wbT, int64_t Kp,
+                                  int32_t* split_ws, unsigned* split_cnt, cudaStream_t s, std::string* why);
 
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t s);
 cudaError_t launch_selftest_quotient(uint64_t pairs, uint64_t seed, unsigned long long* bad, cudaStream_t s);

@@ -297,7 +297,8 @@ bsmm_status bsmm_gemm_grouped(int64_t M, int64_t N, int64_t K, const void* a, bs
  *            (NULL to skip).
  *   workspace  at least bsmm_int8_channel_workspace_size() bytes (holds
  *            K-padded, K-major copies of both operands' codes for the
- *            matmul).
+ *            matmul, and the int32 partial sums of the tiles whose K range
+ *            the matmul splits over otherwise idle SMs).
  *   Any D_in >= 1 (the matmul's copies are zero-padded to a multiple of
  *   128).  With B == 0 only w is quantized (w_q,
  *   w_scales); x, x_q, x_scales, y and acc are not touched, and the

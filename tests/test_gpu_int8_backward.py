@@ -126,6 +126,33 @@ def test_int8_more_tiles_than_clusters(B, D_in, D_out):
     run_int8(x, w)
 
 
+@pytest.mark.parametrize("B,D_in,D_out", [(1024, 4096, 1280), (2304, 4096, 2304), (1, 5000, 2048)])
+def test_int8_split_tail_tiles_reused_workspace(B, D_in, D_out):
+    """The tiles of the matmul's last, partial wave split K over the idle
+    clusters (76 on GB300): 20 tiles in halves of 32 K blocks (two exact
+    chunks each), 81 tiles with a tail of 5 in quarters of 16, 8 tiles of one
+    row in parts of 32, 32 and 16 K blocks.  Every part leaves its int32 sums in the workspace and the last
+    one of each warp slot adds them, so the workspace is handed over full of
+    garbage and then reused for a second call on other inputs: sums, codes
+    and y must be the oracle's both times."""
+    bsmm = _bsmm()
+    g = np.random.default_rng(B + D_in + D_out)
+    ws = torch.full((bsmm.int8_channel_workspace_size(B, D_in, D_out),), 0xA5, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        x = g.standard_normal((B, D_in)).astype(np.float32)
+        w = g.standard_normal((D_in, D_out)).astype(np.float32)
+        x[B // 2] = 0
+        out = bsmm.int8_channel(torch.from_numpy(x).cuda(), torch.from_numpy(w).cuda(), return_acc=True, workspace=ws)
+        torch.cuda.synchronize()
+        assert bsmm.check_device_status()[0] == 0
+        ref = G.int8_channel(x, w)
+        np.testing.assert_array_equal(out["acc"].cpu().numpy().astype(np.int64), ref["acc"])
+        np.testing.assert_array_equal(out["x_q"].cpu().numpy(), ref["x_q"])
+        np.testing.assert_array_equal(out["w_q"].cpu().numpy(), ref["w_q"])
+        y = out["y"].cpu().numpy().astype(np.float64)
+        assert (np.abs(y - ref["y_ref"]) <= 1e-6 * np.abs(ref["y_ref"])).all()
+
+
 def _bf16(a):
     return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
 
