@@ -761,7 +761,7 @@ TRAFFIC_PER_LAUNCH = {
     W.NVFP4_SQUARE.name: 4_353_200_000,
     W.MXFP4_SQUARE.name: 2_436_300_000,
     W.BACKWARD.name: 3_193_600_000,
-    W.INT8_4096.name: 287_500_000,
+    W.INT8_4096.name: 317_200_000,
 }
 
 
