@@ -282,26 +282,29 @@ class GroupedWork(Work):
                 "sb": torch.empty((p.n // p.group_n, p.k // p.group_k), dtype=torch.float32, device=device),
                 "y": torch.empty((p.m, p.n), dtype=torch.float32, device=device)})
         self.flops = sum(2.0 * it["p"].m * it["p"].n * it["p"].k for it in self.items)
+        # every problem's weight quantization in one call (its 128 x 128 tiles share launches)
+        self.b_jobs = [{"x": it["b_raw"], "block": (it["p"].group_n, it["p"].group_k), "code": "e4m3", "scale": "f32",
+                        "codes": it["bq"], "scales": it["sb"]} for it in self.items]
         self.inputs = [t for it in self.items for t in (it["a_raw"], it["b_raw"])]
         self.outputs = [it["y"] for it in self.items]
 
     def step(self, events=None):
         b = self.bsmm
+        b.quantize_batch(self.b_jobs)
         for it in self.items:
             p = it["p"]
             b.quantize(it["a_raw"], (1, p.group_k), "e4m3", "f32", codes=it["aq"], scales=it["sa"])
-            b.quantize(it["b_raw"], (p.group_n, p.group_k), "e4m3", "f32", codes=it["bq"], scales=it["sb"])
             self._timed(events, 2.0 * p.m * p.n * p.k, lambda: b.gemm_grouped(
                 it["aq"], it["bq"], it["sa"], it["sb"], p.group_n, p.group_k, y=it["y"]))
 
     def quantizer_bytes(self):
         # algorithmic bytes: float32 read, one code byte and the scales written
-        out = []
+        out = [("quant_tile_batch (b, 128x128, every problem's in one launch)", "quant_tile_batch",
+                sum(4 * it["p"].n * it["p"].k + it["p"].n * it["p"].k +
+                    4 * (it["p"].n // it["p"].group_n) * (it["p"].k // it["p"].group_k) for it in self.items))]
         for it in self.items:
             p = it["p"]
             out.append(("quant_rows (a, 1x128)", "quant_rows", 4 * p.m * p.k + p.m * p.k + 4 * p.m * (p.k // p.group_k)))
-            out.append(("quant_tile (b, 128x128)", "quant_tile",
-                        4 * p.n * p.k + p.n * p.k + 4 * (p.n // p.group_n) * (p.k // p.group_k)))
         return out
 
     def quantizer_report(self, launches, steps):

@@ -29,7 +29,7 @@ import os
 import torch
 
 __all__ = [
-    "BsmmError", "lib", "library_path", "quantize", "gemm", "gemm_noalloc", "gemm_grouped", "int8_channel",
+    "BsmmError", "lib", "library_path", "quantize", "quantize_batch", "gemm", "gemm_noalloc", "gemm_grouped", "int8_channel",
     "linear_backward", "gemm_workspace_size", "int8_channel_workspace_size",
     "linear_backward_workspace_size", "check_device_status", "selftest_wait_timeout", "selftest_quotient", "trace",
     "scale_atoms_size", "quantize_atoms", "gemm_atoms", "linear_backward_quantized",
@@ -63,6 +63,15 @@ _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _INT = ctypes.c_int
 _SZ = ctypes.c_size_t
+
+
+class _QuantizeJob(ctypes.Structure):
+    """bsmm_quantize_job (include/bsmm.h)."""
+    _fields_ = [("x", _P), ("x_type", _INT), ("rows", _I64), ("cols", _I64), ("ld_x", _I64),
+                ("block_rows", _INT), ("block_cols", _INT), ("code_type", _INT), ("scale_type", _INT),
+                ("transpose_out", _INT), ("codes", _P), ("ld_codes", _I64), ("scales", _P), ("ld_scales", _I64)]
+
+
 _SIGS = {
     "bsmm_version": ([], _INT),
     "bsmm_last_error": ([], ctypes.c_char_p),
@@ -76,6 +85,7 @@ _SIGS = {
     "bsmm_trace_read": ([_INT, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float),
                          ctypes.POINTER(ctypes.c_float)], _INT),
     "bsmm_quantize": ([_P, _INT, _I64, _I64, _I64, _INT, _INT, _INT, _INT, _INT, _P, _I64, _P, _I64, _P], _INT),
+    "bsmm_quantize_batch": ([ctypes.POINTER(_QuantizeJob), _INT, _P], _INT),
     "bsmm_gemm_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
     "bsmm_gemm": ([_I64, _I64, _I64, _I64, _P, _INT, _P, _INT, _P, _I64, _P, _I64, _INT, _P, _INT, _P, _SZ, _P],
                   _INT),
@@ -235,13 +245,9 @@ class trace:
         return False
 
 
-def quantize(x: torch.Tensor, block, code="e4m3", scale="f32", transpose=False, codes=None, scales=None,
-             stream=None):
-    """Block-quantize a 2-D float32/bfloat16 CUDA tensor.
-
-    Returns ``(codes, scales)``: codes uint8 (int8 for INT8; E2M1 packed two
-    per byte) of shape [rows, cols] (or [cols, rows] transposed), scales
-    float32 or uint8 of shape [rows/br, cols/bc] (or transposed)."""
+def _quantize_job(x, block, code, scale, transpose, codes, scales):
+    """Checked arguments of one quantization, its outputs (allocated where
+    not given) and the C job that describes it."""
     _want(x, "x", dtypes=_FLOATS)
     if x.dim() != 2:
         raise ValueError("x must be a 2-D float32 or bfloat16 tensor")
@@ -261,10 +267,37 @@ def quantize(x: torch.Tensor, block, code="e4m3", scale="f32", transpose=False, 
         codes = torch.empty((orows, width), dtype=torch.int8 if c == INT8 else torch.uint8, device=dev)
     if scales is None:
         scales = torch.empty((srows, scols), dtype=scale_dtype, device=dev)
-    _check(lib().bsmm_quantize(_ptr(x), BF16 if x.dtype == torch.bfloat16 else F32, rows, cols, cols, br, bc, c, s,
-                               1 if transpose else 0, _ptr(codes), ocols, _ptr(scales), scols, _stream(stream)),
-           "bsmm_quantize")
+    job = _QuantizeJob(_ptr(x), BF16 if x.dtype == torch.bfloat16 else F32, rows, cols, cols, br, bc, c, s,
+                       1 if transpose else 0, _ptr(codes), ocols, _ptr(scales), scols)
+    return job, codes, scales
+
+
+def quantize(x: torch.Tensor, block, code="e4m3", scale="f32", transpose=False, codes=None, scales=None,
+             stream=None):
+    """Block-quantize a 2-D float32/bfloat16 CUDA tensor.
+
+    Returns ``(codes, scales)``: codes uint8 (int8 for INT8; E2M1 packed two
+    per byte) of shape [rows, cols] (or [cols, rows] transposed), scales
+    float32 or uint8 of shape [rows/br, cols/bc] (or transposed)."""
+    j, codes, scales = _quantize_job(x, block, code, scale, transpose, codes, scales)
+    _check(lib().bsmm_quantize(j.x, j.x_type, j.rows, j.cols, j.ld_x, j.block_rows, j.block_cols, j.code_type,
+                               j.scale_type, j.transpose_out, j.codes, j.ld_codes, j.scales, j.ld_scales,
+                               _stream(stream)), "bsmm_quantize")
     return codes, scales
+
+
+def quantize_batch(jobs, stream=None):
+    """Several independent quantizations in one call (bsmm_quantize_batch).
+
+    ``jobs`` is a list of dicts with the arguments of :func:`quantize`
+    (``x`` and ``block`` required; ``code``, ``scale``, ``transpose``,
+    ``codes``, ``scales`` optional).  Returns the ``(codes, scales)`` pairs in
+    job order."""
+    prepared = [_quantize_job(j["x"], j["block"], j.get("code", "e4m3"), j.get("scale", "f32"),
+                              j.get("transpose", False), j.get("codes"), j.get("scales")) for j in jobs]
+    arr = (_QuantizeJob * max(len(prepared), 1))(*[p[0] for p in prepared])
+    _check(lib().bsmm_quantize_batch(arr, len(prepared), _stream(stream)), "bsmm_quantize_batch")
+    return [(p[1], p[2]) for p in prepared]
 
 
 # --------------------------------------------------------------------------- #

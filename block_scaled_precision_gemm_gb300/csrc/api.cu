@@ -156,6 +156,46 @@ bsmm_status launched(cudaError_t e, const char* what) {
   return BSMM_OK;
 }
 
+std::string last_error_text() { return t_last_error; }
+
+static_assert(sizeof(void*) != 8 || sizeof(bsmm_quantize_job) == 96, "bsmm_quantize_job layout (the binding mirrors it)");
+
+// One quantization's arguments checked as bsmm_quantize documents them, and
+// turned into a launch request (*empty: a zero-sized job, nothing to do).
+bsmm_status quantize_request(const bsmm_quantize_job& j, QuantRequest* q, bool* empty) {
+  if (j.x_type != BSMM_F32 && j.x_type != BSMM_BF16) return fail(BSMM_ERR_INVALID_ARG, "x_type must be F32 or BF16");
+  if (!is_code(j.code_type)) return fail(BSMM_ERR_INVALID_ARG, "code_type must be E4M3, E5M2, E2M1 or INT8");
+  if (!is_scale(j.scale_type)) return fail(BSMM_ERR_INVALID_ARG, "bad scale_type");
+  if (j.rows < 0 || j.cols < 0) return fail(BSMM_ERR_INVALID_ARG, "negative size");
+  *empty = j.rows == 0 || j.cols == 0;
+  if (*empty) return BSMM_OK;
+  if (!j.x || !j.codes || !j.scales) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
+  if (j.block_rows < 1 || j.block_cols < 1) return fail(BSMM_ERR_INVALID_ARG, "block sizes must be positive");
+  if (j.rows % j.block_rows || j.cols % j.block_cols) return fail(BSMM_ERR_SHAPE, "rows/cols not divisible by the block");
+  if (j.code_type == BSMM_INT8 && j.scale_type != BSMM_SCALE_F32)
+    return fail(BSMM_ERR_UNSUPPORTED, "INT8 codes take F32 scales");
+  if (j.transpose_out && j.block_cols != 1) return fail(BSMM_ERR_UNSUPPORTED, "transposed output needs column blocks");
+  if (j.ld_x < j.cols) return fail(BSMM_ERR_SHAPE, "ld_x < cols");
+  const int64_t out_cols = j.transpose_out ? j.rows : j.cols;
+  if (j.ld_codes < out_cols) return fail(BSMM_ERR_SHAPE, "ld_codes too small");
+  const int64_t s_cols = j.transpose_out ? j.rows / j.block_rows : j.cols / j.block_cols;
+  if (j.ld_scales < s_cols) return fail(BSMM_ERR_SHAPE, "ld_scales too small");
+  if (j.code_type == BSMM_E2M1) {
+    if (j.ld_codes % 2 || out_cols % 2) return fail(BSMM_ERR_SHAPE, "E2M1 codes need an even contiguous extent");
+    // Column blocks written untransposed are packed across lanes by the
+    // column kernels; every other layout packs within one block.
+    const int br = j.block_rows;
+    const bool pow2r = br == 16 || br == 32 || br == 64 || br == 128;
+    const bool paired = !j.transpose_out && j.block_cols == 1 && (pow2r || br == j.rows);
+    const int ext = j.transpose_out ? j.block_rows : j.block_cols;
+    if (ext % 2 && !paired) return fail(BSMM_ERR_UNSUPPORTED, "E2M1 blocks need an even extent along the contiguous axis");
+  }
+  *q = QuantRequest{j.x,         j.x_type == BSMM_BF16, j.rows,   j.cols,   j.ld_x,   j.block_rows,
+                    j.block_cols, j.code_type,          j.scale_type, j.transpose_out != 0, j.codes, j.ld_codes,
+                    j.scales,    j.ld_scales};
+  return BSMM_OK;
+}
+
 // Which kernel a bsmm_gemm problem takes.  The tensor cores scale per 32
 // elements (UE8M0: MXFP8, MXFP4) or 16 (UE4M3 with E2M1: NVFP4); a block that
 // is a multiple of that repeats its scale there.  Any other block size, and
@@ -310,41 +350,37 @@ bsmm_status bsmm_quantize(const void* x, bsmm_dtype x_type, int64_t rows, int64_
                           int block_rows, int block_cols, bsmm_dtype code_type, bsmm_scale_type scale_type,
                           int transpose_out, void* codes, int64_t ld_codes, void* scales, int64_t ld_scales,
                           bsmm_stream_t stream) {
-  if (x_type != BSMM_F32 && x_type != BSMM_BF16) return fail(BSMM_ERR_INVALID_ARG, "x_type must be F32 or BF16");
-  if (!is_code(code_type)) return fail(BSMM_ERR_INVALID_ARG, "code_type must be E4M3, E5M2, E2M1 or INT8");
-  if (!is_scale(scale_type)) return fail(BSMM_ERR_INVALID_ARG, "bad scale_type");
-  if (rows < 0 || cols < 0) return fail(BSMM_ERR_INVALID_ARG, "negative size");
-  if (rows == 0 || cols == 0) {
+  const bsmm_quantize_job j{x,          x_type,     rows,          cols,  ld_x,     block_rows, block_cols,
+                            code_type,  scale_type, transpose_out, codes, ld_codes, scales,     ld_scales};
+  QuantRequest q{};
+  bool empty = false;
+  const bsmm_status st = quantize_request(j, &q, &empty);
+  if (st != BSMM_OK) return st;
+  if (empty) {
     set_error("");
     return BSMM_OK;
   }
-  if (!x || !codes || !scales) return fail(BSMM_ERR_INVALID_ARG, "null pointer");
-  if (block_rows < 1 || block_cols < 1) return fail(BSMM_ERR_INVALID_ARG, "block sizes must be positive");
-  if (rows % block_rows || cols % block_cols) return fail(BSMM_ERR_SHAPE, "rows/cols not divisible by the block");
-  if (code_type == BSMM_INT8 && scale_type != BSMM_SCALE_F32)
-    return fail(BSMM_ERR_UNSUPPORTED, "INT8 codes take F32 scales");
-  if (transpose_out && block_cols != 1) return fail(BSMM_ERR_UNSUPPORTED, "transposed output needs column blocks");
-  if (ld_x < cols) return fail(BSMM_ERR_SHAPE, "ld_x < cols");
-  const int64_t out_cols = transpose_out ? rows : cols, out_rows = transpose_out ? cols : rows;
-  if (ld_codes < out_cols) return fail(BSMM_ERR_SHAPE, "ld_codes too small");
-  const int64_t s_rows = transpose_out ? cols / block_cols : rows / block_rows;
-  const int64_t s_cols = transpose_out ? rows / block_rows : cols / block_cols;
-  if (ld_scales < s_cols) return fail(BSMM_ERR_SHAPE, "ld_scales too small");
-  (void)s_rows;
-  (void)out_rows;
-  if (code_type == BSMM_E2M1) {
-    if (ld_codes % 2 || out_cols % 2) return fail(BSMM_ERR_SHAPE, "E2M1 codes need an even contiguous extent");
-    // Column blocks written untransposed are packed across lanes by the
-    // column kernels; every other layout packs within one block.
-    const bool pow2r = block_rows == 16 || block_rows == 32 || block_rows == 64 || block_rows == 128;
-    const bool paired = !transpose_out && block_cols == 1 && (pow2r || block_rows == rows);
-    const int ext = transpose_out ? block_rows : block_cols;
-    if (ext % 2 && !paired)
-      return fail(BSMM_ERR_UNSUPPORTED, "E2M1 blocks need an even extent along the contiguous axis");
-  }
-  QuantRequest q{x, x_type == BSMM_BF16, rows, cols, ld_x, block_rows, block_cols, code_type, scale_type,
-                 transpose_out != 0, codes, ld_codes, scales, ld_scales};
   return launched(launch_quantize(q, reinterpret_cast<cudaStream_t>(stream)), "quantize launch");
+}
+
+bsmm_status bsmm_quantize_batch(const bsmm_quantize_job* jobs, int count, bsmm_stream_t stream) {
+  if (count < 0) return fail(BSMM_ERR_INVALID_ARG, "negative count");
+  if (count > 0 && !jobs) return fail(BSMM_ERR_INVALID_ARG, "null jobs");
+  std::vector<QuantRequest> q;
+  q.reserve(static_cast<size_t>(count));
+  for (int i = 0; i < count; ++i) {  // every job checked before any launch
+    QuantRequest r{};
+    bool empty = false;
+    const bsmm_status st = quantize_request(jobs[i], &r, &empty);
+    if (st != BSMM_OK) return fail(st, "job " + std::to_string(i) + ": " + last_error_text());
+    if (!empty) q.push_back(r);
+  }
+  if (q.empty()) {
+    set_error("");
+    return BSMM_OK;
+  }
+  return launched(launch_quantize_batch(q.data(), static_cast<int>(q.size()), reinterpret_cast<cudaStream_t>(stream)),
+                  "quantize batch launch");
 }
 
 size_t bsmm_gemm_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K, bsmm_dtype a_type) {

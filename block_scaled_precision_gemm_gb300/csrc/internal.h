@@ -74,6 +74,10 @@ struct QuantRequest {
   int64_t sf_rows = 0, sf_rt = 0, sf_ks4 = 0;
 };
 cudaError_t launch_quantize(const QuantRequest& q, cudaStream_t s);
+// Independent quantizations, all on s (bsmm_quantize_batch): the 128 x 128
+// ones quant_tile takes run as one launch per input type and scale kind,
+// the rest one launch each.
+cudaError_t launch_quantize_batch(const QuantRequest* q, int n, cudaStream_t s);
 // Two quantizations of one bf16 array (qc: 32 x 1 blocks, transposed; qr:
 // 1 x 32 blocks) in a single pass over it where the formats allow, else the
 // two launches.

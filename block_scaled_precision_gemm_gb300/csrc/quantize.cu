@@ -19,6 +19,9 @@
 //   quant_any    one thread per block: every other block shape.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "quotient.cuh"
@@ -764,16 +767,16 @@ __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant_
 // ---------------------------------------------------------------------------
 // 128 x 128 blocks
 // ---------------------------------------------------------------------------
-template <typename In, bool POW2>
 // 512 threads: lane l of warp w owns columns 4l .. 4l+3 of rows w, w+16, ...,
 // w+112, so every load instruction of a warp reads one whole tile row (512
 // bytes of FP32, 256 of bf16) and every store writes that row's 128 codes.
 // Sixteen warps of 32 values each (rather than eight of 64): two CTAs on an
-// SM, so one CTA's loads overlap another's encoding.
-__global__ void __launch_bounds__(512) quant_tile(QP p) {
+// SM, so one CTA's loads overlap another's encoding.  One CTA, tile (ty, tx).
+template <typename In, bool POW2>
+__device__ __forceinline__ void quant_tile_body(const QP& p, int64_t ty, int64_t tx) {
   __shared__ float wmax[16];
   __shared__ Scale tile_sc;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
+  const int64_t r0 = ty * 128, c0 = tx * 128;
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
   const In* x = reinterpret_cast<const In*>(p.x) + (r0 + warp) * p.ld_x + c0 + 4 * lane;
@@ -808,7 +811,7 @@ __global__ void __launch_bounds__(512) quant_tile(QP p) {
     if (lane == 0) {
       const Scale s0 = make_scale(m, p.code, p.scale);
       tile_sc = s0;
-      store_scale(p.scales, blockIdx.y * p.ld_scales + blockIdx.x, p.scale, s0.stored);
+      store_scale(p.scales, ty * p.ld_scales + tx, p.scale, s0.stored);
     }
   }
   __syncthreads();
@@ -828,6 +831,30 @@ __global__ void __launch_bounds__(512) quant_tile(QP p) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) put(k, encode4<POW2>(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], sc, p.code));
   }
+}
+
+template <typename In, bool POW2>
+__global__ void __launch_bounds__(512) quant_tile(QP p) {
+  quant_tile_body<In, POW2>(p, blockIdx.y, blockIdx.x);
+}
+
+// Several 128 x 128 quantizations in one launch: CTA t takes the tile of job
+// j with first[j] <= t < first[j + 1], row-major over that job's tiles.
+constexpr int kTileBatchMax = 16;
+struct QTileBatch {
+  QP p[kTileBatchMax];
+  int64_t first[kTileBatchMax + 1];
+  int64_t tiles_c[kTileBatchMax];
+  int n;
+};
+
+template <typename In, bool POW2>
+__global__ void __launch_bounds__(512) quant_tile_batch(const __grid_constant__ QTileBatch b) {
+  const int64_t t = blockIdx.x;
+  int j = 0;
+  while (j + 1 < b.n && t >= b.first[j + 1]) ++j;
+  const int64_t local = t - b.first[j];
+  quant_tile_body<In, POW2>(b.p[j], local / b.tiles_c[j], local % b.tiles_c[j]);
 }
 
 // ---------------------------------------------------------------------------
@@ -1048,7 +1075,61 @@ QP to_qp(const QuantRequest& q) {
   return QP{q.x, q.rows, q.cols, q.ld_x, q.br, q.bc, q.code, q.scale, q.transpose ? 1 : 0,
             q.codes, q.ld_codes, q.scales, q.ld_scales, q.sf_atoms ? 1 : 0, q.sf_rows, q.sf_rt, q.sf_ks4};
 }
+
+// Whether dispatch() runs p on quant_tile (the earlier branches all need
+// 1-wide blocks or a transposed output).
+template <typename In>
+bool tile_eligible(const QP& p) {
+  const int esz = sizeof(In);
+  const bool x_vec = aligned(p.x, 16) && (p.ld_x * esz) % 16 == 0 && p.cols % (16 / esz) == 0;
+  const bool codes16 = aligned(p.codes, 16) && p.ld_codes % 32 == 0;
+  return p.br == 128 && p.bc == 128 && !p.transpose && x_vec && codes16;
+}
+
+template <typename In, bool POW2>
+cudaError_t launch_tile_batch(const QuantRequest* q, const std::vector<int>& jobs, cudaStream_t s) {
+  for (size_t j0 = 0; j0 < jobs.size(); j0 += kTileBatchMax) {
+    QTileBatch b{};
+    b.n = static_cast<int>(std::min<size_t>(kTileBatchMax, jobs.size() - j0));
+    b.first[0] = 0;
+    for (int k = 0; k < b.n; ++k) {
+      const QuantRequest& r = q[jobs[j0 + k]];
+      b.p[k] = to_qp(r);
+      b.tiles_c[k] = r.cols / 128;
+      b.first[k + 1] = b.first[k] + (r.rows / 128) * (r.cols / 128);
+    }
+    if (b.first[b.n] > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    TraceScope tr("quant_tile_batch", s);
+    quant_tile_batch<In, POW2><<<static_cast<unsigned>(b.first[b.n]), 512, 0, s>>>(b);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 }  // namespace
+
+cudaError_t launch_quantize_batch(const QuantRequest* q, int n, cudaStream_t s) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  // the 128 x 128 jobs quant_tile takes, by input type and scale kind
+  // (f32 / bf16 x divided / power of two); the rest run one launch each
+  std::vector<int> tiles[4];
+  for (int i = 0; i < n; ++i) {
+    const QP p = to_qp(q[i]);
+    const bool ok = q[i].x_bf16 ? tile_eligible<__nv_bfloat16>(p) : tile_eligible<float>(p);
+    if (ok) {
+      tiles[(q[i].x_bf16 ? 2 : 0) + (q[i].scale == BSMM_SCALE_UE8M0 ? 1 : 0)].push_back(i);
+    } else {
+      const cudaError_t e = launch_quantize(q[i], s);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  cudaError_t e = launch_tile_batch<float, false>(q, tiles[0], s);
+  if (e == cudaSuccess) e = launch_tile_batch<float, true>(q, tiles[1], s);
+  if (e == cudaSuccess) e = launch_tile_batch<__nv_bfloat16, false>(q, tiles[2], s);
+  if (e == cudaSuccess) e = launch_tile_batch<__nv_bfloat16, true>(q, tiles[3], s);
+  return e;
+}
 
 cudaError_t launch_quantize_dual(const QuantRequest& qc, const QuantRequest& qr, cudaStream_t s) {
   const DeviceCtx* ctx = device_ctx();

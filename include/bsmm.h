@@ -187,6 +187,39 @@ bsmm_status bsmm_quantize(const void* x, bsmm_dtype x_type, int64_t rows, int64_
                           int64_t ld_codes, void* scales, int64_t ld_scales,
                           bsmm_stream_t stream);
 
+/* Several independent quantizations in one call: the same results as
+ * bsmm_quantize on each job in turn.  block_scaled_mm quantizes a weight
+ * matrix per problem in 128 x 128 tiles; a single such matrix of 2048 x 2048
+ * is too small to keep the GPU busy, so the 128 x 128 jobs that would run
+ * on the tile quantizer share launches (up to 16 jobs a launch, per input
+ * type and per divided / power-of-two scale), and every other job runs as
+ * bsmm_quantize runs it.
+ *
+ *   jobs     count job descriptions (host memory, read during the call);
+ *            each field means what the bsmm_quantize argument of that name
+ *            means.  No job's codes or scales may overlap another job's
+ *            input or output: the order of the jobs' launches is unspecified.
+ *   count    0 is a no-op.
+ *
+ * Errors: every job is checked before anything is launched; the first bad
+ * job's error is returned, its index leading the bsmm_last_error() message.
+ * BSMM_ERR_INVALID_ARG also for count < 0 or a null jobs with count > 0. */
+typedef struct bsmm_quantize_job {
+  const void* x;
+  bsmm_dtype x_type;
+  int64_t rows, cols, ld_x;
+  int block_rows, block_cols;
+  bsmm_dtype code_type;
+  bsmm_scale_type scale_type;
+  int transpose_out;
+  void* codes;
+  int64_t ld_codes;
+  void* scales;
+  int64_t ld_scales;
+} bsmm_quantize_job;
+
+bsmm_status bsmm_quantize_batch(const bsmm_quantize_job* jobs, int count, bsmm_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Batched block-scaled GEMM                                                */
 /* ------------------------------------------------------------------------ */

@@ -185,3 +185,24 @@ def test_trace_and_selftest_argument_checks_without_gpu(lib):
     assert lib.bsmm_trace_stop() == b.OK
     assert lib.bsmm_trace_count() == 0
     assert lib.bsmm_selftest_quotient(16, 1, None, None) == b.ERR_INVALID_ARG
+
+
+def test_quantize_batch_argument_checks_without_gpu(lib):
+    """bsmm_quantize_batch checks every job before it launches anything: a
+    bad count or jobs pointer, then the first bad job by index; zero jobs and
+    zero-sized jobs are no-ops.  The ctypes job matches the C layout (LP64)."""
+    import block_scaled_precision_gemm_gb300 as b
+    J = b._QuantizeJob
+    assert ctypes.sizeof(J) == 96
+    assert lib.bsmm_quantize_batch(None, -1, None) == b.ERR_INVALID_ARG
+    assert lib.bsmm_quantize_batch(None, 1, None) == b.ERR_INVALID_ARG
+    assert lib.bsmm_quantize_batch(None, 0, None) == b.OK
+    ok = J(0x1000, b.F32, 256, 256, 256, 128, 128, b.E4M3, b.SCALE_F32, 0, 0x2000, 256, 0x3000, 2)
+    empty = J(None, b.F32, 0, 256, 256, 128, 128, b.E4M3, b.SCALE_F32, 0, None, 256, None, 2)
+    ragged = J(0x1000, b.F32, 200, 256, 256, 128, 128, b.E4M3, b.SCALE_F32, 0, 0x2000, 256, 0x3000, 2)
+    int8_ue8m0 = J(0x1000, b.F32, 256, 256, 256, 1, 32, b.INT8, b.SCALE_UE8M0, 0, 0x2000, 256, 0x3000, 8)
+    assert lib.bsmm_quantize_batch((J * 1)(empty), 1, None) == b.OK
+    assert lib.bsmm_quantize_batch((J * 3)(ok, empty, ragged), 3, None) == b.ERR_SHAPE
+    assert lib.bsmm_last_error().decode().startswith("job 2:")
+    assert lib.bsmm_quantize_batch((J * 2)(int8_ue8m0, ragged), 2, None) == b.ERR_UNSUPPORTED
+    assert lib.bsmm_last_error().decode().startswith("job 0:")

@@ -182,3 +182,32 @@ def test_int8_channel_codes_on_rounding_ties(B, D_in, D_out):
     np.testing.assert_array_equal(out["x_scales"].cpu().numpy().view(np.uint32), np.asarray(xs, np.float32).view(np.uint32))
     np.testing.assert_array_equal(out["w_scales"].cpu().numpy().view(np.uint32), np.asarray(ws, np.float32).view(np.uint32))
     assert bsmm.check_device_status()[0] == 0
+
+
+def test_quantize_batch_matches_the_oracle():
+    """bsmm_quantize_batch: 20 jobs of 128 x 128 tiles in one input type and
+    scale kind (one launch of 16, one of 4), others of each other kind, and
+    jobs on the other quantizers (row blocks, transposed column blocks, a
+    zero-sized job) in one call; every job's codes and scales bit-exact."""
+    import block_scaled_precision_gemm_gb300 as bsmm
+    specs = [(256 + 128 * (i % 3), 384 - 128 * (i % 2), (128, 128), "e4m3", "f32", "f32", False) for i in range(20)]
+    specs += [(384, 256, (128, 128), "e2m1", "ue4m3", "bf16", False), (256, 256, (128, 128), "e5m2", "ue8m0", "f32", False),
+              (256, 512, (128, 128), "int8", "f32", "bf16", False), (128, 128, (128, 128), "e4m3", "ue8m0", "bf16", False),
+              (160, 384, (1, 32), "e4m3", "ue8m0", "f32", False), (144, 200, (16, 1), "e5m2", "ue8m0", "bf16", True)]
+    xs = [make_x(r, c, 1000 + i, dt) for i, (r, c, _, _, _, dt, _) in enumerate(specs)]
+    jobs = [{"x": x.cuda(), "block": blk, "code": code, "scale": scale, "transpose": tr}
+            for x, (_, _, blk, code, scale, _, tr) in zip(xs, specs)]
+    jobs.insert(3, {"x": torch.empty(0, 256, device="cuda"), "block": (128, 128)})
+    out = bsmm.quantize_batch(jobs)
+    torch.cuda.synchronize()
+    assert bsmm.check_device_status()[0] == 0
+    del out[3]
+    for x, (codes, scales), (_, _, blk, code, scale, _, tr) in zip(xs, out, specs):
+        rc, rs = oracle_quantize(x, blk, code, scale, tr)
+        got_c = codes.cpu().numpy()
+        np.testing.assert_array_equal(got_c.astype(np.int8) if code == "int8" else got_c, rc)
+        got_s = scales.cpu().numpy()
+        if scale == "f32":
+            np.testing.assert_array_equal(got_s.view(np.uint32), np.asarray(rs, np.float32).view(np.uint32))
+        else:
+            np.testing.assert_array_equal(got_s, rs)

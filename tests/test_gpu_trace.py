@@ -38,3 +38,18 @@ def test_quantize_and_gemm_record_in_order():
     assert names[2].startswith("tc_gemm")
     starts = [t0 for _, t0, _ in launches]
     assert starts == sorted(starts)
+
+
+def test_quantize_batch_shares_launches():
+    """Three 128 x 128 jobs of one input type and scale kind run as one
+    quant_tile_batch launch; a job of another kind gets its own, and a row
+    quantization runs as bsmm_quantize runs it."""
+    import block_scaled_precision_gemm_gb300 as bsmm
+    jobs = [{"x": torch.randn(256, 384, device="cuda"), "block": (128, 128)} for _ in range(3)]
+    jobs.append({"x": torch.randn(128, 256, device="cuda").bfloat16(), "block": (128, 128), "scale": "ue8m0"})
+    jobs.append({"x": torch.randn(64, 256, device="cuda"), "block": (1, 128)})
+    bsmm.quantize_batch(jobs)
+    with bsmm.trace() as launches:
+        bsmm.quantize_batch(jobs)
+    names = sorted(n for n, _, _ in launches)
+    assert names == ["quant_rows", "quant_tile_batch", "quant_tile_batch"]
