@@ -759,7 +759,7 @@ def run_gpu(args):
 # nvfp4, mxfp4: the GEMM launch (the scale relayouts add under 1%).
 # backward (5 launches) and int8 (3): the whole call.
 TRAFFIC_PER_LAUNCH = {
-    W.GROUPED_SWEEP.name: 1_997_700_000,
+    W.GROUPED_SWEEP.name: 1_971_700_000,
     W.MXFP8_BATCHED.name: 1_317_400_000,
     W.NVFP4_SQUARE.name: 4_353_200_000,
     W.MXFP4_SQUARE.name: 2_436_300_000,
