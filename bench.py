@@ -512,10 +512,13 @@ class BackwardWork(Work):
         # bf16 read once, E5M2 codes and UE8M0 scales (one per 32) written
         p = self.p
         M, N, K = p.M, p.N, p.K
-        return [("quant_cols_tma2 dual (dY along N and along M)", "quant_cols_tma2 (dual)",
-                 2 * M * N + 2 * (M * N + M * N // 32)),
-                ("quant_cols_tma2 (W along N -> W^T)", "quant_cols_tma2", 2 * N * K + N * K + N * K // 32),
-                ("quant_cols_tma2 (X along M -> X^T)", "quant_cols_tma2", 2 * M * K + M * K + M * K // 32)]
+        dual = ("quant_cols_tma2 dual (dY along N and along M)", "quant_cols_tma2 (dual)",
+                2 * M * N + 2 * (M * N + M * N // 32))
+        wt, xt = 2 * N * K + N * K + N * K // 32, 2 * M * K + M * K + M * K // 32
+        return [[dual, ("quant_cols_tma2 pair (W along N -> W^T and X along M -> X^T)", "quant_cols_tma2 (pair)",
+                        wt + xt)],
+                [dual, ("quant_cols_tma2 (W along N -> W^T)", "quant_cols_tma2", wt),
+                 ("quant_cols_tma2 (X along M -> X^T)", "quant_cols_tma2", xt)]]
 
     def config(self):
         p = self.p

@@ -678,10 +678,11 @@ bsmm_status bsmm_linear_backward(const void* dY, const void* W, const void* X, i
   if (e == cudaSuccess)
     e = atoms_request(dY, true, 1, N, M, true, ft, BSMM_SCALE_UE8M0, dyt, dyt_s, s, &q_dyt);  // dY^T [N, M]
   if (e == cudaSuccess) e = launch_quantize_dual(q_dyt, q_dyn, s);
-  if (e == cudaSuccess)  // W [N,K] along N -> W^T [K, N]
-    e = quantize_to_atoms(W, true, 1, K, N, true, ft, BSMM_SCALE_UE8M0, wt, wt_s, s);
-  if (e == cudaSuccess)  // X [M,K] along M -> X^T [K, M]
-    e = quantize_to_atoms(X, true, 1, K, M, true, ft, BSMM_SCALE_UE8M0, xt, xt_s, s);
+  // W [N,K] along N -> W^T [K, N] and X [M,K] along M -> X^T [K, M], one launch
+  QuantRequest q_wt, q_xt;
+  if (e == cudaSuccess) e = atoms_request(W, true, 1, K, N, true, ft, BSMM_SCALE_UE8M0, wt, wt_s, s, &q_wt);
+  if (e == cudaSuccess) e = atoms_request(X, true, 1, K, M, true, ft, BSMM_SCALE_UE8M0, xt, xt_s, s, &q_xt);
+  if (e == cudaSuccess) e = launch_quantize_pair(q_wt, q_xt, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward quantize launch");
   return backward_gemms(M, N, K, ft, dy_n, dy_n_s, wt, wt_s, dyt, dyt_s, xt, xt_s, true, dX, dW, nullptr, s);
 }

@@ -82,6 +82,10 @@ cudaError_t launch_quantize_batch(const QuantRequest* q, int n, cudaStream_t s);
 // 1 x 32 blocks) in a single pass over it where the formats allow, else the
 // two launches.
 cudaError_t launch_quantize_dual(const QuantRequest& qc, const QuantRequest& qr, cudaStream_t s);
+// Two independent quantizations of bf16 arrays into transposed 32 x 1 blocks
+// (the backward's W^T and X^T) in one launch where both take the TMA-fed
+// column kernel, else the two launches.
+cudaError_t launch_quantize_pair(const QuantRequest& qa, const QuantRequest& qb, cudaStream_t s);
 
 // Block-scaled formats of bsmm_gemm.
 enum MxFormat { kFmtMXF8 = 0, kFmtNVF4 = 1, kFmtMXF4 = 2 };

@@ -606,12 +606,17 @@ constexpr int kCol2TileBytes = kColTileR * kCol2C * 2;  // 32 KB of bf16
 // DUAL: the same tiles are also quantized along their rows (1 x 32 blocks,
 // untransposed output described by p2: codes, scales and their layout), so
 // an array both GEMMs of the backward read along different axes (dY) is
-// read from HBM once.  CODE (E4M3 or E5M2) is fixed at compile time, and
-// block maxima are taken on the bf16 pairs as loaded (packed max of
-// magnitudes): the kernel is bound by instruction issue, not by HBM.
-template <bool POW2, bool DUAL, int CODE>
-__global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant__ CUtensorMap tm, QP p, int tiles_c,
-                                                          int64_t n_tiles, int* status, uint64_t timeout_ns, QP p2) {
+// read from HBM once.  PAIR: p2 (read through tm2, tiles_c2 tiles a row) is
+// a second array quantized like p, its tiles numbered after p's n_a: two
+// arrays in one launch pay its start and its last wave once.  CODE (E4M3 or
+// E5M2) is fixed at compile time, and block maxima are taken on the bf16
+// pairs as loaded (packed max of magnitudes): the kernel is bound by
+// instruction issue, not by HBM.
+template <bool POW2, bool DUAL, bool PAIR, int CODE>
+__global__ void __launch_bounds__(256, 2)
+    quant_cols_tma2(const __grid_constant__ CUtensorMap tm, const __grid_constant__ QP p, int tiles_c, int64_t n_tiles,
+                    int* status, uint64_t timeout_ns, const __grid_constant__ QP p2,
+                    const __grid_constant__ CUtensorMap tm2, int tiles_c2, int64_t n_a) {
   extern __shared__ uint8_t qsm_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 127) & ~uintptr_t(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + kColStages * kCol2TileBytes);
@@ -631,11 +636,14 @@ __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant_
   __syncthreads();
   const int64_t my_n = (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
   auto issue = [&](int64_t i) {  // this CTA's i-th tile into stage i % kColStages
-    const int64_t tt = blockIdx.x + i * gridDim.x;
+    int64_t tt = blockIdx.x + i * gridDim.x;
+    const bool b2 = PAIR && tt >= n_a;
+    if (b2) tt -= n_a;
+    const int tc = b2 ? tiles_c2 : tiles_c;
     const int st = static_cast<int>(i % kColStages);
     mbar_arrive_expect_tx(&full[st], kCol2TileBytes);
-    tma_load_3d(ring + st * kCol2TileBytes, &tm, &full[st], static_cast<int>((tt % tiles_c) * kCol2C),
-                static_cast<int>((tt / tiles_c) * kColTileR), 0);
+    tma_load_3d(ring + st * kCol2TileBytes, b2 ? &tm2 : &tm, &full[st], static_cast<int>((tt % tc) * kCol2C),
+                static_cast<int>((tt / tc) * kColTileR), 0);
   };
   int64_t issued = 0;
   if (t == 0)
@@ -647,11 +655,15 @@ __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant_
     const bool ok = mbar_wait(&full[st], static_cast<uint32_t>(i / kColStages) & 1u, timeout_ns, &abort_flag,
                               status, kSiteQuantTile);
     uint32_t w[32];  // bf16 pairs: rows 32 part + r, columns 2cp (low half) and 2cp+1 (high half)
-    const int64_t tt = blockIdx.x + i * gridDim.x;
-    const int64_t r0 = (tt / tiles_c) * kColTileR;
-    const int64_t c0 = (tt % tiles_c) * kCol2C;
-    const int nr = static_cast<int>(p.rows - r0 < kColTileR ? p.rows - r0 : kColTileR);
-    const int nc = static_cast<int>(p.cols - c0 < kCol2C ? p.cols - c0 : kCol2C);
+    int64_t tt = blockIdx.x + i * gridDim.x;
+    const bool b2 = PAIR && tt >= n_a;
+    if (b2) tt -= n_a;
+    const QP& q = b2 ? p2 : p;  // the array this tile belongs to
+    const int tc = b2 ? tiles_c2 : tiles_c;
+    const int64_t r0 = (tt / tc) * kColTileR;
+    const int64_t c0 = (tt % tc) * kCol2C;
+    const int nr = static_cast<int>(q.rows - r0 < kColTileR ? q.rows - r0 : kColTileR);
+    const int nc = static_cast<int>(q.cols - c0 < kCol2C ? q.cols - c0 : kCol2C);
     if (ok) {
       const uint32_t* tile = reinterpret_cast<const uint32_t*>(ring + st * kCol2TileBytes);
       if constexpr (DUAL) {
@@ -744,12 +756,12 @@ __global__ void __launch_bounds__(256, 2) quant_cols_tma2(const __grid_constant_
       const int idx = t + 256 * k;
       const int c = idx >> 3, ch = idx & 7;
       if (c < nc && ch * 16 < nr)
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.codes) + (c0 + c) * p.ld_codes + r0 + ch * 16) =
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(q.codes) + (c0 + c) * q.ld_codes + r0 + ch * 16) =
             *reinterpret_cast<const uint4*>(ostg + c * kColTileR + ((ch ^ (c & 7)) * 16));
     }
     if (t < nc) {  // this column's scale bytes for the tile's rows (atoms: one word)
       const int nblk = (nr + 31) / 32;
-      uint8_t* dst = reinterpret_cast<uint8_t*>(p.scales) + scale_index(p, c0 + t, r0 / 32);
+      uint8_t* dst = reinterpret_cast<uint8_t*>(q.scales) + scale_index(q, c0 + t, r0 / 32);
       if (nblk == 4 && (reinterpret_cast<uintptr_t>(dst) & 3) == 0)
         *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(&sstg[t][0]);
       else
@@ -967,32 +979,44 @@ __global__ void __launch_bounds__(256) quant_any(QP p) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-template <bool POW2, bool DUAL, int CODE>
+// DUAL: p2 is p's row-block output.  PAIR: p2 is a second array, quantized
+// like p in the same launch.
+template <bool POW2, bool DUAL, bool PAIR, int CODE>
 cudaError_t launch_cols_tma2_code(const QP& p, const DeviceCtx* ctx, cudaStream_t s, const QP& p2) {
-  CUtensorMap tm;
+  CUtensorMap tm, tm2;
   if (!make_tmap_3d(&tm, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.cols, p.rows, 1, kCol2C, kColTileR, false))
     return cudaErrorInvalidValue;
   const int tiles_c = static_cast<int>(ceil_div(p.cols, kCol2C));
-  const int64_t n_tiles = static_cast<int64_t>(tiles_c) * ceil_div(p.rows, kColTileR);
+  const int64_t n_a = static_cast<int64_t>(tiles_c) * ceil_div(p.rows, kColTileR);
+  int tiles_c2 = 0;
+  int64_t n_tiles = n_a;
+  if (PAIR) {
+    if (!make_tmap_3d(&tm2, p2.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p2.cols, p2.rows, 1, kCol2C, kColTileR, false))
+      return cudaErrorInvalidValue;
+    tiles_c2 = static_cast<int>(ceil_div(p2.cols, kCol2C));
+    n_tiles += static_cast<int64_t>(tiles_c2) * ceil_div(p2.rows, kColTileR);
+  } else {
+    tm2 = tm;  // not read
+  }
   const int smem = kColStages * kCol2TileBytes + 128 + kColStages * 8;
   cudaError_t e =
-      cudaFuncSetAttribute(quant_cols_tma2<POW2, DUAL, CODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(quant_cols_tma2<POW2, DUAL, PAIR, CODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(n_tiles, static_cast<int64_t>(ctx->num_sms) * 2);
   {
-    TraceScope tr(DUAL ? "quant_cols_tma2 (dual)" : "quant_cols_tma2", s);
-    quant_cols_tma2<POW2, DUAL, CODE><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
-        tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns(), p2);
+    TraceScope tr(DUAL ? "quant_cols_tma2 (dual)" : (PAIR ? "quant_cols_tma2 (pair)" : "quant_cols_tma2"), s);
+    quant_cols_tma2<POW2, DUAL, PAIR, CODE><<<static_cast<unsigned>(std::max<int64_t>(grid, 1)), 256, smem, s>>>(
+        tm, p, tiles_c, n_tiles, ctx->status, wait_timeout_ns(), p2, tm2, tiles_c2, n_a);
   }
   return cudaGetLastError();
 }
 
 // The 8-bit code formats this kernel takes (E4M3, E5M2), as a template
 // parameter.
-template <bool POW2, bool DUAL = false>
+template <bool POW2, bool DUAL = false, bool PAIR = false>
 cudaError_t launch_cols_tma2(const QP& p, const DeviceCtx* ctx, cudaStream_t s, const QP& p2 = QP{}) {
-  return p.code == BSMM_E4M3 ? launch_cols_tma2_code<POW2, DUAL, BSMM_E4M3>(p, ctx, s, p2)
-                             : launch_cols_tma2_code<POW2, DUAL, BSMM_E5M2>(p, ctx, s, p2);
+  return p.code == BSMM_E4M3 ? launch_cols_tma2_code<POW2, DUAL, PAIR, BSMM_E4M3>(p, ctx, s, p2)
+                             : launch_cols_tma2_code<POW2, DUAL, PAIR, BSMM_E5M2>(p, ctx, s, p2);
 }
 
 template <bool POW2>
@@ -1086,6 +1110,15 @@ bool tile_eligible(const QP& p) {
   return p.br == 128 && p.bc == 128 && !p.transpose && x_vec && codes16;
 }
 
+// Whether dispatch() runs a bf16 p on quant_cols_tma2 (transposed 32 x 1
+// blocks of 8-bit codes with one-byte scales).
+bool cols_tma2_eligible(const QuantRequest& q) {
+  const QP p = to_qp(q);
+  const bool codes16 = aligned(p.codes, 16) && p.ld_codes % 32 == 0;
+  return q.x_bf16 && p.transpose && p.bc == 1 && p.br == 32 && p.code != BSMM_E2M1 && p.code != BSMM_INT8 &&
+         p.scale != BSMM_SCALE_F32 && codes16 && p.ld_x == p.cols && p.cols % 8 == 0 && aligned(p.x, 16);
+}
+
 template <typename In, bool POW2>
 cudaError_t launch_tile_batch(const QuantRequest* q, const std::vector<int>& jobs, cudaStream_t s) {
   for (size_t j0 = 0; j0 < jobs.size(); j0 += kTileBatchMax) {
@@ -1107,6 +1140,20 @@ cudaError_t launch_tile_batch(const QuantRequest* q, const std::vector<int>& job
   return cudaSuccess;
 }
 }  // namespace
+
+cudaError_t launch_quantize_pair(const QuantRequest& qa, const QuantRequest& qb, cudaStream_t s) {
+  const DeviceCtx* ctx = device_ctx();
+  if (!ctx) return cudaErrorInitializationError;
+  const bool eligible = cols_tma2_eligible(qa) && cols_tma2_eligible(qb) && qa.code == qb.code &&
+                        qa.scale == qb.scale;
+  if (!eligible) {
+    const cudaError_t e = launch_quantize(qa, s);
+    return e != cudaSuccess ? e : launch_quantize(qb, s);
+  }
+  const QP pa = to_qp(qa), pb = to_qp(qb);
+  return qa.scale == BSMM_SCALE_UE8M0 ? launch_cols_tma2<true, false, true>(pa, ctx, s, pb)
+                                      : launch_cols_tma2<false, false, true>(pa, ctx, s, pb);
+}
 
 cudaError_t launch_quantize_batch(const QuantRequest* q, int n, cudaStream_t s) {
   const DeviceCtx* ctx = device_ctx();
