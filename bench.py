@@ -766,7 +766,7 @@ TRAFFIC_PER_LAUNCH = {
     W.MXFP8_BATCHED.name: 1_317_400_000,
     W.NVFP4_SQUARE.name: 4_353_200_000,
     W.MXFP4_SQUARE.name: 2_436_300_000,
-    W.BACKWARD.name: 3_193_600_000,
+    W.BACKWARD.name: 3_233_100_000,
     W.INT8_4096.name: 317_200_000,
 }
 
