@@ -6,7 +6,7 @@
 // memory and writes a 128 x 256 FP32 result into each CTA's tensor memory.
 // N = 256 instructions keep the tensor pipe busy (N = 128 ones run it at about
 // half rate), and per SM the operands are 32 KB per 128-byte K block for twice
-// the FLOPs of a 128 x 128 tile on one CTA.  Three modes:
+// the FLOPs of a 128 x 128 tile on one CTA.  Five modes:
 //
 //   kPairF32   y = sum_kb sa[m,kb] * sb[n/128,kb] * (a . b over K block kb)
 //              (atrex-bench #002 block_scaled_mm, Reference Implementation):
@@ -16,6 +16,13 @@
 //              kind::mxf8f6f4.block_scale.block32, UE8M0 scale per 32 K.
 //   kPairNVF4  the same with NVFP4: kind::mxf4nvf4.block_scale.block16, packed
 //              E2M1 operands, UE4M3 scale per 16 K.
+//   kPairMXF4  the same with MXFP4: kind::mxf4nvf4.block_scale.block32, UE8M0.
+//   kPairI8    TensorTonic's INT8 per-channel matmul: int8 codes as bf16
+//              (exact), kind::f16, FP32 partials of 16 K blocks (exact
+//              integers below 2^24) added in int32 by the epilogue, then
+//              y = (acc * s_x) * s_w.  The tiles of the last, partial wave
+//              are split along K over the clusters that would idle; the
+//              parts meet through int32 sums in the workspace.
 // In the block-scaled modes the result accumulates over all of K in one
 // 256-column TMEM buffer; each stage's scale-factor atoms are copied into TMEM
 // with tcgen05.cp.cta_group::2, which moves each CTA's own shared memory into
