@@ -13,7 +13,13 @@
 //                by xor-shuffle; HBM-streaming.
 //   quant_cols   {16,32,64,128} x 1 blocks down the columns; a 128 x 64 tile
 //                staged in shared memory, codes written as is or transposed.
-//   quant_tile   128 x 128 blocks (one scale per tile).
+//   quant_cols_tma, quant_cols_tma2
+//                bf16 columns into transposed 8-bit codes with one-byte
+//                scales, tiles fed by a TMA ring; tma2 (32 x 1 blocks) also
+//                quantizes the same tiles along their rows (DUAL) or a second
+//                array in the same launch (PAIR).
+//   quant_tile   128 x 128 blocks (one scale per tile); quant_tile_batch:
+//                several such quantizations in one launch.
 //   quant_wrow   one block per row (1 x cols).
 //   quant_wcol   one block per column (rows x 1).
 //   quant_any    one thread per block: every other block shape.
