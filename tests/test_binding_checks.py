@@ -45,6 +45,19 @@ def test_quantize_checks():
     refused(bsmm.quantize, f32(4, 64), (1, 32), match=CUDA)
 
 
+def test_quantize_batch_checks():
+    """Each job is checked, in order, as quantize() checks its arguments,
+    before the call reaches the library; a missing required key is refused
+    too."""
+    good = {"x": f32(4, 64), "block": (1, 32)}
+    refused(bsmm.quantize_batch, [{"x": f32(4, 64), "block": (1, 32), "codes": u8(4, 63)}, good],
+            match="codes must have shape")
+    refused(bsmm.quantize_batch, [{"x": f32(4, 64).to(torch.float64), "block": (1, 32)}], match="float32 or")
+    with pytest.raises(KeyError):
+        bsmm.quantize_batch([{"x": f32(4, 64)}])
+    refused(bsmm.quantize_batch, [good], match=CUDA)
+
+
 def test_gemm_checks():
     a, b, sa, sb = u8(2, 128, 256), u8(2, 64, 256), u8(2, 128, 8), u8(2, 64, 8)
     refused(bsmm.gemm, a, u8(2, 64, 255), sa, sb, match="b must have shape \\(2, 64, 256\\)")
