@@ -11,7 +11,9 @@
  *    static device arrays in the loaded module: a 4-byte status word, and the
  *    scratch of bsmm_gemm_noalloc.  Scratch memory a call needs is passed in
  *    as `workspace`; its size comes from the matching *_workspace_size()
- *    query (0 means no workspace is needed).
+ *    query (0 means no workspace is needed).  A workspace holds one call's
+ *    scratch until the call's kernels finish: calls that may run at the
+ *    same time on the GPU (different streams) need workspaces of their own.
  *  - Every call is asynchronous with respect to the host: it validates its
  *    arguments, enqueues kernels on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream) and returns.  Results are ready when the stream
