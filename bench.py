@@ -299,7 +299,7 @@ class GroupedWork(Work):
 
     def quantizer_bytes(self):
         # algorithmic bytes: float32 read, one code byte and the scales written
-        out = [("quant_tile_batch (b, 128x128, every problem's in one launch)", "quant_tile_batch",
+        out = [("quant_tile_batch (b, 128x128, every problem's weight in one launch)", "quant_tile_batch",
                 sum(4 * it["p"].n * it["p"].k + it["p"].n * it["p"].k +
                     4 * (it["p"].n // it["p"].group_n) * (it["p"].k // it["p"].group_k) for it in self.items))]
         for it in self.items:
